@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse top-k GQA attention hot path on GB300.
+
+One step = one pass of the prefill hot path over the 32K causal 'sink'
+workload (B=1, Sq=Skv=32768, Hkv=4, qhead_per_kv=16, topk=16, D=128): k->q CSR
+build + work plan, attention tiles, LSE combine, inputs resident in HBM.
+The metric is effective TFLOP/s = 4 * D * sum over (query, head) of visible
+keys / step time.  The paged-decode sweep (B=32, Sq=8, Hkv=4, qpk=16, topk=16,
+L = 1K..128K, seqused = L-17) is reported alongside in GB/s of algorithmic
+bytes.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Multi-GPU runs (torchrun) process one independent problem per rank (weak
+scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import msa_synth as synth  # noqa: E402
+
+METRIC = "sparse-attn fwd effective TFLOP/s & % bf16 peak; paged decode GB/s & % HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_CSR = 8      # hist, column scan, row scan, scatter, tail fill, plan count, plan scan, plan write
+KERNELS_PER_PARTIAL = 1
+KERNELS_PER_COMBINE = 1
+
+# DRAM traffic of the attention-tile kernel from one ncu capture, keyed by the
+# hash of the source it was measured on (stale -> reported as null).
+PROFILED_TRAFFIC: dict = {}
+
+
+# ---------------------------------------------------------------------------
+# workload arithmetic (measurement only)
+# ---------------------------------------------------------------------------
+
+def visible_keys(q2k: torch.Tensor, Sq: int, kv_len: torch.Tensor, causal: bool, blk: int = 128,
+                 positions: torch.Tensor | None = None) -> torch.Tensor:
+    """Visible keys per (b, h, s): union of the distinct valid blocks, below kv_len, causal limit."""
+    B, Hkv, S, topk = q2k.shape
+    kv = kv_len.to(torch.int64).view(B, 1, 1, 1)
+    ids = q2k.to(torch.int64)
+    nvalid = (kv + blk - 1) // blk
+    valid = (ids >= 0) & (ids < nvalid)
+    srt, _ = torch.sort(torch.where(valid, ids, torch.full_like(ids, -1)), dim=-1)
+    dup = torch.zeros_like(valid)
+    dup[..., 1:] = srt[..., 1:] == srt[..., :-1]
+    keep = (srt >= 0) & ~dup
+    s = torch.arange(S, dtype=torch.int64, device=q2k.device).view(1, 1, S, 1) if positions is None \
+        else positions.to(torch.int64).view(1, 1, S, 1)
+    limit = kv - 1
+    if causal:
+        limit = torch.minimum(limit, s + (kv - Sq))
+    n = torch.clamp(limit - srt * blk + 1, 0, blk)
+    return torch.where(keep, n, torch.zeros_like(n)).sum(-1)
+
+
+def prefill_flops(spec: synth.PrefillSpec, q2k: torch.Tensor) -> float:
+    kv = torch.full((spec.B,), spec.Skv, dtype=torch.int64, device=q2k.device)
+    vis = visible_keys(q2k, spec.Sq, kv, spec.causal)
+    return 4.0 * spec.D * spec.qpk * float(vis.sum())
+
+
+def decode_bytes(spec: synth.DecodeSpec, q2k: torch.Tensor, seqused: torch.Tensor) -> float:
+    """Unique K+V bytes of the union of selected blocks per (b, h), tokens < seqused, plus
+    Q, O, LSE, q2k and the page-table entries of the union."""
+    B, Hkv, Sq, topk = q2k.shape
+    ids = q2k.to(torch.int64).cpu()
+    su = seqused.to(torch.int64).cpu()
+    kv_bytes = 0
+    entries = 0
+    for b in range(B):
+        nvalid = (int(su[b]) + 127) // 128
+        for h in range(Hkv):
+            blocks = {int(j) for j in ids[b, h].flatten().tolist() if 0 <= j < nvalid}
+            entries += len(blocks)
+            for j in blocks:
+                kv_bytes += min(128, int(su[b]) - 128 * j) * spec.D * 2 * 2
+    q_o = 2 * B * Sq * spec.Hq * spec.D * 2
+    return float(kv_bytes + q_o + B * Sq * spec.Hq * 4 + q2k.numel() * 4 + entries * 4)
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_sparse_top_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_rate(spec: synth.PrefillSpec, x_cpu: dict, budget_s: float, seed: int = 7) -> dict:
+    """Times the float64 oracle on a sample of query rows; returns effective TFLOP/s."""
+    import oracle
+    total_q = spec.B * spec.Sq
+    kv = torch.full((spec.B,), spec.Skv, dtype=torch.int64)
+
+    def rows_flops(rows):
+        r = torch.tensor(rows, dtype=torch.int64)
+        b, s = r // spec.Sq, r % spec.Sq
+        sub = x_cpu["q2k"][b, :, s, :].permute(1, 0, 2).unsqueeze(0)  # [1,Hkv,n,topk]
+        vis = visible_keys(sub, spec.Sq, kv[:1], spec.causal, positions=s)
+        return 4.0 * spec.D * spec.qpk * float(vis.sum())
+
+    n = 16
+    while True:
+        rows = synth.sample_query_rows(total_q, n, seed=seed)
+        t0 = time.perf_counter()
+        _, _, threads = oracle.sparse_attn(x_cpu["q"], x_cpu["k"], x_cpu["v"], x_cpu["q2k"], causal=spec.causal,
+                                           rows=rows, return_threads=True)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= total_q:
+            break
+        n = min(total_q, max(n * 2, int(n * budget_s / max(dt, 1e-3) * 1.05)))
+    fl = rows_flops(rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {total_q} query rows (all {spec.Hq} heads), float64, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# main GPU benchmark
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank):
+    import block_sparse_top_gb300 as msa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    spec = synth.C2_SINK32K
+    spec_r = synth.PrefillSpec(**{**spec.__dict__, "seed": spec.seed + rank})
+    x = synth.make_prefill_inputs(spec_r, device=dev)
+    flops = prefill_flops(spec_r, x["q2k"])
+    nominal = 4.0 * spec.D * spec.Hq * spec.Sq * spec.B * spec.topk * 128
+    csr, csr_ws = msa.csr_buffers(spec.B, spec.Hkv, spec.Sq, spec.Skv, spec.topk, spec.qpk, dev)
+    fwd_ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, dev)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((spec.B, spec.Sq, spec.Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        msa.build_k2q_csr(x["q2k"], spec.Skv, spec.qpk, out=csr, workspace=csr_ws)
+        if ev is not None:
+            ev[1].record(stream)
+        msa.sparse_attn_fwd_partial(x["q"], x["k"], x["v"], csr, causal=True, workspace=fwd_ws)
+        if ev is not None:
+            ev[2].record(stream)
+        msa.sparse_attn_combine(csr, spec.Hq, out, lse, fwd_ws)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    total_ms = start.elapsed_time(stop)
+    csr_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    comb_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    step_ms = total_ms / K
+    step_ms_max = reduce_max(step_ms, world)
+    flops_all = reduce_sum(flops, world)
+    value = flops_all / (step_ms_max * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers: H2D inputs, step, D2H outputs
+    host = {k_: v_.cpu().pin_memory() for k_, v_ in x.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dev_in = {k_: torch.empty_like(v_) for k_, v_ in x.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def e2e_step():
+        for k_ in dev_in:
+            dev_in[k_].copy_(host[k_], non_blocking=True)
+        msa.build_k2q_csr(dev_in["q2k"], spec.Skv, spec.qpk, out=csr, workspace=csr_ws)
+        msa.sparse_attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], csr, causal=True, out=out, lse=lse,
+                            workspace=fwd_ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(3, min(K, 20))
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / Ke, world)
+    e2e_val = flops_all / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    long_region = total_ms > 2000
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    khash = source_hash("attn.cu", "attn_mma.cuh", "common.cuh")
+    traffic = PROFILED_TRAFFIC.get(khash)
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
+                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": True,
+                   "pattern": "sink", "per_rank_problem": "independent (seed + rank)",
+                   "l2": "inputs larger than L2 (Q 512 MiB, split partials 8.6 GB per step); no flush"},
+        "breakdown_ms": {"csr_build_and_plan": round(csr_ms, 4), "attention_tiles": round(attn_ms, 4),
+                         "lse_combine": round(comb_ms, 4)},
+        "effective_flop_per_step": flops, "nominal_tflops": round(nominal / (step_ms_max * 1e-3) / 1e12, 3),
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": K * (KERNELS_PER_CSR + KERNELS_PER_PARTIAL + KERNELS_PER_COMBINE),
+        "roofline": {"bound": "tensor", "kernel": "attention tiles (msa_sparse_attn_fwd_partial)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 {'sustained' if long_region else 'burst'}",
+                     "kernel_source_hash": khash},
+    }
+    if not args.no_decode:
+        result["decode"] = decode_sweep(args, dev, peaks, peak_src)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        x_cpu = {k_: v_.cpu() for k_, v_ in x.items()}
+        result["cpu_baseline"] = oracle_rate(spec, x_cpu, args.cpu_budget)
+    return result
+
+
+def decode_sweep(args, dev, peaks, peak_src):
+    import block_sparse_top_gb300 as msa
+    out = []
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2, rewritten between calls
+    for L in args.decode_L:
+        spec = synth.c3_decode(L)
+        d = synth.make_decode_inputs(spec, device=dev)
+        nbytes = decode_bytes(spec, d["q2k"], d["seqused"])
+        o = torch.empty_like(d["q"])
+        lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        ws = msa.paged_workspace(spec.B, spec.Sq, spec.Hq, spec.Hkv, spec.topk, spec.pages_per_seq, dev)
+
+        def call():
+            msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], d["q2k"],
+                                      out=o, lse=lse, workspace=ws)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        times = []
+        n = 30
+        for _ in range(n):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        us = statistics.median(times) * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out.append({"L": L, "us": round(us, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "bytes": nbytes, "launches_per_call": 2})
+        del d
+        torch.cuda.empty_cache()
+    return {"unit": "GB/s", "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
+            "timing": "median of 30 single calls, L2 flushed (512 MiB write) before each", "sweep": out}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    spec = synth.C2_SINK32K
+    x_cpu = synth.make_prefill_inputs(spec, device="cuda" if torch.cuda.is_available() else "cpu")
+    x_cpu = {k_: v_.cpu() for k_, v_ in x_cpu.items()}
+    per_step = max(0.2, args.ref_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(spec, x_cpu, per_step)
+    vals = []
+    last = None
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        last = oracle_rate(spec, x_cpu, per_step, seed=100 + i)
+        vals.append(last["value"])
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
+                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "causal": True, "pattern": "sink"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": f"per step: {last['sample']}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-L", type=int, nargs="*", default=[1024, 8192, 32768, 131072])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=150.0, help="seconds for the whole reference arm")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, _ = dist_setup()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args, world, rank)
+        print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, world, rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

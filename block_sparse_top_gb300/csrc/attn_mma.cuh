@@ -1,0 +1,112 @@
+// attn_mma.cuh -- warp-level bf16 MMA helpers (mma.sync m16n8k16, ldmatrix) on
+// XOR-swizzled 128 x 128 bf16 shared-memory tiles (row = 256 B = 16 chunks of
+// 16 B; chunk c of row r is stored at chunk c ^ (r & 7)).
+#pragma once
+#include "common.cuh"
+
+namespace msa {
+
+__device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
+    return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// S[16 x 128] = Q_rows[16 x 128] . K[128 x 128]^T for the warp's 16 query
+// rows starting at `row0` of the Q tile; acc[nt][4] in the m16n8 C layout.
+__device__ __forceinline__ void warp_qk(uint32_t q_base, uint32_t k_base, int row0, float (&acc)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        int arow = row0 + (lane & 15);
+        int achunk = 2 * kk + (lane >> 4);
+        ldsm_x4(q_base + swz_off(arow, achunk), a0, a1, a2, a3);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t b0, b1, b2, b3;
+            int brow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            int bchunk = 2 * kk + ((lane >> 3) & 1);
+            ldsm_x4(k_base + swz_off(brow, bchunk), b0, b1, b2, b3);
+            mma_bf16(acc[2 * np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+
+// O[16 x 128] += P[16 x 128 keys] . V[128 keys x 128 d]; P given as the S
+// accumulator layout already converted to bf16 pairs: pk[nt][0] = row g,
+// pk[nt][1] = row g + 8 (keys 8nt + 2t, +1).
+__device__ __forceinline__ void warp_pv(uint32_t v_base, const uint32_t (&pk)[16][2], float (&o)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0 = pk[2 * kk][0], a1 = pk[2 * kk][1], a2 = pk[2 * kk + 1][0], a3 = pk[2 * kk + 1][1];
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+            uint32_t b0, b1, b2, b3;
+            int vrow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            int vchunk = 2 * dp + (lane >> 4);
+            ldsm_x4_t(v_base + swz_off(vrow, vchunk), b0, b1, b2, b3);
+            mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
+            mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+
+// e4m3 (fn) byte -> float, exact.
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+    uint32_t e = (b >> 3) & 0xF, m = b & 7;
+    float v = (e == 0) ? (float)m * (1.0f / 512.0f) : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (b & 0x80) ? -v : v;
+}
+
+// e2m1 code (4 bits) -> float.
+__device__ __forceinline__ float e2m1_to_float(uint32_t c) {
+    // magnitudes 0, .5, 1, 1.5 (m < 4) and 2, 3, 4, 6 (m >= 4)
+    const uint32_t m = c & 7;
+    float v = (m < 4) ? 0.5f * (float)m : (float)(1u << ((m >> 1) - 1)) * (1.0f + 0.5f * (float)(m & 1));
+    return (c & 8) ? -v : v;
+}
+
+// Dequantises 16 NVFP4 values (8 packed bytes, one e4m3 scale) into 16 bf16
+// (two 16-byte chunks).  Each product is exact in bf16.
+__device__ __forceinline__ void nvfp4_group_to_bf16(uint2 packed, uint32_t scale_byte, uint4 &lo, uint4 &hi) {
+    float s = e4m3_to_float(scale_byte);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t byte = ((i < 4 ? packed.x : packed.y) >> (8 * (i & 3))) & 0xFF;
+        w[i] = pack_bf16x2(e2m1_to_float(byte & 0xF) * s, e2m1_to_float(byte >> 4) * s);
+    }
+    lo = make_uint4(w[0], w[1], w[2], w[3]);
+    hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+}  // namespace msa

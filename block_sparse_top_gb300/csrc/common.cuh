@@ -1,0 +1,95 @@
+// common.cuh -- shared device/host helpers of libmsa (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+#define MSA_CUDA_TRY(expr)                                  \
+    do {                                                    \
+        cudaError_t _e = (expr);                            \
+        if (_e != cudaSuccess) return MSA_ERR_CUDA;         \
+    } while (0)
+
+#define MSA_LAUNCH_CHECK()                                  \
+    do {                                                    \
+        if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA; \
+    } while (0)
+
+namespace msa {
+
+constexpr int kBlk = 128;      // KV block = page = 128 tokens
+constexpr int kD = 128;        // head dimension
+constexpr int kMaxNblk = 8192; // CSR builder bitmap limit (blocks per sequence)
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool supported_topk(int t) { return t == 4 || t == 8 || t == 16 || t == 32; }
+inline bool supported_qpk(int q) { return q == 1 || q == 2 || q == 4 || q == 8 || q == 16; }
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device status word (OR of MSA_STATUS_* bits); tolerates a null pointer.
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Work plan shared by the CSR builder (writer) and the prefill kernel (reader)
+// ---------------------------------------------------------------------------
+// A unit is (KV head, CSR row, first q_indices position, query count); its
+// queries are processed in chunks of 128/qhead_per_kv queries, 128 rows each.
+struct PlanHeader {
+    int32_t work_count;  // units written (device side, no host readback)
+    int32_t capacity;    // units the buffer holds
+    int32_t qhead_per_kv;
+    int32_t q_per_unit;
+    int32_t reserved[12];
+};
+static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
+
+struct PlanUnit {
+    int32_t head;   // KV head h
+    int32_t row;    // global CSR row r = b*nblk + j
+    int32_t start;  // first position in q_indices[h]
+    int32_t count;  // queries in this unit
+};
+
+inline int q_per_chunk(int qpk) { return 128 / qpk; }
+// Queries per unit: 8 chunks (K/V block loaded once per unit).
+inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
+
+inline int64_t plan_capacity(int B, int Hkv, int Sq, int Skv, int topk, int qpk) {
+    int64_t nblk = ceil_div(Skv, kBlk);
+    int64_t rows = (int64_t)B * nblk;
+    int64_t per_head = rows + ceil_div((int64_t)B * Sq * topk, q_per_unit(qpk));
+    return per_head * Hkv;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared async copy (L2 only), optionally zero-filled.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid = true) {
+    int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+}  // namespace msa

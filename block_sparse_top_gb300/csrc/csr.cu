@@ -1,0 +1,358 @@
+// csr.cu -- deterministic k->q CSR inversion and the prefill work plan.
+//
+// Source: interface.py module docstring (q2k [Hkv,total_q,topK] is inverted
+// into k2q_row_ptr [Hkv,total_rows+1] and k2q_q_indices [Hkv,total_q*topK])
+// and test_sparse_atten.py test_scheduler_builds_packed_qsplit_metadata /
+// test_k2q_csr_builder_matches_torch_reference (bit-exact CSR, packed
+// q | split << 24, work items bounded by the per-CTA query target, every row
+// covered).
+//
+// Three passes over tiles of 128 queries of one (sequence, KV head):
+//   1. hist: a 128-bit mask per KV block (bit i = query i of the tile names
+//      the block) built in shared memory; per-tile counts written out.
+//   2. scan: per block, exclusive scan of the tile counts (tile offsets inside
+//      the row) and row totals; then per head an inclusive scan of the row
+//      totals gives row_ptr.
+//   3. scatter: position = row_ptr + tile offset + popcount of the mask bits
+//      below the query, so each row lists its queries in ascending order with
+//      no atomics on positions (bit-deterministic).
+// The plan then cuts every row into units of at most 8 chunks of 128 rows.
+#include "common.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kTileQ = 128;  // queries per CSR tile (4 x 32-bit mask words)
+
+struct CsrShape {
+    int B, Hkv, Sq, Skv, topk, nblk, ntiles;
+    int64_t rows, cap;
+};
+
+// Validity of one slot: 0 <= j < nvalid and not named by an earlier slot.
+__device__ __forceinline__ bool slot_valid(const int32_t *sel, int t, int nvalid, uint32_t *status) {
+    int j = sel[t];
+    if (j < 0) return false;
+    if (j >= nvalid) {
+        set_status(status, MSA_STATUS_INDEX_RANGE);
+        return false;
+    }
+    for (int u = 0; u < t; ++u)
+        if (sel[u] == j) {
+            set_status(status, MSA_STATUS_DUPLICATE);
+            return false;
+        }
+    return true;
+}
+
+__device__ __forceinline__ int seq_nvalid(const int32_t *seqused, int b, int Skv, int nblk) {
+    int64_t kv = seqused ? (int64_t)seqused[b] : (int64_t)Skv;
+    int64_t n = ceil_div(kv, kBlk);
+    if (n > nblk) n = nblk;
+    if (n < 0) n = 0;
+    return (int)n;
+}
+
+// Builds the per-block query masks of one tile in shared memory.
+__device__ void build_masks(uint32_t *masks, const int32_t *q2k, const int32_t *seqused, const CsrShape &s,
+                            int tile, int b, int h, uint32_t *status, int32_t *split_counts) {
+    for (int i = threadIdx.x; i < s.nblk * 4; i += blockDim.x) masks[i] = 0u;
+    __syncthreads();
+    int i = threadIdx.x;
+    int sq = tile * kTileQ + i;
+    if (sq < s.Sq) {
+        int nvalid = seq_nvalid(seqused, b, s.Skv, s.nblk);
+        const int32_t *sel = q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sq) * s.topk;
+        int cnt = 0;
+        for (int t = 0; t < s.topk; ++t) {
+            if (!slot_valid(sel, t, nvalid, status)) continue;
+            atomicOr(&masks[sel[t] * 4 + (i >> 5)], 1u << (i & 31));
+            ++cnt;
+        }
+        if (split_counts) split_counts[((int64_t)b * s.Sq + sq) * s.Hkv + h] = cnt;
+    }
+    __syncthreads();
+}
+
+__global__ void csr_hist_kernel(const int32_t *__restrict__ q2k, const int32_t *__restrict__ seqused, CsrShape s,
+                                int32_t *__restrict__ tile_counts, int32_t *__restrict__ split_counts,
+                                uint32_t *status) {
+    extern __shared__ uint32_t masks[];
+    int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+    build_masks(masks, q2k, seqused, s, tile, b, h, status, split_counts);
+    int32_t *out = tile_counts + (((int64_t)h * s.B + b) * s.ntiles + tile) * s.nblk;
+    for (int j = threadIdx.x; j < s.nblk; j += blockDim.x) {
+        const uint32_t *m = masks + j * 4;
+        out[j] = __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+    }
+}
+
+// Column scan: for each (h, b, j) turn the tile counts into exclusive offsets
+// within the row and write the row total to row_ptr[h][b*nblk + j + 1].
+// Block (32, 32): threadIdx.x = block id offset, threadIdx.y = tile range.
+__global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_ptr, CsrShape s) {
+    __shared__ int32_t part[32][33];
+    int j = blockIdx.x * 32 + threadIdx.x;
+    int b = blockIdx.y, h = blockIdx.z;
+    int per = (s.ntiles + 31) / 32;
+    int t0 = threadIdx.y * per;
+    int t1 = min(t0 + per, s.ntiles);
+    int32_t *base = tile_counts + ((int64_t)h * s.B + b) * s.ntiles * (int64_t)s.nblk;
+    int32_t sum = 0;
+    if (j < s.nblk)
+        for (int t = t0; t < t1; ++t) sum += base[(int64_t)t * s.nblk + j];
+    part[threadIdx.y][threadIdx.x] = sum;
+    __syncthreads();
+    if (threadIdx.y == 0) {
+        int32_t run = 0;
+        for (int y = 0; y < 32; ++y) {
+            int32_t v = part[y][threadIdx.x];
+            part[y][threadIdx.x] = run;
+            run += v;
+        }
+        if (j < s.nblk) row_ptr[(int64_t)h * (s.rows + 1) + (int64_t)b * s.nblk + j + 1] = run;
+    }
+    __syncthreads();
+    if (j < s.nblk) {
+        int32_t run = part[threadIdx.y][threadIdx.x];
+        for (int t = t0; t < t1; ++t) {
+            int32_t v = base[(int64_t)t * s.nblk + j];
+            base[(int64_t)t * s.nblk + j] = run;
+            run += v;
+        }
+    }
+}
+
+// In-place scan of n int32 per blockIdx.x segment (segment stride `stride`),
+// one CTA of 1024 threads per segment.  exclusive != 0: out[i] = sum_{<i};
+// the segment total goes to totals[blockIdx.x] when totals != nullptr.
+__global__ void segment_scan_kernel(int32_t *data, int64_t n, int64_t stride, int exclusive, int32_t *totals) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry_s;
+    int32_t *d = data + blockIdx.x * stride;
+    if (threadIdx.x == 0) carry_s = 0;
+    __syncthreads();
+    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t base = 0; base < n; base += blockDim.x) {
+        int64_t i = base + threadIdx.x;
+        int32_t v = (i < n) ? d[i] : 0;
+        int32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        int32_t carry = carry_s;
+        int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+        if (i < n) d[i] = exclusive ? incl - v : incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry_s = incl;
+        __syncthreads();
+    }
+    if (totals && threadIdx.x == 0) totals[blockIdx.x] = carry_s;
+}
+
+__global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_t *__restrict__ seqused, CsrShape s,
+                                   const int32_t *__restrict__ tile_off, const int32_t *__restrict__ row_ptr,
+                                   int32_t *__restrict__ q_indices, int32_t *__restrict__ qsplit) {
+    extern __shared__ uint32_t masks[];
+    int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+    build_masks(masks, q2k, seqused, s, tile, b, h, nullptr, nullptr);
+    int i = threadIdx.x;
+    int sq = tile * kTileQ + i;
+    if (sq >= s.Sq) return;
+    int nvalid = seq_nvalid(seqused, b, s.Skv, s.nblk);
+    const int32_t *sel = q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sq) * s.topk;
+    const int32_t *off = tile_off + (((int64_t)h * s.B + b) * s.ntiles + tile) * s.nblk;
+    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1) + (int64_t)b * s.nblk;
+    int32_t *qi = q_indices + (int64_t)h * s.cap;
+    int32_t *qs = qsplit + (int64_t)h * s.cap;
+    int32_t gq = (int32_t)((int64_t)b * s.Sq + sq);
+    int w = i >> 5;
+    uint32_t below = (1u << (i & 31)) - 1u;
+    int rank = 0;
+    for (int t = 0; t < s.topk; ++t) {
+        if (!slot_valid(sel, t, nvalid, nullptr)) continue;
+        int j = sel[t];
+        const uint32_t *m = masks + j * 4;
+        int r = __popc(m[w] & below);
+        for (int x = 0; x < w; ++x) r += __popc(m[x]);
+        int64_t pos = (int64_t)rp[j] + off[j] + r;
+        qi[pos] = gq;
+        qs[pos] = gq | (rank << 24);
+        ++rank;
+    }
+}
+
+__global__ void csr_tail_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int32_t *__restrict__ q_indices,
+                                int32_t *__restrict__ qsplit) {
+    int h = blockIdx.y;
+    int64_t nnz = row_ptr[(int64_t)h * (s.rows + 1) + s.rows];
+    for (int64_t i = nnz + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < s.cap;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        q_indices[(int64_t)h * s.cap + i] = -1;
+        qsplit[(int64_t)h * s.cap + i] = -1;
+    }
+}
+
+// Units per (h, row): ceil(count / q_per_unit).
+__global__ void plan_count_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int qpu,
+                                  int32_t *__restrict__ units_per_row) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)s.Hkv * s.rows) return;
+    int h = (int)(idx / s.rows);
+    int64_t r = idx % s.rows;
+    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
+    int32_t c = rp[r + 1] - rp[r];
+    units_per_row[idx] = (c + qpu - 1) / qpu;
+}
+
+__global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int qpu,
+                                  const int32_t *__restrict__ unit_off, const int32_t *__restrict__ total,
+                                  PlanHeader *plan, PlanUnit *units, int capacity, int qpk, uint32_t *status) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx == 0) {
+        int32_t tot = *total;
+        if (tot > capacity) {
+            set_status(status, MSA_STATUS_PLAN_OVERFLOW);
+            tot = capacity;
+        }
+        plan->work_count = tot;
+        plan->capacity = capacity;
+        plan->qhead_per_kv = qpk;
+        plan->q_per_unit = qpu;
+    }
+    if (idx >= (int64_t)s.Hkv * s.rows) return;
+    int h = (int)(idx / s.rows);
+    int64_t r = idx % s.rows;
+    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
+    int32_t begin = rp[r], c = rp[r + 1] - begin;
+    int32_t u0 = unit_off[idx];
+    for (int32_t u = 0; u * qpu < c; ++u) {
+        if (u0 + u >= capacity) break;
+        PlanUnit pu;
+        pu.head = h;
+        pu.row = (int32_t)r;
+        pu.start = begin + u * qpu;
+        pu.count = min(qpu, c - u * qpu);
+        units[u0 + u] = pu;
+    }
+}
+
+CsrShape make_shape(int B, int Hkv, int Sq, int Skv, int topk) {
+    CsrShape s;
+    s.B = B; s.Hkv = Hkv; s.Sq = Sq; s.Skv = Skv; s.topk = topk;
+    s.nblk = (int)ceil_div(Skv, kBlk);
+    s.ntiles = (int)ceil_div(Sq, kTileQ);
+    s.rows = (int64_t)B * s.nblk;
+    s.cap = (int64_t)B * Sq * topk;
+    return s;
+}
+
+struct CsrWorkspace {
+    size_t tile_counts, units_per_row, total, bytes;
+};
+
+CsrWorkspace csr_workspace_layout(const CsrShape &s) {
+    CsrWorkspace w;
+    size_t off = 0;
+    w.tile_counts = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)s.Hkv * s.B * s.ntiles * s.nblk, 256);
+    w.units_per_row = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)s.Hkv * s.rows, 256);
+    w.total = off;
+    off = align_up(off + 256, 256);
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" size_t msa_k2q_csr_workspace_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv) {
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk) return 0;
+    return csr_workspace_layout(make_shape(B, Hkv, Sq, Skv, topk)).bytes;
+}
+
+extern "C" size_t msa_plan_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv, int qhead_per_kv) {
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk || !supported_qpk(qhead_per_kv))
+        return 0;
+    return sizeof(PlanHeader) + sizeof(PlanUnit) * (size_t)plan_capacity(B, Hkv, Sq, Skv, topk, qhead_per_kv);
+}
+
+extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, int topk, int blk_kv,
+                                 int qhead_per_kv, const int32_t *seqused, int32_t *row_ptr, int32_t *q_indices,
+                                 int32_t *qsplit, int32_t *split_counts, void *plan, size_t plan_bytes,
+                                 void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
+    if (!q2k || !row_ptr || !q_indices || !qsplit || !split_counts || !workspace) return MSA_ERR_INVALID_ARG;
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0) return MSA_ERR_INVALID_ARG;
+    if (blk_kv != kBlk || !supported_topk(topk) || !supported_qpk(qhead_per_kv)) return MSA_ERR_UNSUPPORTED;
+    if ((int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
+    CsrShape s = make_shape(B, Hkv, Sq, Skv, topk);
+    if (s.nblk > kMaxNblk) return MSA_ERR_UNSUPPORTED;
+    CsrWorkspace w = csr_workspace_layout(s);
+    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
+    if (plan && (plan_bytes < msa_plan_size(B, Hkv, Sq, Skv, topk, blk_kv, qhead_per_kv) || !aligned(plan, 16)))
+        return MSA_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    int32_t *tile_counts = reinterpret_cast<int32_t *>(ws + w.tile_counts);
+
+    size_t mask_smem = sizeof(uint32_t) * 4 * (size_t)s.nblk;
+    static bool smem_set = false;
+    if (!smem_set) {
+        MSA_CUDA_TRY(cudaFuncSetAttribute(csr_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          sizeof(uint32_t) * 4 * kMaxNblk));
+        MSA_CUDA_TRY(cudaFuncSetAttribute(csr_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          sizeof(uint32_t) * 4 * kMaxNblk));
+        smem_set = true;
+    }
+    dim3 tgrid(s.ntiles, B, Hkv);
+    csr_hist_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, split_counts, status_dev);
+    MSA_LAUNCH_CHECK();
+    dim3 cgrid((unsigned)ceil_div(s.nblk, 32), B, Hkv);
+    csr_colscan_kernel<<<cgrid, dim3(32, 32), 0, stream>>>(tile_counts, row_ptr, s);
+    MSA_LAUNCH_CHECK();
+    // row_ptr[h][0] = 0, then inclusive scan of the row totals in [1, rows]
+    MSA_CUDA_TRY(cudaMemset2DAsync(row_ptr, sizeof(int32_t) * (s.rows + 1), 0, sizeof(int32_t), Hkv, stream));
+    segment_scan_kernel<<<Hkv, 1024, 0, stream>>>(row_ptr + 1, s.rows, s.rows + 1, 0, nullptr);
+    MSA_LAUNCH_CHECK();
+    csr_scatter_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, row_ptr, q_indices,
+                                                             qsplit);
+    MSA_LAUNCH_CHECK();
+    int tail_blocks = (int)std::min<int64_t>(ceil_div(s.cap, 256), 1024);
+    csr_tail_kernel<<<dim3(tail_blocks, Hkv), 256, 0, stream>>>(row_ptr, s, q_indices, qsplit);
+    MSA_LAUNCH_CHECK();
+
+    if (plan) {
+        int qpu = q_per_unit(qhead_per_kv);
+        int32_t *upr = reinterpret_cast<int32_t *>(ws + w.units_per_row);
+        int32_t *total = reinterpret_cast<int32_t *>(ws + w.total);
+        int64_t n = (int64_t)Hkv * s.rows;
+        int blocks = (int)ceil_div(n, 256);
+        plan_count_kernel<<<blocks, 256, 0, stream>>>(row_ptr, s, qpu, upr);
+        MSA_LAUNCH_CHECK();
+        segment_scan_kernel<<<1, 1024, 0, stream>>>(upr, n, 0, 1, total);
+        MSA_LAUNCH_CHECK();
+        PlanHeader *ph = static_cast<PlanHeader *>(plan);
+        PlanUnit *units = reinterpret_cast<PlanUnit *>(ph + 1);
+        int capacity = (int)plan_capacity(B, Hkv, Sq, Skv, topk, qhead_per_kv);
+        plan_write_kernel<<<blocks, 256, 0, stream>>>(row_ptr, s, qpu, upr, total, ph, units, capacity,
+                                                      qhead_per_kv, status_dev);
+        MSA_LAUNCH_CHECK();
+    }
+    return MSA_OK;
+}
