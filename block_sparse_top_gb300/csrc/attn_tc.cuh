@@ -146,6 +146,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             for (int c = 0; c < x.nch; ++c, ++ci) {
                 const int qs = ci % kNQ;
                 bool mine = true;
+                if (c == 0 && ci >= 1) {
+                    // Publish the previous chunk before any wait on the K/V
+                    // buffer: that wait can depend (through the MMA issue
+                    // order) on the previous chunk's S MMA.
+                    cp_async_wait<0>();
+                    tc::fence_proxy_async();
+                    tc::mbar_arrive(bar(Q_FULL + (ci - 1) % kNQ));
+                }
                 if (c == 0) {
                     if (KV_FORMAT == MSA_KV_BF16) {
                         if (tid == 0) {
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     cp_async16(qt + (ch >> 3) * 16384 + tc::sw128_off(R, ch & 7), src, gq >= 0);
                 }
                 cp_async_commit();
-                if (ci >= 1) {
+                if (c >= 1) {
                     cp_async_wait<1>();
                     tc::fence_proxy_async();
                     tc::mbar_arrive(bar(Q_FULL + (ci - 1) % kNQ));

@@ -46,7 +46,9 @@ struct PlanHeader {
     int32_t capacity;    // units the buffer holds
     int32_t qhead_per_kv;
     int32_t q_per_unit;
-    int32_t reserved[12];
+    int32_t wave_queries;  // queries per wave (units are ordered wave-major)
+    int32_t nwaves;
+    int32_t reserved[10];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
@@ -61,10 +63,27 @@ inline int q_per_chunk(int qpk) { return 128 / qpk; }
 // Queries per unit: 8 chunks (K/V block loaded once per unit).
 inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
 
+// Queries per wave: the Q rows of one wave (all heads) fill about 32 MiB, so
+// a wave's gathered Q stays resident in L2 while its units run.
+inline int64_t wave_queries(int B, int Sq, int Hkv, int qpk) {
+    int64_t per_q = (int64_t)Hkv * qpk * kD * 2;
+    int64_t w = ((int64_t)32 << 20) / per_q;
+    w = w < 128 ? 128 : (w / 128) * 128;
+    int64_t total = (int64_t)B * Sq;
+    return w > total ? total : w;
+}
+inline int64_t num_waves(int B, int Sq, int Hkv, int qpk) {
+    return ceil_div((int64_t)B * Sq, wave_queries(B, Sq, Hkv, qpk));
+}
+
+// Units: every (head, row, wave) segment adds at most one partial unit.
 inline int64_t plan_capacity(int B, int Hkv, int Sq, int Skv, int topk, int qpk) {
     int64_t nblk = ceil_div(Skv, kBlk);
     int64_t rows = (int64_t)B * nblk;
-    int64_t per_head = rows + ceil_div((int64_t)B * Sq * topk, q_per_unit(qpk));
+    int64_t nnz = (int64_t)B * Sq * topk;
+    int64_t segs = rows * num_waves(B, Sq, Hkv, qpk);
+    if (segs > nnz) segs = nnz;
+    int64_t per_head = segs + ceil_div(nnz, q_per_unit(qpk));
     return per_head * Hkv;
 }
 

@@ -16,7 +16,9 @@
 //   3. scatter: position = row_ptr + tile offset + popcount of the mask bits
 //      below the query, so each row lists its queries in ascending order with
 //      no atomics on positions (bit-deterministic).
-// The plan then cuts every row into units of at most 8 chunks of 128 rows.
+// The plan then cuts every row into units of at most 8 chunks of 128 rows,
+// ordered wave-major: wave w holds the queries [w*W, (w+1)*W) with W sized so
+// that a wave's Q rows (all heads) fill about 32 MiB and stay in L2.
 #include "common.cuh"
 
 namespace msa {
@@ -207,21 +209,54 @@ __global__ void csr_tail_kernel(const int32_t *__restrict__ row_ptr, CsrShape s,
     }
 }
 
-// Units per (h, row): ceil(count / q_per_unit).
-__global__ void plan_count_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int qpu,
-                                  int32_t *__restrict__ units_per_row) {
-    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (int64_t)s.Hkv * s.rows) return;
-    int h = (int)(idx / s.rows);
-    int64_t r = idx % s.rows;
-    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
-    int32_t c = rp[r + 1] - rp[r];
-    units_per_row[idx] = (c + qpu - 1) / qpu;
+// First position in the ascending run a[lo, hi) holding a value >= key.
+__device__ __forceinline__ int32_t lower_bound(const int32_t *a, int32_t lo, int32_t hi, int32_t key) {
+    while (lo < hi) {
+        int32_t mid = lo + ((hi - lo) >> 1);
+        if (a[mid] < key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
 }
 
-__global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int qpu,
-                                  const int32_t *__restrict__ unit_off, const int32_t *__restrict__ total,
-                                  PlanHeader *plan, PlanUnit *units, int capacity, int qpk, uint32_t *status) {
+// Segment (wave w, head h, row r) = the queries of row r in [w*W, (w+1)*W);
+// the flat index is wave-major so the unit list runs wave by wave.
+struct PlanShape {
+    int64_t W, nwaves;
+    int qpu;
+};
+
+__device__ __forceinline__ void segment_range(const int32_t *row_ptr, const int32_t *q_indices, const CsrShape &s,
+                                              const PlanShape &ps, int64_t idx, int &h, int64_t &r, int32_t &lo,
+                                              int32_t &hi) {
+    const int64_t per_wave = (int64_t)s.Hkv * s.rows;
+    const int64_t w = idx / per_wave;
+    const int64_t rem = idx % per_wave;
+    h = (int)(rem / s.rows);
+    r = rem % s.rows;
+    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
+    const int32_t *qi = q_indices + (int64_t)h * s.cap;
+    const int32_t b0 = rp[r], b1 = rp[r + 1];
+    lo = lower_bound(qi, b0, b1, (int32_t)(w * ps.W));
+    hi = lower_bound(qi, lo, b1, (int32_t)((w + 1) * ps.W));
+}
+
+// Units per segment: ceil(count / q_per_unit).
+__global__ void plan_count_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ q_indices,
+                                  CsrShape s, PlanShape ps, int32_t *__restrict__ units_per_seg) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= ps.nwaves * s.Hkv * s.rows) return;
+    int h;
+    int64_t r;
+    int32_t lo, hi;
+    segment_range(row_ptr, q_indices, s, ps, idx, h, r, lo, hi);
+    units_per_seg[idx] = (hi - lo + ps.qpu - 1) / ps.qpu;
+}
+
+__global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ q_indices,
+                                  CsrShape s, PlanShape ps, const int32_t *__restrict__ unit_off,
+                                  const int32_t *__restrict__ total, PlanHeader *plan, PlanUnit *units, int capacity,
+                                  int qpk, uint32_t *status) {
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx == 0) {
         int32_t tot = *total;
@@ -232,21 +267,24 @@ __global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, CsrShape 
         plan->work_count = tot;
         plan->capacity = capacity;
         plan->qhead_per_kv = qpk;
-        plan->q_per_unit = qpu;
+        plan->q_per_unit = ps.qpu;
+        plan->wave_queries = (int32_t)ps.W;
+        plan->nwaves = (int32_t)ps.nwaves;
     }
-    if (idx >= (int64_t)s.Hkv * s.rows) return;
-    int h = (int)(idx / s.rows);
-    int64_t r = idx % s.rows;
-    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
-    int32_t begin = rp[r], c = rp[r + 1] - begin;
-    int32_t u0 = unit_off[idx];
-    for (int32_t u = 0; u * qpu < c; ++u) {
+    if (idx >= ps.nwaves * s.Hkv * s.rows) return;
+    int h;
+    int64_t r;
+    int32_t lo, hi;
+    segment_range(row_ptr, q_indices, s, ps, idx, h, r, lo, hi);
+    const int32_t c = hi - lo;
+    const int32_t u0 = unit_off[idx];
+    for (int32_t u = 0; u * ps.qpu < c; ++u) {
         if (u0 + u >= capacity) break;
         PlanUnit pu;
         pu.head = h;
         pu.row = (int32_t)r;
-        pu.start = begin + u * qpu;
-        pu.count = min(qpu, c - u * qpu);
+        pu.start = lo + u * ps.qpu;
+        pu.count = min(ps.qpu, c - u * ps.qpu);
         units[u0 + u] = pu;
     }
 }
@@ -265,13 +303,27 @@ struct CsrWorkspace {
     size_t tile_counts, units_per_row, total, bytes;
 };
 
+PlanShape make_plan_shape(const CsrShape &s, int qpk) {
+    PlanShape ps;
+    ps.W = wave_queries(s.B, s.Sq, s.Hkv, qpk);
+    ps.nwaves = num_waves(s.B, s.Sq, s.Hkv, qpk);
+    ps.qpu = q_per_unit(qpk);
+    return ps;
+}
+
+// Segments (wave, head, row) of the plan; qpk 16 gives the smallest waves,
+// hence the most of them.
+int64_t max_segments(const CsrShape &s) {
+    return num_waves(s.B, s.Sq, s.Hkv, 16) * s.Hkv * s.rows;
+}
+
 CsrWorkspace csr_workspace_layout(const CsrShape &s) {
     CsrWorkspace w;
     size_t off = 0;
     w.tile_counts = off;
     off = align_up(off + sizeof(int32_t) * (size_t)s.Hkv * s.B * s.ntiles * s.nblk, 256);
     w.units_per_row = off;
-    off = align_up(off + sizeof(int32_t) * (size_t)s.Hkv * s.rows, 256);
+    off = align_up(off + sizeof(int32_t) * (size_t)max_segments(s), 256);
     w.total = off;
     off = align_up(off + 256, 256);
     w.bytes = off;
@@ -338,19 +390,19 @@ extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int
     MSA_LAUNCH_CHECK();
 
     if (plan) {
-        int qpu = q_per_unit(qhead_per_kv);
-        int32_t *upr = reinterpret_cast<int32_t *>(ws + w.units_per_row);
+        PlanShape ps = make_plan_shape(s, qhead_per_kv);
+        int32_t *ups = reinterpret_cast<int32_t *>(ws + w.units_per_row);
         int32_t *total = reinterpret_cast<int32_t *>(ws + w.total);
-        int64_t n = (int64_t)Hkv * s.rows;
+        int64_t n = ps.nwaves * Hkv * s.rows;
         int blocks = (int)ceil_div(n, 256);
-        plan_count_kernel<<<blocks, 256, 0, stream>>>(row_ptr, s, qpu, upr);
+        plan_count_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups);
         MSA_LAUNCH_CHECK();
-        segment_scan_kernel<<<1, 1024, 0, stream>>>(upr, n, 0, 1, total);
+        segment_scan_kernel<<<1, 1024, 0, stream>>>(ups, n, 0, 1, total);
         MSA_LAUNCH_CHECK();
         PlanHeader *ph = static_cast<PlanHeader *>(plan);
         PlanUnit *units = reinterpret_cast<PlanUnit *>(ph + 1);
         int capacity = (int)plan_capacity(B, Hkv, Sq, Skv, topk, qhead_per_kv);
-        plan_write_kernel<<<blocks, 256, 0, stream>>>(row_ptr, s, qpu, upr, total, ph, units, capacity,
+        plan_write_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups, total, ph, units, capacity,
                                                       qhead_per_kv, status_dev);
         MSA_LAUNCH_CHECK();
     }

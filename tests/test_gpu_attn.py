@@ -17,11 +17,17 @@ DEV = "cuda:0"
 
 def run_gpu(x, spec, kv_format="bf16", k=None, v=None, k_scales=None, v_scales=None, status=None):
     import block_sparse_top_gb300 as msa
+    own = status is None
+    if own:
+        status = msa.new_status(DEV)
     csr = msa.build_k2q_csr(x["q2k"], spec.Skv, spec.qpk, status=status)
     o, lse = msa.sparse_attn_fwd(x["q"], x["k"] if k is None else k, x["v"] if v is None else v, csr,
                                  causal=spec.causal, kv_format=kv_format, k_scales=k_scales, v_scales=v_scales,
                                  status=status)
     torch.cuda.synchronize()
+    if own:
+        st = msa.read_status(status)
+        assert st & 0x18 == 0, f"fatal device status {st:#x} (timeout / plan overflow)"
     return o, lse
 
 
@@ -94,6 +100,21 @@ def test_prefill_custom_scale_and_repeat_calls_are_identical():
     o_ref, l_ref = oracle.sparse_attn(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["q2k"].cpu(), causal=True,
                                       scale=0.05)
     assert_attn_close(o1.view(-1, spec.Hq, 128), l1.view(-1, spec.Hq), o_ref, l_ref, "scale")
+
+
+MID = [
+    # several waves, tens of units per CTA, many single-chunk units
+    P("mid_sink_two_waves", Hkv=1, Sq=16384, Skv=16384, topk=16),
+    P("mid_uniform_topk4", Hkv=2, Sq=12000, Skv=12288, topk=4, pattern="uniform"),
+    P("mid_qpk2_sink", Hkv=1, qpk=2, Sq=70000, Skv=70016, topk=8),
+]
+
+
+@pytest.mark.parametrize("spec", MID, ids=lambda s: s.name)
+def test_prefill_mid_size_sampled(spec):
+    total = spec.B * spec.Sq
+    rows = synth.sample_query_rows(total, 64, must=[0, 127, 128, 8191, 8192, total - 1])
+    check_spec(spec, rows=rows)
 
 
 FULL = [synth.C2_SINK32K, synth.C4_UNIFORM48K, synth.C5_SINK384K]
