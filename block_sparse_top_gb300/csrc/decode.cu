@@ -414,3 +414,61 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     MSA_LAUNCH_CHECK();
     return MSA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Paged decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run a
+// decode step: a serving loop whose memory is fixed at start-up, or code that
+// must not call cudaMalloc while other work is queued.  This variant keeps
+// its scratch (split counters and partials) in one file-scope device array of
+// kNoAllocScratchBytes, which every GPU that loads the library holds until
+// the process exits.  The array's address is looked up once per device with
+// that device current (cudaGetSymbolAddress), on the first call made on that
+// device.  Calls share the array: the split counters are cleared on the
+// stream at the start of each call, and calls that overlap on the GPU race
+// for it.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace msa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_paged_scratch[kNoAllocScratchBytes];
+
+// Device address of g_paged_scratch on the current device; nullptr on error.
+void *paged_scratch_for_current_device() {
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_paged_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace msa
+
+extern "C" int msa_sparse_attn_paged_fwd_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                                                 int num_pages, const int32_t *page_table, int max_pages,
+                                                 const int32_t *seqused_k, const int32_t *q2k, int B, int Sq,
+                                                 int Hq, int Hkv, int D, int page_size, int topk, int causal,
+                                                 float softmax_scale, void *o, float *lse, uint32_t *status_dev,
+                                                 cudaStream_t stream) {
+    size_t need = msa_sparse_attn_paged_fwd_workspace_size(B, Sq, Hq, Hkv, D, topk, max_pages);
+    if (need == 0) return MSA_ERR_UNSUPPORTED;
+    if (need > msa::kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // shape needs more than the static scratch
+    void *scratch = msa::paged_scratch_for_current_device();
+    if (!scratch) return MSA_ERR_CUDA;
+    return msa_sparse_attn_paged_fwd(q, k_pool, v_pool, num_pages, page_table, max_pages, seqused_k, q2k, B, Sq, Hq,
+                                     Hkv, D, page_size, topk, causal, softmax_scale, o, lse, scratch,
+                                     msa::kNoAllocScratchBytes, status_dev, stream);
+}

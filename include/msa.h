@@ -177,6 +177,29 @@ int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_p
                               int topk, int causal, float softmax_scale, void *o, float *lse, void *workspace,
                               size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream);
 
+/*
+ * msa_sparse_attn_paged_fwd without a workspace argument: the same paged
+ * decode, with its scratch (split counters and partials) in a static device
+ * array of 32 MiB that every GPU loading the library holds until exit.  The
+ * source pages have no counterpart; it exists for callers that cannot
+ * allocate device memory when they run a decode step (memory fixed at
+ * start-up, or no cudaMalloc allowed while work is queued).
+ *   - The first call on a device looks up the array's address on that
+ *     device (make it before any stream capture); later calls allocate
+ *     nothing and call no allocating routine.
+ *   - Returns MSA_ERR_WORKSPACE when the shape needs more than 32 MiB
+ *     (msa_sparse_attn_paged_fwd_workspace_size() > 33554432); other
+ *     arguments and errors are those of msa_sparse_attn_paged_fwd.
+ *   - All calls share the one array: it keeps the last call's contents, the
+ *     split counters are cleared on `stream` at the start of each call, and
+ *     calls that overlap on the GPU (other streams, other host threads) race.
+ */
+int msa_sparse_attn_paged_fwd_noalloc(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+                                      const int32_t *page_table, int max_pages, const int32_t *seqused_k,
+                                      const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                                      int topk, int causal, float softmax_scale, void *o, float *lse,
+                                      uint32_t *status_dev, cudaStream_t stream);
+
 /* =========================================================================
  * NVFP4 encoder for K/V rows (input side of MSA_KV_NVFP4)
  * =========================================================================

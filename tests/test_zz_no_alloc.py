@@ -1,0 +1,78 @@
+"""The paged decode entry point that allocates nothing (msa_sparse_attn_paged_fwd_noalloc).
+
+It serves callers that cannot allocate device memory when they run a decode
+step; its scratch is a static device array inside the library.  This test
+calls it through the C ABI twice in a row and checks each result against the
+allocating entry point (msa_sparse_attn_paged_fwd with a caller workspace),
+within the parity tolerances.  The file sorts last so that a stop-at-first-
+failure run has already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import msa_synth as synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+O_MAX_ABS = 2e-2
+O_MEAN_ABS = 2e-3
+LSE_REL = 1e-3
+
+
+def _call_noalloc(L, d, spec, o, lse, status):
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn = L.msa_sparse_attn_paged_fwd_noalloc
+    fn.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, P]
+    fn.restype = I
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return fn(p(d["q"]), p(d["k_pool"]), p(d["v_pool"]), spec.num_pages, p(d["page_table"]), spec.pages_per_seq,
+              p(d["seqused"]), p(d["q2k"]), spec.B, spec.Sq, spec.Hq, spec.Hkv, 128, 128, spec.topk, 1, -1.0,
+              p(o), p(lse), p(status), stream)
+
+
+def _close(a_o, a_l, b_o, b_l):
+    err = (a_o.float() - b_o.float()).abs()
+    assert err.max().item() <= O_MAX_ABS and err.mean().item() <= O_MEAN_ABS
+    assert torch.equal(torch.isneginf(a_l), torch.isneginf(b_l))
+    fin = torch.isfinite(b_l)
+    rel = ((a_l[fin] - b_l[fin]).abs() / b_l[fin].abs().clamp_min(1e-6)).max().item()
+    assert rel <= LSE_REL
+
+
+@pytest.mark.parametrize("L_kv", [4096, 32768])
+def test_noalloc_decode_matches_allocating_entry_point_twice(L_kv):
+    import block_sparse_top_gb300 as msa
+    L = msa.lib()
+    spec = synth.c3_decode(L_kv)
+    d = synth.make_decode_inputs(spec, device=DEV)
+    ref_o, ref_l = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"],
+                                             d["q2k"])
+    for _ in range(2):
+        o = torch.full_like(d["q"], float("nan"))
+        lse = torch.full(d["q"].shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        rc = _call_noalloc(L, d, spec, o, lse, status)
+        assert rc == 0, L.msa_status_string(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) & 0x1C == 0
+        _close(o, lse, ref_o, ref_l)
+
+
+def test_noalloc_decode_rejects_shapes_beyond_its_scratch():
+    import block_sparse_top_gb300 as msa
+    L = msa.lib()
+    # 4096 sequences x 4 KV heads need far more than the 32 MiB static scratch
+    spec = synth.DecodeSpec("too_big", B=4096, Sq=8, Hkv=4, qpk=16, topk=16, kv_len=4096, trim=0)
+    need = L.msa_sparse_attn_paged_fwd_workspace_size(spec.B, spec.Sq, spec.Hq, spec.Hkv, 128, spec.topk,
+                                                      spec.pages_per_seq)
+    assert need > (32 << 20)
+    t = torch.zeros(16, dtype=torch.bfloat16, device=DEV)
+    d = {"q": t, "k_pool": t, "v_pool": t, "page_table": t, "seqused": t, "q2k": t}
+    rc = _call_noalloc(L, d, spec, t, t, t)
+    assert rc == -3   # MSA_ERR_WORKSPACE, returned before any launch
