@@ -80,6 +80,127 @@ __device__ __forceinline__ void warp_pv(uint32_t v_base, const uint32_t (&pk)[16
     }
 }
 
+// Byte offset of 16-byte chunk c (0..15) of row r in a TMA tile stored as two
+// 128-byte-swizzled half tiles [2][128 rows][128 B] (1024-byte aligned base).
+__device__ __forceinline__ uint32_t tma_tile_off(int row, int chunk) {
+    return (uint32_t)((chunk >> 3) * 16384 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// A fragments (m16n8k16 layout) of 16 query rows x 128 dims read straight
+// from global memory: qf[kk] = {a0, a1, a2, a3} of k-step kk.  row_g and
+// row_g8 point at the rows of this thread's groupID and groupID + 8 (or are
+// null for rows that do not exist, which read as zero).
+__device__ __forceinline__ void load_q_frags(const __nv_bfloat16 *row_g, const __nv_bfloat16 *row_g8,
+                                             uint32_t (&qf)[8][4]) {
+    const int t = threadIdx.x & 3;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int col = kk * 16 + 2 * t;
+        qf[kk][0] = row_g ? *reinterpret_cast<const uint32_t *>(row_g + col) : 0u;
+        qf[kk][1] = row_g8 ? *reinterpret_cast<const uint32_t *>(row_g8 + col) : 0u;
+        qf[kk][2] = row_g ? *reinterpret_cast<const uint32_t *>(row_g + col + 8) : 0u;
+        qf[kk][3] = row_g8 ? *reinterpret_cast<const uint32_t *>(row_g8 + col + 8) : 0u;
+    }
+}
+
+// S[16 x 128] = Q (register fragments) . K^T with K in a TMA half-tile pair.
+__device__ __forceinline__ void warp_qk_tma(const uint32_t (&qf)[8][4], uint32_t k_base, float (&acc)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t b0, b1, b2, b3;
+            int brow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            int bchunk = 2 * kk + ((lane >> 3) & 1);
+            ldsm_x4(k_base + tma_tile_off(brow, bchunk), b0, b1, b2, b3);
+            mma_bf16(acc[2 * np], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+            mma_bf16(acc[2 * np + 1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+        }
+    }
+}
+
+// S[16 x 128] = Q . K^T with Q in a warp-private XOR-swizzled 16-row tile
+// (swz_off layout) and K in a TMA half-tile pair.
+__device__ __forceinline__ void warp_qk_qs_tma(uint32_t q_base, uint32_t k_base, float (&acc)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(q_base + swz_off(lane & 15, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t b0, b1, b2, b3;
+            int brow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            int bchunk = 2 * kk + ((lane >> 3) & 1);
+            ldsm_x4(k_base + tma_tile_off(brow, bchunk), b0, b1, b2, b3);
+            mma_bf16(acc[2 * np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+
+// Half-block forms: keys [64*kh, 64*kh + 64) only.
+__device__ __forceinline__ void warp_qk_qs_tma_half(uint32_t q_base, uint32_t k_base, int kh, float (&acc)[8][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(q_base + swz_off(lane & 15, 2 * kk + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t b0, b1, b2, b3;
+            int brow = kh * 64 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            int bchunk = 2 * kk + ((lane >> 3) & 1);
+            ldsm_x4(k_base + tma_tile_off(brow, bchunk), b0, b1, b2, b3);
+            mma_bf16(acc[2 * np], a0, a1, a2, a3, b0, b1);
+            mma_bf16(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+__device__ __forceinline__ void warp_pv_tma_half(uint32_t v_base, int kh, const uint32_t (&pk)[8][2],
+                                                 float (&o)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {
+        const int kk = kh * 4 + kq;
+        uint32_t a0 = pk[2 * kq][0], a1 = pk[2 * kq][1], a2 = pk[2 * kq + 1][0], a3 = pk[2 * kq + 1][1];
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+            uint32_t b0, b1, b2, b3;
+            int vrow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            int vchunk = 2 * dp + (lane >> 4);
+            ldsm_x4_t(v_base + tma_tile_off(vrow, vchunk), b0, b1, b2, b3);
+            mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
+            mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+
+// O[16 x 128] += P . V with V in a TMA half-tile pair.
+__device__ __forceinline__ void warp_pv_tma(uint32_t v_base, const uint32_t (&pk)[16][2], float (&o)[16][4]) {
+    int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0 = pk[2 * kk][0], a1 = pk[2 * kk][1], a2 = pk[2 * kk + 1][0], a3 = pk[2 * kk + 1][1];
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {
+            uint32_t b0, b1, b2, b3;
+            int vrow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            int vchunk = 2 * dp + (lane >> 4);
+            ldsm_x4_t(v_base + tma_tile_off(vrow, vchunk), b0, b1, b2, b3);
+            mma_bf16(o[2 * dp], a0, a1, a2, a3, b0, b1);
+            mma_bf16(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+        }
+    }
+}
+
 // e4m3 (fn) byte -> float, exact.
 __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
     uint32_t e = (b >> 3) & 0xF, m = b & 7;

@@ -63,11 +63,11 @@ inline int q_per_chunk(int qpk) { return 128 / qpk; }
 // Queries per unit: 8 chunks (K/V block loaded once per unit).
 inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
 
-// Queries per wave: the Q rows of one wave (all heads) fill about 32 MiB, so
+// Queries per wave: the Q rows of one wave (all heads) fill about 16 MiB, so
 // a wave's gathered Q stays resident in L2 while its units run.
 inline int64_t wave_queries(int B, int Sq, int Hkv, int qpk) {
     int64_t per_q = (int64_t)Hkv * qpk * kD * 2;
-    int64_t w = ((int64_t)32 << 20) / per_q;
+    int64_t w = ((int64_t)16 << 20) / per_q;
     w = w < 128 ? 128 : (w / 128) * 128;
     int64_t total = (int64_t)B * Sq;
     return w > total ? total : w;

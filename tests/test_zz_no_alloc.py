@@ -67,8 +67,8 @@ def test_noalloc_decode_matches_allocating_entry_point_twice(L_kv):
 def test_noalloc_decode_rejects_shapes_beyond_its_scratch():
     import block_sparse_top_gb300 as msa
     L = msa.lib()
-    # 4096 sequences x 4 KV heads need far more than the 32 MiB static scratch
-    spec = synth.DecodeSpec("too_big", B=4096, Sq=8, Hkv=4, qpk=16, topk=16, kv_len=4096, trim=0)
+    # 16384 sequences x 4 KV heads need more than the 32 MiB static scratch
+    spec = synth.DecodeSpec("too_big", B=16384, Sq=8, Hkv=4, qpk=16, topk=16, kv_len=4096, trim=0)
     need = L.msa_sparse_attn_paged_fwd_workspace_size(spec.B, spec.Sq, spec.Hq, spec.Hkv, 128, spec.topk,
                                                       spec.pages_per_seq)
     assert need > (32 << 20)
