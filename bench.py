@@ -38,8 +38,8 @@ import msa_synth as synth  # noqa: E402
 METRIC = "sparse-attn fwd effective TFLOP/s & % bf16 peak; paged decode GB/s & % HBM"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_CSR = 8      # hist, column scan, row scan, scatter, tail fill, plan count, plan scan, plan write
-KERNELS_PER_PARTIAL = 1
-KERNELS_PER_COMBINE = 1
+KERNELS_PER_PARTIAL = 1  # attention tiles
+KERNELS_PER_COMBINE = 1  # LSE combine
 
 # DRAM traffic of the attention-tile kernel from one ncu capture, keyed by the
 # hash of the source it was measured on (stale -> reported as null).
@@ -259,7 +259,7 @@ def run_ours(args, world, rank):
     flops = prefill_flops(spec_r, x["q2k"])
     nominal = 4.0 * spec.D * spec.Hq * spec.Sq * spec.B * spec.topk * 128
     q_mib = spec.B * spec.Sq * spec.Hq * spec.D * 2 / 2 ** 20
-    part_gb = spec.B * spec.Sq * spec.topk * spec.Hq * (spec.D * 2 + 4) / 1e9
+    part_gb = spec.B * spec.Sq * spec.topk * spec.Hq * (spec.D * 2 + 8) / 1e9
     csr, csr_ws = msa.csr_buffers(spec.B, spec.Hkv, spec.Sq, spec.Skv, spec.topk, spec.qpk, dev)
     fwd_ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, dev)
     out = torch.empty_like(x["q"])
@@ -342,7 +342,7 @@ def run_ours(args, world, rank):
     long_region = total_ms > 2000
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     achieved = flops / (attn_ms * 1e-3) / 1e12
-    khash = source_hash("attn.cu", "attn_tc.cuh", "attn_mma.cuh", "tc.cuh", "common.cuh")
+    khash = source_hash("attn.cu", "attn_tc.cuh", "attn_mma.cuh", "tc.cuh", "common.cuh", "combine.cuh")
     traffic = PROFILED_TRAFFIC.get(khash)
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -351,7 +351,7 @@ def run_ours(args, world, rank):
         "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
                    "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": True,
                    "pattern": spec.pattern, "per_rank_problem": "independent (seed + rank)",
-                   "l2": f"inputs larger than L2 (Q {q_mib:.0f} MiB, split partials {part_gb:.1f} GB per step); "
+                   "l2": f"inputs larger than L2 (Q {q_mib:.0f} MiB; split partials {part_gb:.1f} GB per step); "
                          "no flush"},
         "breakdown_ms": {"csr_build_and_plan": round(csr_ms, 4), "attention_tiles": round(attn_ms, 4),
                          "lse_combine": round(comb_ms, 4)},

@@ -14,8 +14,9 @@ from typing import Optional
 
 import torch
 
-from ._lib import (MSA_KV_BF16, MSA_KV_NVFP4, MSA_STATUS_DUPLICATE, MSA_STATUS_INDEX_RANGE,  # noqa: F401
-                   MSA_STATUS_PAGE_RANGE, MSA_STATUS_PLAN_OVERFLOW, MsaError, check, lib)
+from ._lib import (MSA_KV_BF16, MSA_KV_NVFP4, MSA_STATUS_DUPLICATE, MSA_STATUS_FATAL_MASK,  # noqa: F401
+                   MSA_STATUS_INDEX_RANGE, MSA_STATUS_LAUNCH, MSA_STATUS_PAGE_RANGE, MSA_STATUS_PLAN_OVERFLOW,
+                   MSA_STATUS_TIMEOUT, MsaError, check, lib)
 
 BLK = 128
 

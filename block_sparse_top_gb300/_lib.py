@@ -23,6 +23,9 @@ MSA_STATUS_INDEX_RANGE = 0x1
 MSA_STATUS_DUPLICATE = 0x2
 MSA_STATUS_PAGE_RANGE = 0x4
 MSA_STATUS_PLAN_OVERFLOW = 0x8
+MSA_STATUS_TIMEOUT = 0x10
+MSA_STATUS_LAUNCH = 0x20
+MSA_STATUS_FATAL_MASK = MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH
 
 MSA_KV_BF16 = 0
 MSA_KV_NVFP4 = 1

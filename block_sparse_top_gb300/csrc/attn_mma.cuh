@@ -36,6 +36,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// max of three floats in one instruction (sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // S[16 x 128] = Q_rows[16 x 128] . K[128 x 128]^T for the warp's 16 query
 // rows starting at `row0` of the Q tile; acc[nt][4] in the m16n8 C layout.
 __device__ __forceinline__ void warp_qk(uint32_t q_base, uint32_t k_base, int row0, float (&acc)[16][4]) {

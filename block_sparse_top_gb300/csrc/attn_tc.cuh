@@ -1,14 +1,15 @@
 // attn_tc.cuh -- the tcgen05 (5th-gen tensor core) block-sparse prefill tile
 // kernel: persistent, one CTA per SM, warp-specialised, 11 warps.
 //
-//   warp 0      loader, one issuing lane: per work unit the K and V block by
-//               TMA (bf16, 128-byte swizzle, two buffers); per chunk the 128
+//   warp 0      loader: per work unit the K and V block by TMA (bf16, 128-byte
+//               swizzle, two buffers, one issuing lane); per chunk the 128
 //               gathered Q rows (128/qhead_per_kv queries x all heads of the
-//               GQA group) by TMA into a 3-stage ring -- one tile box of
-//               qhead_per_kv rows per query when qhead_per_kv >= 8, four
-//               arbitrary rows per tile::gather4 copy otherwise.  The whole
-//               warp fetches the chunk's query ids before waiting for a free
-//               stage, so their latency hides behind that wait.
+//               GQA group) by TMA into a 3-stage ring: one 5D box per query
+//               (its whole 4 KB group) when qhead_per_kv >= 8, four rows per
+//               tile::gather4 copy otherwise.  The copy engine's cost is per
+//               request, so requests are kept few and large.  Query ids are
+//               prefetched into L2 four chunks ahead and loaded into
+//               registers one chunk ahead.
 //   warp 1      NVFP4 only: dequantises the K and V block into the same
 //               swizzled bf16 layout (exact products).
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
@@ -16,28 +17,33 @@
 //   warps 3-6,  softmax + epilogue for even / odd chunks: each thread owns one
 //   warps 7-10  S row (TMEM lane), loads it whole (128 columns), applies the
 //               bottom-right causal limit, writes P = exp(S - m) as bf16 over
-//               S, then scales O by 1/l and stores the split partial (bf16)
-//               and its lse.
+//               S, then stores the split partial unnormalised -- O = P V as
+//               bf16 with its statistics (m * scale, l = sum P) -- so that the
+//               combine applies each split's weight and 1/l in one product.
+//               Packed f32x2 FMA/add and three-input max halve the per-element
+//               instruction count of the row pass.
 //
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 // Every wait is bounded; on a timeout the CTA raises MSA_STATUS_TIMEOUT,
 // drains its copies and MMAs, frees tensor memory and exits.
 #pragma once
 #include "attn_mma.cuh"
+#include "combine.cuh"
 #include "tc.cuh"
 
 namespace msa {
 
 struct TcParams {
+    const __nv_bfloat16 *q;               // [B*Sq][Hq][D]
     const uint8_t *k_packed, *v_packed;   // NVFP4 only
     const uint8_t *k_scales, *v_scales;   // NVFP4 only
     const int32_t *qsplit;
     const PlanHeader *plan;
     const PlanUnit *units;
-    __nv_bfloat16 *o_part;                // [B*Sq][topk][Hq][D]
-    float *lse_part;                      // [B*Sq][topk][Hq]
+    __nv_bfloat16 *o_part;                // split partials, layout in combine.cuh
+    float2 *stat_part;                    // split statistics, layout in combine.cuh
     uint32_t *status;
-    int B, Sq, Skv, Hq, Hkv, qpk, topk, nblk, causal;
+    int B, Sq, Skv, Hq, Hkv, qpk, lqpk, topk, nblk, causal;  // lqpk = log2(qpk)
     int64_t cap;
     float scale, scale_log2;
 };
@@ -45,6 +51,7 @@ struct TcParams {
 namespace tck {
 
 constexpr int kNQ = 3;
+constexpr int kIdAhead = 4;  // chunks of query ids the loader fetches ahead
 constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3;
@@ -65,8 +72,9 @@ enum : int {
 constexpr uint32_t kSmTslot = kSmBar + 8 * NBAR;
 constexpr uint32_t kSmAbort = kSmTslot + 4;
 constexpr uint32_t kSmBytes = kSmAbort + 4;
-constexpr uint32_t kSmAlloc = kSmBytes + 1024;  // slack for 1024-byte alignment
-static_assert(kSmAlloc <= 232448, "shared memory budget");
+// The dynamic shared memory base is 1024-byte aligned (no static shared
+// memory); the kernel checks this instead of reserving slack.
+static_assert(kSmBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, 0, 1);
@@ -100,8 +108,12 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
     using namespace tck;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    uint8_t *const gbase = smem_raw + (base - smem_u32(smem_raw));
+    const uint32_t base = smem_u32(smem_raw);
+    uint8_t *const gbase = smem_raw;
+    if (base & 1023u) {  // 128-byte swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) set_status(p.status, MSA_STATUS_LAUNCH);
+        return;
+    }
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kSmAbort);
     auto bar = [&](int i) -> uint32_t { return base + kSmBar + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -144,8 +156,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loader
         int ci = 0, ui = 0;
-        int kv_armed[2] = {-1, -1}, q_armed[kNQ];
-        for (int i = 0; i < kNQ; ++i) q_armed[i] = -1;
+        int kv_armed[2] = {-1, -1};
         bool ok = true;
         const int G = gridDim.x;
         // query ids of chunk c of unit x: lane l holds queries l, l+32, l+64, l+96
@@ -157,17 +168,44 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                                                     : -1;
             }
         };
+        // A second cursor runs kIdAhead chunks ahead of the issuing one and
+        // prefetches its query ids into L2; the ids of the next chunk are
+        // loaded into registers one chunk ahead and then hit in L2.  (Values
+        // are never shuffled through a register ring: a move of a register
+        // whose load is still in flight would wait for that load.)
+        struct Cursor {
+            int u, c;
+            Unit x;
+        };
+        auto advance = [&](Cursor &k) {
+            if (k.u >= work) return;
+            if (++k.c == k.x.nch) {
+                k.u += G;
+                k.c = 0;
+                if (k.u < work) k.x = load_unit(p, k.u);
+            }
+        };
+        auto prefetch_ids = [&](const Cursor &k) {
+            const int idx = lane * 32;  // one 128-byte line per 32 ids
+            if (k.u < work && idx < qc && k.c * qc + idx < k.x.count)
+                tc::prefetch_l2(p.qsplit + (int64_t)k.x.h * p.cap + k.x.start + k.c * qc + idx);
+        };
+        // every plan entry this CTA will read, into L2 up front (16 bytes each)
+        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) tc::prefetch_l2(p.units + u);
         const uint64_t keep = tc::l2_policy_evict_last();
-        int u = blockIdx.x;
-        Unit x{}, xn{};
-        int ids[4] = {-1, -1, -1, -1};
-        if (u < work) {
-            x = load_unit(p, u);
-            fetch_ids(x, 0, ids);
+        Cursor cur{(int)blockIdx.x, 0, Unit{}}, ahead{(int)blockIdx.x, 0, Unit{}};
+        if (cur.u < work) cur.x = ahead.x = load_unit(p, cur.u);
+        for (int d = 0; d < kIdAhead; ++d) {
+            prefetch_ids(ahead);
+            advance(ahead);
         }
-        if (u + G < work) xn = load_unit(p, u + G);
-        int c = 0;
-        while (u < work && ok) {
+        // One chunk: issue its Q (and, on a unit's first chunk, K/V) with the ids
+        // in `ids`, while loading the next chunk's ids into `nids`.  The loop
+        // below alternates two id buffers, so no register with a load in
+        // flight is ever copied.
+        auto step = [&](const int (&ids)[4], int (&nids)[4]) -> bool {
+            const Unit &x = cur.x;
+            const int c = cur.c;
             const int kb = ui & 1;
             if (c == 0 && KV_FORMAT == MSA_KV_BF16) {
                 if (lane == 0) {
@@ -186,35 +224,38 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                if (!ok) return false;
             }
-            // prefetch the next chunk's ids (its latency hides behind this chunk)
-            const bool last_in_unit = (c + 1 == x.nch);
-            const bool has_next = !last_in_unit || (u + G < work);
-            int nids[4] = {-1, -1, -1, -1};
-            if (has_next) fetch_ids(last_in_unit ? xn : x, last_in_unit ? 0 : c + 1, nids);
+            // next chunk's ids (registers, one chunk ahead) and an L2 prefetch further out
+            Cursor nxt = cur;
+            advance(nxt);
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) nids[s4] = -1;
+            if (nxt.u < work) fetch_ids(nxt.x, nxt.c, nids);
+            prefetch_ids(ahead);
+            advance(ahead);
             const int qs = ci % kNQ;
-            const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
             if (lane == 0 && ci >= kNQ)
                 ok = tc::mbar_wait(bar(Q_EMPTY + qs), ((ci / kNQ) - 1) & 1, abort_flag, p.status,
                                    MSA_STATUS_TIMEOUT);
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            if (!ok) return false;
+            // The chunk's 128 Q rows (row R = query R / qpk of the chunk, head
+            // R % qpk of the group), 128-byte swizzled K-major.  qpk >= 8: one
+            // 5D box per query holds its whole group (row octets 2048 bytes
+            // apart, column halves 1024 apart); qpk < 8: four arbitrary rows
+            // per tile::gather4 copy (rows 128 bytes apart, halves 16384).
+            // Padding rows repeat the chunk's first query.
             const uint32_t qt = base + kSmQ + qs * 32768;
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(bar(Q_FULL + qs), 32768);
-                q_armed[qs] = (ci / kNQ) & 1;
-            }
+            const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
+            if (lane == 0) tc::mbar_arrive_expect_tx(bar(Q_FULL + qs), 32768);
             if (p.qpk >= 8) {
                 for (int qi = 0; qi < qc; ++qi) {
                     int gq = __shfl_sync(0xffffffffu, ids[0], qi);
                     if (gq < 0) gq = first;
-                    if (lane == 0) {
-                        const int row0 = gq * p.Hq + x.h * p.qpk;
-                        const uint32_t off = (uint32_t)(qi * p.qpk * 128);
-                        tc::tma_load_2d_hint(qt + off, &tm_q, bar(Q_FULL + qs), 0, row0, keep);
-                        tc::tma_load_2d_hint(qt + 16384 + off, &tm_q, bar(Q_FULL + qs), 64, row0, keep);
-                    }
+                    if (lane == 0)
+                        tc::tma_load_5d(qt + (uint32_t)(qi * p.qpk * 256), &tm_q, bar(Q_FULL + qs), 0, 0, 0, 0,
+                                        gq * p.Hkv + x.h);
                 }
             } else {
                 for (int j = 0; j < 32; ++j) {
@@ -230,31 +271,28 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     }
                     if (lane == 0) {
                         tc::tma_gather4_hint(qt + j * 512, &tm_q, bar(Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
-                        tc::tma_gather4_hint(qt + 16384 + j * 512, &tm_q, bar(Q_FULL + qs), 64, r[0], r[1], r[2], r[3], keep);
+                        tc::tma_gather4_hint(qt + 16384 + j * 512, &tm_q, bar(Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
+                                             keep);
                     }
                 }
             }
-            // advance to the next chunk
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) ids[s4] = nids[s4];
             ++ci;
-            if (last_in_unit) {
-                u += G;
-                ++ui;
-                x = xn;
-                if (u + G < work) xn = load_unit(p, u + G);
-                c = 0;
-            } else {
-                ++c;
+            const bool last_in_unit = (c + 1 == x.nch);
+            advance(cur);
+            if (last_in_unit) ++ui;
+            return cur.u < work;
+        };
+        int ids_a[4] = {-1, -1, -1, -1}, ids_b[4] = {-1, -1, -1, -1};
+        if (cur.u < work) {
+            fetch_ids(cur.x, 0, ids_a);
+            while (step(ids_a, ids_b) && step(ids_b, ids_a)) {
             }
         }
-        // drain outstanding TMA loads before the CTA can exit
+        // drain outstanding copies before the CTA can exit
         if (lane == 0) {
             volatile int dummy = 0;
             for (int i = 0; i < 2; ++i)
                 if (kv_armed[i] >= 0) tc::mbar_wait(bar(KV_FULL + i), (uint32_t)kv_armed[i], &dummy, p.status, 0);
-            for (int i = 0; i < kNQ; ++i)
-                if (q_armed[i] >= 0) tc::mbar_wait(bar(Q_FULL + i), (uint32_t)q_armed[i], &dummy, p.status, 0);
         }
         __syncwarp();
     } else if (warp == kWarpDequant) {
@@ -296,17 +334,23 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
+        // Per chunk ci two MMA groups are due: S_ci = Q_ci K^T (needs Q_ci, and the
+        // unit's K/V on its first chunk) and O_{ci-1} = P_{ci-1} V (needs P_{ci-1}
+        // and a free O buffer).  Neither depends on the other, so the issuer polls
+        // all their barriers and issues whichever becomes ready first.
         if (lane == 0) {
             int ci = 0, ui = 0;
             bool ok = true;
             int pv_ci = -1, pv_kb = 0, pv_last = 0;
-            auto issue_pv = [&](int cj, int kbj, int last) -> bool {
+            // Q tile geometry (see the loader): octet stride and half offset
+            const uint32_t q_sbo = p.qpk >= 8 ? 2048u : 1024u, q_half = p.qpk >= 8 ? 1024u : 16384u;
+            auto pv_ready = [&](int cj) -> bool {
                 const int b = cj & 1;
-                if (!tc::mbar_wait(bar(P_FULL + b), (cj >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT))
-                    return false;
-                if (cj >= 2 &&
-                    !tc::mbar_wait(bar(O_EMPTY + b), ((cj >> 1) - 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT))
-                    return false;
+                return tc::mbar_test(bar(P_FULL + b), (cj >> 1) & 1) &&
+                       (cj < 2 || tc::mbar_test(bar(O_EMPTY + b), ((cj >> 1) - 1) & 1));
+            };
+            auto issue_pv = [&](int cj, int kbj, int last) {
+                const int b = cj & 1;
                 tc::fence_after_sync();
                 const uint32_t vs = base + kSmV + kbj * 32768;
 #pragma unroll
@@ -315,7 +359,42 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                                tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, kk > 0);
                 tc::mma_commit(bar(O_FULL + b));
                 if (last) tc::mma_commit(bar(KV_EMPTY + kbj));
-                return true;
+            };
+            auto issue_s = [&](int cj, int kbj) {
+                const int b = cj & 1, qs = cj % kNQ;
+                tc::fence_after_sync();
+                const uint32_t qt = base + kSmQ + qs * 32768, ks = base + kSmK + kbj * 32768;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * q_half + (kk & 3) * 32;
+                    tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + qoff, 16, q_sbo),
+                               tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
+                }
+                tc::mma_commit(bar(S_FULL + b));
+                tc::mma_commit(bar(Q_EMPTY + qs));
+            };
+            // polls until S_ci (if s_cj >= 0) and the pending PV are both issued
+            auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par) -> bool {
+                bool s_done = s_cj < 0, pv_done = pv_ci < 0, kv_ok = !need_kv;
+                for (uint32_t i = 0; i < tc::kPollLimit; ++i) {
+                    if (!s_done) {
+                        if (!kv_ok) kv_ok = tc::mbar_test(bar(KV_FULL + kbj), (uint32_t)kv_par);
+                        if (kv_ok && tc::mbar_test(bar(Q_FULL + s_cj % kNQ), (s_cj / kNQ) & 1)) {
+                            issue_s(s_cj, kbj);
+                            s_done = true;
+                        }
+                    }
+                    if (!pv_done && pv_ready(pv_ci)) {
+                        issue_pv(pv_ci, pv_kb, pv_last);
+                        pv_done = true;
+                    }
+                    if (s_done && pv_done) return true;
+                    if ((i & 255u) == 255u && *abort_flag) return false;
+                }
+                *abort_flag = 1;
+                set_status(p.status, MSA_STATUS_TIMEOUT);
+                return false;
             };
             Unit xnext{};
             if (blockIdx.x < work) xnext = load_unit(p, blockIdx.x);
@@ -323,29 +402,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 const Unit x = xnext;
                 if (u + (int)gridDim.x < work) xnext = load_unit(p, u + gridDim.x);
                 const int kb = ui & 1;
-                ok = tc::mbar_wait(bar(KV_FULL + kb), (ui >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                const uint32_t ks = base + kSmK + kb * 32768;
                 for (int c = 0; c < x.nch && ok; ++c, ++ci) {
-                    const int b = ci & 1, qs = ci % kNQ;
-                    ok = tc::mbar_wait(bar(Q_FULL + qs), (ci / kNQ) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint32_t qt = base + kSmQ + qs * 32768;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + off, 16, 1024),
-                                   tc::sdesc_sw128(ks + off, 16, 1024), kIdescS, kk > 0);
-                    }
-                    tc::mma_commit(bar(S_FULL + b));
-                    tc::mma_commit(bar(Q_EMPTY + qs));
-                    if (pv_ci >= 0) ok = issue_pv(pv_ci, pv_kb, pv_last);
+                    ok = drive(ci, kb, c == 0, (ui >> 1) & 1);
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
                 }
             }
-            if (ok && pv_ci >= 0) issue_pv(pv_ci, pv_kb, pv_last);
+            if (ok && pv_ci >= 0) drive(-1, 0, false, 0);
             // all issued MMAs complete before tensor memory is released
             tc::mma_commit(bar(DRAIN));
             volatile int dummy = 0;
@@ -359,10 +423,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t s_addr = tmem + lane_base + wg * 128;
         const uint32_t o_addr = tmem + lane_base + 256 + wg * 128;
+        const int j_of_row = R % p.qpk;  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
+        Unit xnext{};
+        if (blockIdx.x < work) xnext = load_unit(p, blockIdx.x);
         for (int u = blockIdx.x; u < work && ok; u += gridDim.x) {
-            const Unit x = load_unit(p, u);
+            const Unit x = xnext;  // loaded one unit ahead
+            if (u + (int)gridDim.x < work) xnext = load_unit(p, u + gridDim.x);
             for (int c = 0; c < x.nch && ok; ++c, ++ci) {
                 if ((ci & 1) != wg) continue;
                 const uint32_t par = (ci >> 1) & 1;
@@ -387,40 +455,43 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                 }
                 tc::tmem_ld_wait();
-                // row max over visible keys
-                // four independent chains keep the reductions off the latency path
+                // keys past the causal limit (diagonal block rows) become -inf
+                if (nvis < 128) {
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        if (j >= nvis) r[j] = 0xff800000u;
+                }
+                // row max: three-input max, four independent chains
                 float mm[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-                if (nvis == 128) {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) mm[j & 3] = fmaxf(mm[j & 3], __uint_as_float(r[j]));
-                } else {
+                for (int j = 0; j < 128; j += 8) {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
-                        if (j < nvis) mm[j & 3] = fmaxf(mm[j & 3], __uint_as_float(r[j]));
+                    for (int a = 0; a < 4; ++a)
+                        mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                 }
-                const float m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-                // P = exp(S - m) packed to bf16 in place (r[j] <- keys 2j, 2j+1), row sum
+                const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                // P = exp2(S * scale_log2 - m * scale_log2) packed to bf16 in place
+                // (r[j] <- keys 2j, 2j+1); row sum in packed f32x2 adds
                 const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
-                float ll[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) ll[a] = 0.f;
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                const float2 nm2 = make_float2(-mc, -mc);
+                float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    const float x0 = (2 * j < nvis) ? ex2_approx(fmaf(__uint_as_float(r[2 * j]), p.scale_log2, -mc))
-                                                    : 0.f;
-                    const float x1 =
-                        (2 * j + 1 < nvis) ? ex2_approx(fmaf(__uint_as_float(r[2 * j + 1]), p.scale_log2, -mc)) : 0.f;
-                    ll[j & 3] += x0 + x1;
-                    r[j] = pack_bf16x2(x0, x1);
+                    float2 e = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
+                    e.x = ex2_approx(e.x);
+                    e.y = ex2_approx(e.y);
+                    ll[j & 1] = __fadd2_rn(ll[j & 1], e);
+                    r[j] = pack_bf16x2(e.x, e.y);
                 }
-                const float l = (ll[0] + ll[1]) + (ll[2] + ll[3]);
+                const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
                 tc::tmem_st64(s_addr, r);
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 tc::mbar_arrive(bar(P_FULL + wg));
-                // epilogue: O / l -> bf16 partial, lse
+                // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
                 ok = tc::mbar_wait(bar(O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -430,23 +501,22 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::fence_before_sync();
                 tc::mbar_arrive(bar(O_EMPTY + wg));  // O is in registers: the next PV may start
                 if (valid) {
-                    // partial layout [query][split][chunk c of 8 dims][query head][8]: for a
-                    // fixed c the heads of one query are contiguous, so each store
-                    // instruction of the warp writes whole 256-byte runs
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    const int hq = x.h * p.qpk + (R % p.qpk);
-                    const int64_t qs_row = (int64_t)gq * p.topk + split;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + qs_row * 16 * p.Hq + hq;
+                    // grouped layout: for a fixed (split, c) the heads of one group are
+                    // contiguous, so each store instruction writes whole runs
+                    const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
 #pragma unroll
                     for (int v4 = 0; v4 < 16; ++v4) {
                         uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-                        o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-                        o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-                        o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
-                        __stcs(dst + (int64_t)v4 * p.Hq, o4);  // streaming: evict first from L2
+                        o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
+                        o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
+                        o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
+                        o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
+                        __stcs(dst + (int64_t)v4 * p.qpk, o4);  // streaming: evict first from L2
                     }
-                    __stcs(p.lse_part + qs_row * p.Hq + hq, (l > 0.f) ? (m * p.scale + logf(l)) : -INFINITY);
+                    const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
+                    float2 *sdst = p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
+                    __stcs(sdst, st);
                 }
             }
         }

@@ -1,0 +1,87 @@
+// combine.cuh -- split partial layout (written by the tile kernel, read by
+// the LSE combine) and the merge of one output piece.
+//
+// A (query, KV head) pair is a group g = gq * Hkv + h; its split partials are
+// contiguous:
+//   o_part    [B*Sq][Hkv][topk][D/8][qhead_per_kv][8] bf16, the unnormalised
+//             U_s = sum_k exp(scale (s_k - m_s)) v_k of split s;
+//   stat_part [B*Sq][Hkv][topk][qhead_per_kv] float2 (a_s = scale m_s, l_s).
+// Split s alone normalises to U_s / l_s with lse_s = a_s + ln l_s, so
+//   LSE = logsumexp_s lse_s = A + ln sum_s l_s exp(a_s - A)      (A = max a_s)
+//   O   = sum_s exp(lse_s - LSE) U_s / l_s = sum_s exp(a_s - A) U_s / sum_s l_s exp(a_s - A)
+// (interface.py _sparse_atten_csr_varlen_forward: per-split O and LSE merged
+// by LSE; test_sparse_atten.py sparse_attention_ref: a row with no visible key
+// has O = 0 and LSE = -inf).  A split with a non-finite a_s has weight 0.
+#pragma once
+#include "common.cuh"
+
+namespace msa {
+
+__host__ __device__ inline int64_t part_o_index(int64_t grp, int topk, int qpk, int split, int c, int j) {
+    return ((grp * topk + split) * 16 + c) * qpk + j;  // in 16-byte pieces
+}
+__host__ __device__ inline int64_t part_stat_index(int64_t grp, int topk, int qpk, int split, int j) {
+    return (grp * topk + split) * qpk + j;
+}
+
+// Merges the first n of topk splits of piece (group grp, 8-dim chunk c, head j
+// of the group) into out (8 bf16) and lse_out.  Every load of a batch of BATCH
+// splits is issued before any is used (all topk slots are read, those at or
+// past n are ignored); batches merge online with a running max.
+template <int MAXS, int BATCH = 16>
+__device__ __forceinline__ void combine_piece(const uint4 *__restrict__ o_part, const float2 *__restrict__ stat_part,
+                                              int64_t grp, int n, int topk, int qpk, int c, int j, uint4 &out,
+                                              float &lse_out) {
+    const uint4 *src = o_part + part_o_index(grp, topk, qpk, 0, c, j);
+    const float2 *st = stat_part + part_stat_index(grp, topk, qpk, 0, j);
+    const int64_t o_stride = 16 * (int64_t)qpk;
+    float mx = -INFINITY, den = 0.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int s0 = 0; s0 < (MAXS < topk ? MAXS : topk); s0 += BATCH) {
+        uint4 v[BATCH];
+        float2 sv[BATCH];
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t)
+            if (s0 + t < topk) v[t] = __ldcs(src + (s0 + t) * o_stride);  // read once: evict first
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t)
+            sv[t] = (s0 + t < topk) ? __ldg(st + (int64_t)(s0 + t) * qpk) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t)
+            if (s0 + t >= n) sv[t].x = -INFINITY;
+        float bm = mx;
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t)
+            if (isfinite(sv[t].x)) bm = fmaxf(bm, sv[t].x);
+        if (bm > mx) {
+            const float r = __expf(mx - bm);  // 0 when mx is -inf
+            den *= r;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] *= r;
+            mx = bm;
+        }
+#pragma unroll
+        for (int t = 0; t < BATCH; ++t) {
+            if (!isfinite(sv[t].x)) continue;
+            const float e = __expf(sv[t].x - mx);
+            den += e * sv[t].y;
+            acc[0] += e * bf16_lo(v[t].x);
+            acc[1] += e * bf16_hi(v[t].x);
+            acc[2] += e * bf16_lo(v[t].y);
+            acc[3] += e * bf16_hi(v[t].y);
+            acc[4] += e * bf16_lo(v[t].z);
+            acc[5] += e * bf16_hi(v[t].z);
+            acc[6] += e * bf16_lo(v[t].w);
+            acc[7] += e * bf16_hi(v[t].w);
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    lse_out = den > 0.f ? mx + logf(den) : -INFINITY;
+}
+
+}  // namespace msa

@@ -46,7 +46,7 @@ struct PlanHeader {
     int32_t capacity;    // units the buffer holds
     int32_t qhead_per_kv;
     int32_t q_per_unit;
-    int32_t wave_queries;  // queries per wave (units are ordered wave-major)
+    int32_t wave_queries;  // queries per wave (units run head-major, then wave-major)
     int32_t nwaves;
     int32_t reserved[10];
 };
@@ -63,17 +63,19 @@ inline int q_per_chunk(int qpk) { return 128 / qpk; }
 // Queries per unit: 8 chunks (K/V block loaded once per unit).
 inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
 
-// Queries per wave: the Q rows of one wave (all heads) fill about 16 MiB, so
-// a wave's gathered Q stays resident in L2 while its units run.
-inline int64_t wave_queries(int B, int Sq, int Hkv, int qpk) {
-    int64_t per_q = (int64_t)Hkv * qpk * kD * 2;
-    int64_t w = ((int64_t)16 << 20) / per_q;
-    w = w < 128 ? 128 : (w / 128) * 128;
-    int64_t total = (int64_t)B * Sq;
+// Queries per wave.  Units run head-major, then wave by wave: one (KV head,
+// wave) pass writes W * qhead_per_kv * topk split partials of D bf16 plus two
+// floats each, and W is sized so that those are about 32 MiB -- small enough
+// to stay in L2, next to the head's K/V, until their combine reads them.
+inline int64_t wave_queries(int B, int Sq, int qpk, int topk) {
+    const int64_t per_q = (int64_t)qpk * topk * (kD * 2 + 8);
+    int64_t w = ((((int64_t)32 << 20) / per_q) + 64) / 128 * 128;  // nearest multiple of 128
+    if (w < 128) w = 128;
+    const int64_t total = (int64_t)B * Sq;
     return w > total ? total : w;
 }
-inline int64_t num_waves(int B, int Sq, int Hkv, int qpk) {
-    return ceil_div((int64_t)B * Sq, wave_queries(B, Sq, Hkv, qpk));
+inline int64_t num_waves(int B, int Sq, int qpk, int topk) {
+    return ceil_div((int64_t)B * Sq, wave_queries(B, Sq, qpk, topk));
 }
 
 // Units: every (head, row, wave) segment adds at most one partial unit.
@@ -81,7 +83,7 @@ inline int64_t plan_capacity(int B, int Hkv, int Sq, int Skv, int topk, int qpk)
     int64_t nblk = ceil_div(Skv, kBlk);
     int64_t rows = (int64_t)B * nblk;
     int64_t nnz = (int64_t)B * Sq * topk;
-    int64_t segs = rows * num_waves(B, Sq, Hkv, qpk);
+    int64_t segs = rows * num_waves(B, Sq, qpk, topk);
     if (segs > nnz) segs = nnz;
     int64_t per_head = segs + ceil_div(nnz, q_per_unit(qpk));
     return per_head * Hkv;

@@ -17,8 +17,9 @@
 //      below the query, so each row lists its queries in ascending order with
 //      no atomics on positions (bit-deterministic).
 // The plan then cuts every row into units of at most 8 chunks of 128 rows,
-// ordered wave-major: wave w holds the queries [w*W, (w+1)*W) with W sized so
-// that a wave's Q rows (all heads) fill about 32 MiB and stay in L2.
+// ordered by KV head, then by wave: wave w holds the queries [w*W, (w+1)*W)
+// with W sized so that one (head, wave) pass writes about 32 MiB of split
+// partials, which stay in L2 until they are combined.
 #include "common.cuh"
 
 namespace msa {
@@ -219,8 +220,10 @@ __device__ __forceinline__ int32_t lower_bound(const int32_t *a, int32_t lo, int
     return lo;
 }
 
-// Segment (wave w, head h, row r) = the queries of row r in [w*W, (w+1)*W);
-// the flat index is wave-major so the unit list runs wave by wave.
+// Segment (head h, wave w, row r) = the queries of row r in [w*W, (w+1)*W);
+// the flat index is head-major, then wave-major, so the unit list runs one
+// KV head at a time (its K/V stays in L2) and, within it, wave by wave (each
+// wave's split partials are all written within one short stretch).
 struct PlanShape {
     int64_t W, nwaves;
     int qpu;
@@ -229,10 +232,10 @@ struct PlanShape {
 __device__ __forceinline__ void segment_range(const int32_t *row_ptr, const int32_t *q_indices, const CsrShape &s,
                                               const PlanShape &ps, int64_t idx, int &h, int64_t &r, int32_t &lo,
                                               int32_t &hi) {
-    const int64_t per_wave = (int64_t)s.Hkv * s.rows;
-    const int64_t w = idx / per_wave;
-    const int64_t rem = idx % per_wave;
-    h = (int)(rem / s.rows);
+    const int64_t per_head = ps.nwaves * s.rows;
+    h = (int)(idx / per_head);
+    const int64_t rem = idx % per_head;
+    const int64_t w = rem / s.rows;
     r = rem % s.rows;
     const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
     const int32_t *qi = q_indices + (int64_t)h * s.cap;
@@ -305,16 +308,16 @@ struct CsrWorkspace {
 
 PlanShape make_plan_shape(const CsrShape &s, int qpk) {
     PlanShape ps;
-    ps.W = wave_queries(s.B, s.Sq, s.Hkv, qpk);
-    ps.nwaves = num_waves(s.B, s.Sq, s.Hkv, qpk);
+    ps.W = wave_queries(s.B, s.Sq, qpk, s.topk);
+    ps.nwaves = num_waves(s.B, s.Sq, qpk, s.topk);
     ps.qpu = q_per_unit(qpk);
     return ps;
 }
 
-// Segments (wave, head, row) of the plan; qpk 16 gives the smallest waves,
+// Segments (head, wave, row) of the plan; qpk 16 gives the smallest waves,
 // hence the most of them.
 int64_t max_segments(const CsrShape &s) {
-    return num_waves(s.B, s.Sq, s.Hkv, 16) * s.Hkv * s.rows;
+    return num_waves(s.B, s.Sq, 16, s.topk) * s.Hkv * s.rows;
 }
 
 CsrWorkspace csr_workspace_layout(const CsrShape &s) {

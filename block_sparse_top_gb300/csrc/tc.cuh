@@ -35,6 +35,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 
+// L2 prefetch of the 128-byte line holding `p`.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
+// Non-blocking probe of an mbarrier phase (for a thread that polls several).
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Poll budget of a multi-barrier polling loop (about a second of polls).
+constexpr uint32_t kPollLimit = 1u << 26;
+
 // Bounded wait: gives up after `limit` polls, raises the CTA abort flag and
 // the device status bit so every role can drain and exit.
 constexpr uint32_t kSpinLimit = 1u << 22;
@@ -109,6 +127,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
         "%4}], [%2], %5;\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, "
+        "%7}], [%2];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
 __device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int r0,
@@ -291,9 +317,8 @@ inline bool make_kv_map(CUtensorMap *map, const void *base, int heads, int64_t t
     return r == CUDA_SUCCESS;
 }
 
-// 2D bf16 map over the query rows [rows][128]: box {64, box_rows}.  box_rows
-// = qhead_per_kv (>= 8) loads one query's heads as one tile; box_rows = 1 is
-// the gather4 form (four arbitrary rows per copy).
+// 2D bf16 map over the query rows [rows][128]: box {64, box_rows}; box_rows
+// = 1 is the gather4 form (four arbitrary rows per copy).
 inline bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int box_rows) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
@@ -302,6 +327,25 @@ inline bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int box
     cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 5D bf16 view of the query rows for qhead_per_kv >= 8, one box per (query,
+// KV head) group of qpk rows: dims {64 elements, 8 rows, 2 column halves,
+// qpk/8 row octets, groups} with byte strides {256, 128, 2048, qpk*256} and
+// box {64, 8, 2, qpk/8, 1}.  A box lands as [octet][half][8 rows][128 B] with
+// the 128-byte swizzle: each (octet, half) is one 1024-byte K-major atom, so
+// the chunk's row octets sit 2048 bytes apart and its halves 1024 bytes apart.
+inline bool make_q_group_map(CUtensorMap *map, const void *base, int64_t groups, int qpk) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)(qpk / 8), (cuuint64_t)groups};
+    cuuint64_t strides[4] = {256, 128, 2048, (cuuint64_t)qpk * 256};
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)(qpk / 8), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -52,7 +52,8 @@ extern "C" {
 #define MSA_STATUS_PAGE_RANGE 0x4u   /* a page_table entry outside [0, num_pages): block skipped (fatal) */
 #define MSA_STATUS_PLAN_OVERFLOW 0x8u /* the plan buffer could not hold the schedule (fatal) */
 #define MSA_STATUS_TIMEOUT 0x10u      /* a bounded wait inside a kernel gave up; output invalid (fatal) */
-#define MSA_STATUS_FATAL_MASK (MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT)
+#define MSA_STATUS_LAUNCH 0x20u       /* a kernel found its shared memory misaligned; nothing written (fatal) */
+#define MSA_STATUS_FATAL_MASK (MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH)
 
 /* K/V storage formats of msa_sparse_attn_fwd */
 #define MSA_KV_BF16 0

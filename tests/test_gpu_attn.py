@@ -27,7 +27,7 @@ def run_gpu(x, spec, kv_format="bf16", k=None, v=None, k_scales=None, v_scales=N
     torch.cuda.synchronize()
     if own:
         st = msa.read_status(status)
-        assert st & 0x18 == 0, f"fatal device status {st:#x} (timeout / plan overflow)"
+        assert st & msa.MSA_STATUS_FATAL_MASK == 0, f"fatal device status {st:#x}"
     return o, lse
 
 
@@ -100,6 +100,27 @@ def test_prefill_custom_scale_and_repeat_calls_are_identical():
     o_ref, l_ref = oracle.sparse_attn(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["q2k"].cpu(), causal=True,
                                       scale=0.05)
     assert_attn_close(o1.view(-1, spec.Hq, 128), l1.view(-1, spec.Hq), o_ref, l_ref, "scale")
+
+
+@pytest.mark.parametrize("spec", [P("split_sink", Sq=1500, Skv=2048, topk=16),
+                                  P("split_qpk2", qpk=2, Hkv=3, Sq=2000, Skv=2048, topk=8, pattern="uniform")],
+                         ids=lambda s: s.name)
+def test_partial_then_combine_equals_fwd(spec):
+    """msa_sparse_attn_fwd_partial then msa_sparse_attn_combine, called
+    separately, give msa_sparse_attn_fwd's output bit for bit."""
+    import block_sparse_top_gb300 as msa
+    x = synth.make_prefill_inputs(spec, device=DEV)
+    csr = msa.build_k2q_csr(x["q2k"], spec.Skv, spec.qpk)
+    ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, DEV)
+    o2 = torch.empty_like(x["q"])
+    l2 = torch.empty((spec.B, spec.Sq, spec.Hq), dtype=torch.float32, device=DEV)
+    msa.sparse_attn_fwd_partial(x["q"], x["k"], x["v"], csr, causal=True, workspace=ws)
+    msa.sparse_attn_combine(csr, spec.Hq, o2, l2, ws)
+    o1, l1 = msa.sparse_attn_fwd(x["q"], x["k"], x["v"], csr, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o_ref, l_ref = oracle.sparse_attn(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["q2k"].cpu(), causal=True)
+    assert_attn_close(o2.view(-1, spec.Hq, 128), l2.view(-1, spec.Hq), o_ref, l_ref, spec.name)
 
 
 MID = [

@@ -45,6 +45,11 @@ def _check_plan(csr):
             assert (h, x) not in seen
             seen.add((h, x))
     assert np.array_equal(covered, np.diff(rp, axis=1))
+    # units run head-major, then wave by wave
+    W = int(plan[4])
+    qi = csr.q_indices.cpu().numpy()
+    order = [(int(h), int(qi[h, start]) // W) for h, r, start, count in units]
+    assert order == sorted(order)
 
 
 CASES = [
