@@ -141,8 +141,7 @@ extern "C" int msa_sparse_attn_fwd_partial(const void *q, const void *k, const v
                                : make_q_map(&mq, q, (int64_t)B * Sq * Hq, 1);
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
-        if (!make_kv_map(&mk, k, Hkv, (int64_t)B * Skv, (int64_t)Hkv * kD) ||
-            !make_kv_map(&mv, v, Hkv, (int64_t)B * Skv, (int64_t)Hkv * kD))
+        if (!make_kv_map(&mk, k, Hkv, (int64_t)B * Skv) || !make_kv_map(&mv, v, Hkv, (int64_t)B * Skv))
             return MSA_ERR_CUDA;
         return launch_tiles<MSA_KV_BF16>(mk, mv, mq, t, grid, stream);
     }

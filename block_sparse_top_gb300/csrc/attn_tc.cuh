@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         };
         // every plan entry this CTA will read, into L2 up front (16 bytes each)
         for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) tc::prefetch_l2(p.units + u);
-        const uint64_t keep = tc::l2_policy_evict_last();
+        const uint64_t keep = tc::l2_policy_evict_last();  // gather4 Q rows
         Cursor cur{(int)blockIdx.x, 0, Unit{}}, ahead{(int)blockIdx.x, 0, Unit{}};
         if (cur.u < work) cur.x = ahead.x = load_unit(p, cur.u);
         for (int d = 0; d < kIdAhead; ++d) {
@@ -216,10 +216,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         tc::mbar_arrive_expect_tx(bar(KV_FULL + kb), 65536);
                         const int row = x.b * p.Skv + x.tok0;
                         const uint32_t ks = base + kSmK + kb * 32768, vs = base + kSmV + kb * 32768;
-                        tc::tma_load_3d_hint(ks, &tm_k, bar(KV_FULL + kb), 0, x.h, row, keep);
-                        tc::tma_load_3d_hint(ks + 16384, &tm_k, bar(KV_FULL + kb), 64, x.h, row, keep);
-                        tc::tma_load_3d_hint(vs, &tm_v, bar(KV_FULL + kb), 0, x.h, row, keep);
-                        tc::tma_load_3d_hint(vs + 16384, &tm_v, bar(KV_FULL + kb), 64, x.h, row, keep);
+                        tc::tma_load_4d(ks, &tm_k, bar(KV_FULL + kb), 0, row, 0, x.h);
+                        tc::tma_load_4d(vs, &tm_v, bar(KV_FULL + kb), 0, row, 0, x.h);
                         kv_armed[kb] = (ui >> 1) & 1;
                     }
                 }
@@ -377,7 +375,11 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             // polls until S_ci (if s_cj >= 0) and the pending PV are both issued
             auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par) -> bool {
                 bool s_done = s_cj < 0, pv_done = pv_ci < 0, kv_ok = !need_kv;
-                for (uint32_t i = 0; i < tc::kPollLimit; ++i) {
+                const uint64_t t0 = tc::global_ns();
+                for (uint32_t i = 0;; ++i) {
+                    // back off between polls: a spinning lane would take issue
+                    // slots from the softmax warps sharing its sub-partition
+                    if (i > 0) __nanosleep(32);
                     if (!s_done) {
                         if (!kv_ok) kv_ok = tc::mbar_test(bar(KV_FULL + kbj), (uint32_t)kv_par);
                         if (kv_ok && tc::mbar_test(bar(Q_FULL + s_cj % kNQ), (s_cj / kNQ) & 1)) {
@@ -390,7 +392,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         pv_done = true;
                     }
                     if (s_done && pv_done) return true;
-                    if ((i & 255u) == 255u && *abort_flag) return false;
+                    if ((i & 63u) == 63u) {
+                        if (*abort_flag) return false;
+                        if (tc::global_ns() - t0 > tc::kWaitLimitNs) break;
+                    }
                 }
                 *abort_flag = 1;
                 set_status(p.status, MSA_STATUS_TIMEOUT);

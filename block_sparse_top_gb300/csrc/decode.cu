@@ -341,10 +341,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (ok) {
                     const uint32_t st = base + s * 65536;
                     tc::mbar_arrive_expect_tx(full(s), 65536);
-                    tc::tma_load_3d(st, &tm_k, full(s), 0, gi.h, page * kBlk);
-                    tc::tma_load_3d(st + 16384, &tm_k, full(s), 64, gi.h, page * kBlk);
-                    tc::tma_load_3d(st + 32768, &tm_v, full(s), 0, gi.h, page * kBlk);
-                    tc::tma_load_3d(st + 49152, &tm_v, full(s), 64, gi.h, page * kBlk);
+                    tc::tma_load_4d(st, &tm_k, full(s), 0, page * kBlk, 0, gi.h);
+                    tc::tma_load_4d(st + 32768, &tm_v, full(s), 0, page * kBlk, 0, gi.h);
                 } else {
                     set_status(p.status, MSA_STATUS_PAGE_RANGE);
                     tc::mbar_arrive(full(s));
@@ -642,8 +640,8 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     p.scale_log2 = p.scale * 1.4426950408889634f;
 
     CUtensorMap mk, mv;
-    if (!make_kv_map(&mk, k_pool, Hkv, (int64_t)num_pages * kBlk, (int64_t)Hkv * kD) ||
-        !make_kv_map(&mv, v_pool, Hkv, (int64_t)num_pages * kBlk, (int64_t)Hkv * kD))
+    if (!make_kv_map(&mk, k_pool, Hkv, (int64_t)num_pages * kBlk) ||
+        !make_kv_map(&mv, v_pool, Hkv, (int64_t)num_pages * kBlk))
         return MSA_ERR_CUDA;
 
     MSA_CUDA_TRY(cudaMemsetAsync(p.counters, 0, sizeof(int32_t) * (size_t)d.groups, stream));

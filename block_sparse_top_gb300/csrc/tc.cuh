@@ -50,17 +50,28 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Poll budget of a multi-barrier polling loop (about a second of polls).
-constexpr uint32_t kPollLimit = 1u << 26;
+// Waits are bounded in time: a wait that has not completed within
+// kWaitLimitNs of the device's global nanosecond timer gives up.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
 
-// Bounded wait: gives up after `limit` polls, raises the CTA abort flag and
-// the device status bit so every role can drain and exit.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Bounded wait: gives up after kWaitLimitNs, raises the CTA abort flag and
+// the device status bit so every role can drain and exit; returns false at
+// once when another role has raised the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort_flag, uint32_t *status,
                                           uint32_t status_bit) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(addr, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(addr, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
+        if ((i & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) break;
+        }
     }
     *abort_flag = 1;
     set_status(status, status_bit);
@@ -127,6 +138,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
         "%4}], [%2], %5;\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+        "%6}], [%2];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int c0, int c1,
@@ -302,16 +321,18 @@ inline EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// 3D bf16 map over rows of D=128 elements: dims {128, heads, tokens},
-// box {64, 1, 128} (one 128-byte-swizzled [128 token][64 element] half tile).
-inline bool make_kv_map(CUtensorMap *map, const void *base, int heads, int64_t tokens, int64_t token_stride_elems) {
+// 4D bf16 view of a K or V cache [tokens][heads][128]: dims {64 elements,
+// tokens, 2 column halves, heads} with byte strides {heads*256, 128, 256} and
+// box {64, 128, 2, 1}: one copy brings a whole 128-token block of one head as
+// [half][128 tokens][128 B], 128-byte swizzled (halves 16384 bytes apart).
+inline bool make_kv_map(CUtensorMap *map, const void *base, int heads, int64_t tokens) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)token_stride_elems * 2};
-    cuuint32_t box[3] = {64, 1, 128};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    cuuint64_t dims[4] = {64, (cuuint64_t)tokens, 2, (cuuint64_t)heads};
+    cuuint64_t strides[3] = {(cuuint64_t)heads * 256, 128, 256};
+    cuuint32_t box[4] = {64, 128, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
