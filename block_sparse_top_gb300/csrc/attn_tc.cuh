@@ -34,7 +34,6 @@
 namespace msa {
 
 struct TcParams {
-    const __nv_bfloat16 *q;               // [B*Sq][Hq][D]
     const uint8_t *k_packed, *v_packed;   // NVFP4 only
     const uint8_t *k_scales, *v_scales;   // NVFP4 only
     const int32_t *qsplit;
@@ -42,45 +41,51 @@ struct TcParams {
     const PlanUnit *units;
     __nv_bfloat16 *o_part;                // split partials, layout in combine.cuh
     float2 *stat_part;                    // split statistics, layout in combine.cuh
+    // paged KV (decode): per-sequence used length and each unit's physical
+    // page (-1: invalid entry, the unit's keys are skipped); null otherwise
+    const int32_t *seqused;
+    const int32_t *unit_page;
     uint32_t *status;
-    int B, Sq, Skv, Hq, Hkv, qpk, lqpk, topk, nblk, causal;  // lqpk = log2(qpk)
+    int B, Sq, Skv, Hq, Hkv, qpk, topk, nblk, causal;
     int64_t cap;
     float scale, scale_log2;
 };
 
 namespace tck {
 
-constexpr int kNQ = 3;
 constexpr int kIdAhead = 4;  // chunks of query ids the loader fetches ahead
 constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3;
-constexpr uint32_t kSmK = 0, kSmV = 65536, kSmQ = 131072;
-constexpr uint32_t kSmBar = kSmQ + kNQ * 32768;
-enum : int {
-    KV_FULL = 0,
-    KV_EMPTY = 2,
-    Q_FULL = 4,
-    Q_EMPTY = 4 + kNQ,
-    S_FULL = 4 + 2 * kNQ,
-    P_FULL = S_FULL + 2,
-    O_FULL = P_FULL + 2,
-    O_EMPTY = O_FULL + 2,
-    DRAIN = O_EMPTY + 2,
-    NBAR = DRAIN + 1
+
+// Shared memory of a kernel with NKV K/V stages and NQ Q stages (32 KB tiles):
+// K [NKV] | V [NKV] | Q [NQ] | mbarriers | TMEM slot | abort flag.
+template <int NKV, int NQ>
+struct Layout {
+    static constexpr uint32_t K = 0, V = NKV * 32768u, Q = 2u * NKV * 32768u, BAR = Q + NQ * 32768u;
+    enum : int {
+        KV_FULL = 0,
+        KV_EMPTY = NKV,
+        Q_FULL = 2 * NKV,
+        Q_EMPTY = 2 * NKV + NQ,
+        S_FULL = 2 * NKV + 2 * NQ,
+        P_FULL = S_FULL + 2,
+        O_FULL = P_FULL + 2,
+        O_EMPTY = O_FULL + 2,
+        DRAIN = O_EMPTY + 2,
+        NBAR = DRAIN + 1
+    };
+    static constexpr uint32_t TSLOT = BAR + 8 * NBAR, ABORT = TSLOT + 4, BYTES = ABORT + 4;
+    // The dynamic shared memory base is 1024-byte aligned (no static shared
+    // memory); the kernel checks this instead of reserving slack.
+    static_assert(BYTES <= 232448, "shared memory budget");
 };
-constexpr uint32_t kSmTslot = kSmBar + 8 * NBAR;
-constexpr uint32_t kSmAbort = kSmTslot + 4;
-constexpr uint32_t kSmBytes = kSmAbort + 4;
-// The dynamic shared memory base is 1024-byte aligned (no static shared
-// memory); the kernel checks this instead of reserving slack.
-static_assert(kSmBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, 0, 1);
 
 struct Unit {
-    int h, b, tok0, start, count, nch;
+    int h, b, tok0, start, count, nch, page;
 };
 
 __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
@@ -93,6 +98,7 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
     x.count = pu.count;
     int qc = 128 / p.qpk;
     x.nch = (pu.count + qc - 1) / qc;
+    x.page = p.unit_page ? p.unit_page[u] : 0;
     return x;
 }
 
@@ -102,11 +108,15 @@ __device__ __forceinline__ int pick4(const int (&v)[4], int s) {
 
 }  // namespace tck
 
-template <int KV_FORMAT>
+// NKV, NQ: K/V and Q stages -- 2 and 3 when units hold several chunks (the
+// K/V block is reused across them), 3 and 1 when every unit is one chunk
+// (paged decode: a new K/V block per chunk, few Q rows).
+template <int KV_FORMAT, int NKV, int NQ>
 __global__ void __launch_bounds__(tck::kThreads, 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
     using namespace tck;
+    using L = Layout<NKV, NQ>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t *const gbase = smem_raw;
@@ -114,31 +124,33 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         if (threadIdx.x == 0) set_status(p.status, MSA_STATUS_LAUNCH);
         return;
     }
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kSmAbort);
-    auto bar = [&](int i) -> uint32_t { return base + kSmBar + 8u * (uint32_t)i; };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + L::ABORT);
+    auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qc = 128 / p.qpk;
     const int work = p.plan->work_count;
 
     if (tid == 0) {
+        for (int i = 0; i < NKV; ++i) {
+            tc::mbar_init(bar(L::KV_FULL + i), KV_FORMAT == MSA_KV_BF16 ? 1 : 32);
+            tc::mbar_init(bar(L::KV_EMPTY + i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bar(KV_FULL + i), KV_FORMAT == MSA_KV_BF16 ? 1 : 32);
-            tc::mbar_init(bar(KV_EMPTY + i), 1);
-            tc::mbar_init(bar(S_FULL + i), 1);
-            tc::mbar_init(bar(P_FULL + i), 128);
-            tc::mbar_init(bar(O_FULL + i), 1);
-            tc::mbar_init(bar(O_EMPTY + i), 128);
+            tc::mbar_init(bar(L::S_FULL + i), 1);
+            tc::mbar_init(bar(L::P_FULL + i), 128);
+            tc::mbar_init(bar(L::O_FULL + i), 1);
+            tc::mbar_init(bar(L::O_EMPTY + i), 128);
         }
-        for (int i = 0; i < kNQ; ++i) {
-            tc::mbar_init(bar(Q_FULL + i), 1);
-            tc::mbar_init(bar(Q_EMPTY + i), 1);
+        for (int i = 0; i < NQ; ++i) {
+            tc::mbar_init(bar(L::Q_FULL + i), 1);
+            tc::mbar_init(bar(L::Q_EMPTY + i), 1);
         }
-        tc::mbar_init(bar(DRAIN), 1);
+        tc::mbar_init(bar(L::DRAIN), 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
     if (warp == kWarpMma) {
-        tc::tmem_alloc(base + kSmTslot, 512);
+        tc::tmem_alloc(base + L::TSLOT, 512);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
@@ -151,12 +163,13 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + kSmTslot);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + L::TSLOT);
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loader
         int ci = 0, ui = 0;
-        int kv_armed[2] = {-1, -1};
+        int kv_armed[NKV];
+        for (int i = 0; i < NKV; ++i) kv_armed[i] = -1;
         bool ok = true;
         const int G = gridDim.x;
         // query ids of chunk c of unit x: lane l holds queries l, l+32, l+64, l+96
@@ -206,19 +219,24 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         auto step = [&](const int (&ids)[4], int (&nids)[4]) -> bool {
             const Unit &x = cur.x;
             const int c = cur.c;
-            const int kb = ui & 1;
+            const int kb = ui % NKV;
             if (c == 0 && KV_FORMAT == MSA_KV_BF16) {
                 if (lane == 0) {
-                    if (ui >= 2)
-                        ok = tc::mbar_wait(bar(KV_EMPTY + kb), ((ui >> 1) - 1) & 1, abort_flag, p.status,
+                    if (ui >= NKV)
+                        ok = tc::mbar_wait(bar(L::KV_EMPTY + kb), ((ui / NKV) - 1) & 1, abort_flag, p.status,
                                            MSA_STATUS_TIMEOUT);
                     if (ok) {
-                        tc::mbar_arrive_expect_tx(bar(KV_FULL + kb), 65536);
-                        const int row = x.b * p.Skv + x.tok0;
-                        const uint32_t ks = base + kSmK + kb * 32768, vs = base + kSmV + kb * 32768;
-                        tc::tma_load_4d(ks, &tm_k, bar(KV_FULL + kb), 0, row, 0, x.h);
-                        tc::tma_load_4d(vs, &tm_v, bar(KV_FULL + kb), 0, row, 0, x.h);
-                        kv_armed[kb] = (ui >> 1) & 1;
+                        // token row: dense [B][Skv] layout, or the unit's page of the pool
+                        const int row = p.unit_page ? x.page * kBlk : x.b * p.Skv + x.tok0;
+                        if (!p.unit_page || x.page >= 0) {
+                            tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), 65536);
+                            const uint32_t ks = base + L::K + kb * 32768, vs = base + L::V + kb * 32768;
+                            tc::tma_load_4d(ks, &tm_k, bar(L::KV_FULL + kb), 0, row, 0, x.h);
+                            tc::tma_load_4d(vs, &tm_v, bar(L::KV_FULL + kb), 0, row, 0, x.h);
+                        } else {
+                            tc::mbar_arrive(bar(L::KV_FULL + kb));  // invalid page: no copy, keys masked
+                        }
+                        kv_armed[kb] = (ui / NKV) & 1;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -232,9 +250,9 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             if (nxt.u < work) fetch_ids(nxt.x, nxt.c, nids);
             prefetch_ids(ahead);
             advance(ahead);
-            const int qs = ci % kNQ;
-            if (lane == 0 && ci >= kNQ)
-                ok = tc::mbar_wait(bar(Q_EMPTY + qs), ((ci / kNQ) - 1) & 1, abort_flag, p.status,
+            const int qs = ci % NQ;
+            if (lane == 0 && ci >= NQ)
+                ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((ci / NQ) - 1) & 1, abort_flag, p.status,
                                    MSA_STATUS_TIMEOUT);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) return false;
@@ -243,16 +261,19 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             // 5D box per query holds its whole group (row octets 2048 bytes
             // apart, column halves 1024 apart); qpk < 8: four arbitrary rows
             // per tile::gather4 copy (rows 128 bytes apart, halves 16384).
-            // Padding rows repeat the chunk's first query.
-            const uint32_t qt = base + kSmQ + qs * 32768;
+            // qpk >= 8 loads only the chunk's real queries (padding rows keep
+            // stale data; their keys are all masked, so they give P = 0);
+            // gather4 rows of padding repeat the chunk's first query.
+            const uint32_t qt = base + L::Q + qs * 32768;
             const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
-            if (lane == 0) tc::mbar_arrive_expect_tx(bar(Q_FULL + qs), 32768);
+            const int nq = min(qc, x.count - c * qc);
+            if (lane == 0)
+                tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs), p.qpk >= 8 ? (uint32_t)(nq * p.qpk * 256) : 32768u);
             if (p.qpk >= 8) {
-                for (int qi = 0; qi < qc; ++qi) {
-                    int gq = __shfl_sync(0xffffffffu, ids[0], qi);
-                    if (gq < 0) gq = first;
+                for (int qi = 0; qi < nq; ++qi) {
+                    const int gq = __shfl_sync(0xffffffffu, ids[0], qi);
                     if (lane == 0)
-                        tc::tma_load_5d(qt + (uint32_t)(qi * p.qpk * 256), &tm_q, bar(Q_FULL + qs), 0, 0, 0, 0,
+                        tc::tma_load_5d(qt + (uint32_t)(qi * p.qpk * 256), &tm_q, bar(L::Q_FULL + qs), 0, 0, 0, 0,
                                         gq * p.Hkv + x.h);
                 }
             } else {
@@ -268,8 +289,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
                     }
                     if (lane == 0) {
-                        tc::tma_gather4_hint(qt + j * 512, &tm_q, bar(Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
-                        tc::tma_gather4_hint(qt + 16384 + j * 512, &tm_q, bar(Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
+                        tc::tma_gather4_hint(qt + j * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
+                        tc::tma_gather4_hint(qt + 16384 + j * 512, &tm_q, bar(L::Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
                                              keep);
                     }
                 }
@@ -289,8 +310,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         // drain outstanding copies before the CTA can exit
         if (lane == 0) {
             volatile int dummy = 0;
-            for (int i = 0; i < 2; ++i)
-                if (kv_armed[i] >= 0) tc::mbar_wait(bar(KV_FULL + i), (uint32_t)kv_armed[i], &dummy, p.status, 0);
+            for (int i = 0; i < NKV; ++i)
+                if (kv_armed[i] >= 0) tc::mbar_wait(bar(L::KV_FULL + i), (uint32_t)kv_armed[i], &dummy, p.status, 0);
         }
         __syncwarp();
     } else if (warp == kWarpDequant) {
@@ -300,9 +321,9 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             bool ok = true;
             for (int u = blockIdx.x; u < work && ok; u += gridDim.x, ++ui) {
                 const Unit x = load_unit(p, u);
-                const int kb = ui & 1;
-                if (ui >= 2)
-                    ok = tc::mbar_wait(bar(KV_EMPTY + kb), ((ui >> 1) - 1) & 1, abort_flag, p.status,
+                const int kb = ui % NKV;
+                if (ui >= NKV)
+                    ok = tc::mbar_wait(bar(L::KV_EMPTY + kb), ((ui / NKV) - 1) & 1, abort_flag, p.status,
                                        MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -319,7 +340,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         uint2 w = *reinterpret_cast<const uint2 *>(pk + rr * 64 + g * 8);
                         nvfp4_group_to_bf16(w, sc[rr * 8 + g], lo, hi);
                     }
-                    const uint32_t tile = base + (isv ? kSmV : kSmK) + kb * 32768 + (g >> 2) * 16384;
+                    const uint32_t tile = base + (isv ? L::V : L::K) + kb * 32768 + (g >> 2) * 16384;
                     const int cch = (g & 3) * 2;
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(tile + tc::sw128_off(r, cch)),
                                  "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w));
@@ -327,7 +348,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                                  "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w));
                 }
                 tc::fence_proxy_async();
-                tc::mbar_arrive(bar(KV_FULL + kb));
+                tc::mbar_arrive(bar(L::KV_FULL + kb));
             }
         }
     } else if (warp == kWarpMma) {
@@ -344,24 +365,24 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             const uint32_t q_sbo = p.qpk >= 8 ? 2048u : 1024u, q_half = p.qpk >= 8 ? 1024u : 16384u;
             auto pv_ready = [&](int cj) -> bool {
                 const int b = cj & 1;
-                return tc::mbar_test(bar(P_FULL + b), (cj >> 1) & 1) &&
-                       (cj < 2 || tc::mbar_test(bar(O_EMPTY + b), ((cj >> 1) - 1) & 1));
+                return tc::mbar_test(bar(L::P_FULL + b), (cj >> 1) & 1) &&
+                       (cj < 2 || tc::mbar_test(bar(L::O_EMPTY + b), ((cj >> 1) - 1) & 1));
             };
             auto issue_pv = [&](int cj, int kbj, int last) {
                 const int b = cj & 1;
                 tc::fence_after_sync();
-                const uint32_t vs = base + kSmV + kbj * 32768;
+                const uint32_t vs = base + L::V + kbj * 32768;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
                                tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, kk > 0);
-                tc::mma_commit(bar(O_FULL + b));
-                if (last) tc::mma_commit(bar(KV_EMPTY + kbj));
+                tc::mma_commit(bar(L::O_FULL + b));
+                if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
             auto issue_s = [&](int cj, int kbj) {
-                const int b = cj & 1, qs = cj % kNQ;
+                const int b = cj & 1, qs = cj % NQ;
                 tc::fence_after_sync();
-                const uint32_t qt = base + kSmQ + qs * 32768, ks = base + kSmK + kbj * 32768;
+                const uint32_t qt = base + L::Q + qs * 32768, ks = base + L::K + kbj * 32768;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -369,8 +390,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + qoff, 16, q_sbo),
                                tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
                 }
-                tc::mma_commit(bar(S_FULL + b));
-                tc::mma_commit(bar(Q_EMPTY + qs));
+                tc::mma_commit(bar(L::S_FULL + b));
+                tc::mma_commit(bar(L::Q_EMPTY + qs));
             };
             // polls until S_ci (if s_cj >= 0) and the pending PV are both issued
             auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par) -> bool {
@@ -381,8 +402,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     // slots from the softmax warps sharing its sub-partition
                     if (i > 0) __nanosleep(32);
                     if (!s_done) {
-                        if (!kv_ok) kv_ok = tc::mbar_test(bar(KV_FULL + kbj), (uint32_t)kv_par);
-                        if (kv_ok && tc::mbar_test(bar(Q_FULL + s_cj % kNQ), (s_cj / kNQ) & 1)) {
+                        if (!kv_ok) kv_ok = tc::mbar_test(bar(L::KV_FULL + kbj), (uint32_t)kv_par);
+                        if (kv_ok && tc::mbar_test(bar(L::Q_FULL + s_cj % NQ), (s_cj / NQ) & 1)) {
                             issue_s(s_cj, kbj);
                             s_done = true;
                         }
@@ -406,9 +427,9 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             for (int u = blockIdx.x; u < work && ok; u += gridDim.x, ++ui) {
                 const Unit x = xnext;
                 if (u + (int)gridDim.x < work) xnext = load_unit(p, u + gridDim.x);
-                const int kb = ui & 1;
+                const int kb = ui % NKV;
                 for (int c = 0; c < x.nch && ok; ++c, ++ci) {
-                    ok = drive(ci, kb, c == 0, (ui >> 1) & 1);
+                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1);
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
@@ -416,9 +437,9 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             }
             if (ok && pv_ci >= 0) drive(-1, 0, false, 0);
             // all issued MMAs complete before tensor memory is released
-            tc::mma_commit(bar(DRAIN));
+            tc::mma_commit(bar(L::DRAIN));
             volatile int dummy = 0;
-            tc::mbar_wait(bar(DRAIN), 0, &dummy, p.status, MSA_STATUS_TIMEOUT);
+            tc::mbar_wait(bar(L::DRAIN), 0, &dummy, p.status, MSA_STATUS_TIMEOUT);
         }
         __syncwarp();
     } else {
@@ -442,7 +463,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 const int qi = R / p.qpk, idx = c * qc + qi;
                 const bool valid = idx < x.count;
                 const int packed = valid ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
-                ok = tc::mbar_wait(bar(S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -452,10 +473,13 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 const int gq = packed & 0xFFFFFF;
                 const int split = (packed >> 24) & 0xFF;
                 int nvis = 0;
-                if (valid) {
+                if (valid && (!p.unit_page || x.page >= 0)) {
+                    // keys visible to query sq of a sequence of kv_len keys
+                    // (bottom-right causal: up to key sq + kv_len - Sq)
                     const int sq = gq % p.Sq;
-                    int64_t limit = (int64_t)p.Skv - 1;
-                    if (p.causal) limit = min(limit, (int64_t)sq + (int64_t)(p.Skv - p.Sq));
+                    const int64_t kv_len = p.seqused ? (int64_t)__ldg(p.seqused + x.b) : (int64_t)p.Skv;
+                    int64_t limit = kv_len - 1;
+                    if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
                     const int64_t nv = limit - x.tok0 + 1;
                     nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                 }
@@ -495,16 +519,16 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::tmem_st64(s_addr, r);
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
-                tc::mbar_arrive(bar(P_FULL + wg));
+                tc::mbar_arrive(bar(L::P_FULL + wg));
                 // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
-                ok = tc::mbar_wait(bar(O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc::fence_after_sync();
                 tc::tmem_ld128(o_addr, r);
                 tc::tmem_ld_wait();
                 tc::fence_before_sync();
-                tc::mbar_arrive(bar(O_EMPTY + wg));  // O is in registers: the next PV may start
+                tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is in registers: the next PV may start
                 if (valid) {
                     // grouped layout: for a fixed (split, c) the heads of one group are
                     // contiguous, so each store instruction writes whole runs

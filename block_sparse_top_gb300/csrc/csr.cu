@@ -20,6 +20,8 @@
 // ordered by KV head, then by wave: wave w holds the queries [w*W, (w+1)*W)
 // with W sized so that one (head, wave) pass writes about 32 MiB of split
 // partials, which stay in L2 until they are combined.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace msa {
@@ -93,11 +95,14 @@ __global__ void csr_hist_kernel(const int32_t *__restrict__ q2k, const int32_t *
 // Column scan: for each (h, b, j) turn the tile counts into exclusive offsets
 // within the row and write the row total to row_ptr[h][b*nblk + j + 1].
 // Block (32, 32): threadIdx.x = block id offset, threadIdx.y = tile range.
+// blockDim = (32 block columns, ty tile slices): slice y sums its run of
+// tiles, thread y = 0 scans the ty slice sums, each slice rewrites its run.
 __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_ptr, CsrShape s) {
     __shared__ int32_t part[32][33];
+    const int ty = blockDim.y;
     int j = blockIdx.x * 32 + threadIdx.x;
     int b = blockIdx.y, h = blockIdx.z;
-    int per = (s.ntiles + 31) / 32;
+    int per = (s.ntiles + ty - 1) / ty;
     int t0 = threadIdx.y * per;
     int t1 = min(t0 + per, s.ntiles);
     int32_t *base = tile_counts + ((int64_t)h * s.B + b) * s.ntiles * (int64_t)s.nblk;
@@ -108,7 +113,7 @@ __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *_
     __syncthreads();
     if (threadIdx.y == 0) {
         int32_t run = 0;
-        for (int y = 0; y < 32; ++y) {
+        for (int y = 0; y < ty; ++y) {
             int32_t v = part[y][threadIdx.x];
             part[y][threadIdx.x] = run;
             run += v;
@@ -127,19 +132,37 @@ __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *_
 }
 
 // In-place scan of n int32 per blockIdx.x segment (segment stride `stride`),
-// one CTA of 1024 threads per segment.  exclusive != 0: out[i] = sum_{<i};
-// the segment total goes to totals[blockIdx.x] when totals != nullptr.
-__global__ void segment_scan_kernel(int32_t *data, int64_t n, int64_t stride, int exclusive, int32_t *totals) {
+// one CTA of 1024 threads per segment.  Each pass stages kScanItems * 1024
+// values through shared memory with coalesced loads and stores; thread t
+// scans values [t*kScanItems, (t+1)*kScanItems) of the pass.  exclusive != 0:
+// out[i] = sum_{<i}; the segment total goes to totals[blockIdx.x] when
+// totals != nullptr.
+constexpr int kScanItems = 8;
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(int32_t *data, int64_t n, int64_t stride,
+                                                                    int exclusive, int32_t *totals) {
+    __shared__ int32_t tile[kScanItems * kScanThreads + kScanItems * kScanThreads / 32];  // padded rows
     __shared__ int32_t warp_sums[32];
-    __shared__ int32_t carry_s;
     int32_t *d = data + blockIdx.x * stride;
-    if (threadIdx.x == 0) carry_s = 0;
-    __syncthreads();
-    int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int64_t base = 0; base < n; base += blockDim.x) {
-        int64_t i = base + threadIdx.x;
-        int32_t v = (i < n) ? d[i] : 0;
-        int32_t x = v;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // padding of one word per 32 keeps a thread's run free of bank conflicts
+    auto slot = [](int i) { return i + (i >> 5); };
+    int32_t carry = 0;  // identical in every thread
+    for (int64_t base = 0; base < n; base += (int64_t)kScanThreads * kScanItems) {
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int i = k * kScanThreads + tid;
+            tile[slot(i)] = (base + i < n) ? d[base + i] : 0;
+        }
+        __syncthreads();
+        int32_t v[kScanItems];
+        int32_t tsum = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            v[k] = tile[slot(tid * kScanItems + k)];
+            tsum += v[k];
+        }
+        int32_t x = tsum;  // inclusive scan of the thread sums
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int32_t y = __shfl_up_sync(0xffffffffu, x, o);
@@ -157,14 +180,23 @@ __global__ void segment_scan_kernel(int32_t *data, int64_t n, int64_t stride, in
             warp_sums[lane] = w;
         }
         __syncthreads();
-        int32_t carry = carry_s;
-        int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-        if (i < n) d[i] = exclusive ? incl - v : incl;
+        int32_t run = carry + x - tsum + (warp > 0 ? warp_sums[warp - 1] : 0);  // exclusive start of the thread
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int32_t incl = run + v[k];
+            tile[slot(tid * kScanItems + k)] = exclusive ? run : incl;
+            run = incl;
+        }
+        carry += warp_sums[31];
         __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) carry_s = incl;
-        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int i = k * kScanThreads + tid;
+            if (base + i < n) d[base + i] = tile[slot(i)];
+        }
+        __syncthreads();  // tile and warp_sums are rewritten by the next pass
     }
-    if (totals && threadIdx.x == 0) totals[blockIdx.x] = carry_s;
+    if (totals && threadIdx.x == 0) totals[blockIdx.x] = carry;
 }
 
 __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_t *__restrict__ seqused, CsrShape s,
@@ -379,7 +411,7 @@ extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int
     csr_hist_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, split_counts, status_dev);
     MSA_LAUNCH_CHECK();
     dim3 cgrid((unsigned)ceil_div(s.nblk, 32), B, Hkv);
-    csr_colscan_kernel<<<cgrid, dim3(32, 32), 0, stream>>>(tile_counts, row_ptr, s);
+    csr_colscan_kernel<<<cgrid, dim3(32, (unsigned)std::min(32, s.ntiles)), 0, stream>>>(tile_counts, row_ptr, s);
     MSA_LAUNCH_CHECK();
     // row_ptr[h][0] = 0, then inclusive scan of the row totals in [1, rows]
     MSA_CUDA_TRY(cudaMemset2DAsync(row_ptr, sizeof(int32_t) * (s.rows + 1), 0, sizeof(int32_t), Hkv, stream));

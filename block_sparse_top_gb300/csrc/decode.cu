@@ -1,4 +1,7 @@
-// decode.cu -- block-sparse paged decode.
+// decode.cu -- block-sparse paged decode by per-group block unions, the
+// kernel behind msa_sparse_attn_paged_fwd_noalloc (its scratch is small
+// enough for a static device array; msa_sparse_attn_paged_fwd runs the
+// prefill tile pipeline over logical blocks instead, see attn.cu).
 //
 // A group is (sequence b, KV head h, 128/qhead_per_kv consecutive queries):
 // 128 query-head rows that share the KV head.  Three launches:
@@ -587,24 +590,21 @@ DecWorkspace dec_workspace_layout(const DecShape &d) {
 }
 
 }  // namespace
-}  // namespace msa
 
-using namespace msa;
-
-extern "C" size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk,
-                                                           int max_pages) {
+// Scratch bytes of union_paged_fwd for a shape (0: unsupported).
+size_t union_paged_fwd_scratch(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages) {
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || D != kD || topk <= 0 || max_pages <= 0 || Hq % Hkv) return 0;
     const int qpk = Hq / Hkv;
     if (!supported_qpk(qpk)) return 0;
     return dec_workspace_layout(dec_shape(B, Sq, Hkv, qpk, topk, max_pages)).bytes;
 }
 
-extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
-                                         const int32_t *page_table, int max_pages, const int32_t *seqused_k,
-                                         const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
-                                         int topk, int causal, float softmax_scale, void *o, float *lse,
-                                         void *workspace, size_t ws_bytes, uint32_t *status_dev,
-                                         cudaStream_t stream) {
+// Paged decode by per-group block unions (union, scan and main kernels
+// above), in the scratch it is given.
+int union_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages, const int32_t *page_table,
+                    int max_pages, const int32_t *seqused_k, const int32_t *q2k, int B, int Sq, int Hq, int Hkv,
+                    int D, int page_size, int topk, int causal, float softmax_scale, void *o, float *lse,
+                    void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
     if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !q2k || !o || !workspace) return MSA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages <= 0 || topk <= 0 || Hq % Hkv)
         return MSA_ERR_INVALID_ARG;
@@ -660,13 +660,16 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     return MSA_OK;
 }
 
+}  // namespace msa
+
 // ---------------------------------------------------------------------------
 // Paged decode without a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the point where they run a
 // decode step: a serving loop whose memory is fixed at start-up, or code that
-// must not call cudaMalloc while other work is queued.  This variant keeps
-// its scratch (split counters and partials) in one file-scope device array of
+// must not call cudaMalloc while other work is queued.  This variant runs the
+// per-group union decode (whose scratch is small) and keeps that scratch
+// (block unions, split counters and partials) in one file-scope device array of
 // kNoAllocScratchBytes, which every GPU that loads the library holds until
 // the process exits.  The array's address is looked up once per device with
 // that device current (cudaGetSymbolAddress), on the first call made on that
@@ -708,12 +711,12 @@ extern "C" int msa_sparse_attn_paged_fwd_noalloc(const void *q, const void *k_po
                                                  int Hq, int Hkv, int D, int page_size, int topk, int causal,
                                                  float softmax_scale, void *o, float *lse, uint32_t *status_dev,
                                                  cudaStream_t stream) {
-    size_t need = msa_sparse_attn_paged_fwd_workspace_size(B, Sq, Hq, Hkv, D, topk, max_pages);
+    size_t need = msa::union_paged_fwd_scratch(B, Sq, Hq, Hkv, D, topk, max_pages);
     if (need == 0) return MSA_ERR_UNSUPPORTED;
     if (need > msa::kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // shape needs more than the static scratch
     void *scratch = msa::paged_scratch_for_current_device();
     if (!scratch) return MSA_ERR_CUDA;
-    return msa_sparse_attn_paged_fwd(q, k_pool, v_pool, num_pages, page_table, max_pages, seqused_k, q2k, B, Sq, Hq,
-                                     Hkv, D, page_size, topk, causal, softmax_scale, o, lse, scratch,
-                                     msa::kNoAllocScratchBytes, status_dev, stream);
+    return msa::union_paged_fwd(q, k_pool, v_pool, num_pages, page_table, max_pages, seqused_k, q2k, B, Sq, Hq, Hkv,
+                                D, page_size, topk, causal, softmax_scale, o, lse, scratch,
+                                msa::kNoAllocScratchBytes, status_dev, stream);
 }

@@ -169,7 +169,14 @@ int msa_sparse_attn_combine(const int32_t *split_counts, int B, int Sq, int Hq, 
  *   seqused_k  [B] int32, device (1 <= seqused_k[b] <= max_pages*page_size).
  *   q2k        [B][Hkv][Sq][topk] int32, device; ids >= ceil(seqused_k/page) are padding.
  *   o          [B*Sq][Hq][D] bf16; lse [B*Sq][Hq] fp32 or NULL.
- *   workspace  msa_sparse_attn_paged_fwd_workspace_size() bytes.
+ *   workspace  msa_sparse_attn_paged_fwd_workspace_size() bytes: the k->q
+ *              CSR over logical blocks and its plan, each plan unit's page,
+ *              and the split partials (topk per query head).
+ * The work is the prefill's: msa_build_k2q_csr over (KV head, sequence,
+ * logical block) with Skv = max_pages*page_size and seqused_k, a lookup of
+ * each unit's physical page, the attention tiles over the pool (page entries
+ * outside [0, num_pages) set MSA_STATUS_PAGE_RANGE and their block is
+ * skipped), then the LSE combine.  Max max_pages: 8192.
  */
 size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
 int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
@@ -180,17 +187,20 @@ int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_p
 
 /*
  * msa_sparse_attn_paged_fwd without a workspace argument: the same paged
- * decode, with its scratch (split counters and partials) in a static device
- * array of 32 MiB that every GPU loading the library holds until exit.  The
+ * decode (same arguments and output) computed by a per-group block-union
+ * kernel whose scratch is small, with that scratch (unions, split counters
+ * and partials) in a static device array of 32 MiB that every GPU loading
+ * the library holds until exit.  The
  * source pages have no counterpart; it exists for callers that cannot
  * allocate device memory when they run a decode step (memory fixed at
  * start-up, or no cudaMalloc allowed while work is queued).
  *   - The first call on a device looks up the array's address on that
  *     device (make it before any stream capture); later calls allocate
  *     nothing and call no allocating routine.
- *   - Returns MSA_ERR_WORKSPACE when the shape needs more than 32 MiB
- *     (msa_sparse_attn_paged_fwd_workspace_size() > 33554432); other
- *     arguments and errors are those of msa_sparse_attn_paged_fwd.
+ *   - Returns MSA_ERR_WORKSPACE when the shape's union scratch needs more
+ *     than 32 MiB (8 bytes per (sequence, KV head, group of 128/qhead_per_kv
+ *     queries, selectable block), plus 128 KB per SM); other arguments and
+ *     errors are those of msa_sparse_attn_paged_fwd.
  *   - All calls share the one array: it keeps the last call's contents, the
  *     split counters are cleared on `stream` at the start of each call, and
  *     calls that overlap on the GPU (other streams, other host threads) race.
