@@ -19,8 +19,62 @@
 
 #include "attn_tc.cuh"
 #include "combine.cuh"
+#include "tiles.h"
 
 namespace msa {
+
+// Split partials: topk slots per query head.
+FwdWorkspace fwd_workspace_layout(int B, int Sq, int Hq, int topk, int D) {
+    FwdWorkspace w;
+    size_t rows = (size_t)B * Sq * topk * Hq;
+    w.o_part = 0;
+    w.stat_part = align_up(rows * D * sizeof(__nv_bfloat16), 256);
+    w.bytes = align_up(w.stat_part + rows * sizeof(float2), 256);
+    return w;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return n;
+}
+
+namespace {
+template <int KV_FORMAT, int NKV, int NQ>
+int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
+                 cudaStream_t stream) {
+    const size_t smem = tck::Layout<NKV, NQ>::BYTES;
+    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ><<<grid, tck::kThreads, smem, stream>>>(mk, mv, mq, t);
+    MSA_LAUNCH_CHECK();
+    return MSA_OK;
+}
+}  // namespace
+
+// Builds the tensor maps (Q rows; K and V over kv_tokens token rows) and
+// launches the tile kernel for t, one CTA per SM, at most `capacity` CTAs
+// (the plan's unit capacity).
+int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void *k, const void *v, int64_t kv_tokens,
+                 int kv_format, cudaStream_t stream) {
+    int grid = (int)std::min<int64_t>(capacity, (int64_t)num_sms());
+    if (grid < 1) grid = 1;
+    CUtensorMap mk, mv, mq;
+    memset(&mk, 0, sizeof mk);
+    memset(&mv, 0, sizeof mv);
+    const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, (int64_t)t.B * t.Sq * t.Hkv, t.qpk)
+                                 : make_q_map(&mq, q, (int64_t)t.B * t.Sq * t.Hq, 1);
+    if (!q_ok) return MSA_ERR_CUDA;
+    if (kv_format == MSA_KV_BF16) {
+        if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
+        // paged decode: every unit is one chunk with its own K/V block
+        if (t.unit_page) return launch_tiles<MSA_KV_BF16, 3, 1>(mk, mv, mq, t, grid, stream);
+        return launch_tiles<MSA_KV_BF16, 2, 3>(mk, mv, mq, t, grid, stream);
+    }
+    return launch_tiles<MSA_KV_NVFP4, 2, 3>(mk, mv, mq, t, grid, stream);
+}
+
 namespace {
 
 // Standalone LSE combine: one thread per output piece (group, 8-dim chunk c,
@@ -47,116 +101,6 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4 *__restrict
     const int64_t orow = grp * qpk + j;  // == gq*Hq + h*qpk + j
     o[orow * 16 + c] = out;
     if (c == 0 && lse) lse[orow] = l;
-}
-
-struct FwdWorkspace {
-    size_t o_part, stat_part, bytes;
-};
-
-// Split partials: topk slots per query head.
-FwdWorkspace fwd_workspace_layout(int B, int Sq, int Hq, int topk, int D) {
-    FwdWorkspace w;
-    size_t rows = (size_t)B * Sq * topk * Hq;
-    w.o_part = 0;
-    w.stat_part = align_up(rows * D * sizeof(__nv_bfloat16), 256);
-    w.bytes = align_up(w.stat_part + rows * sizeof(float2), 256);
-    return w;
-}
-
-int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-    return n;
-}
-
-template <int KV_FORMAT, int NKV, int NQ>
-int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
-                 cudaStream_t stream) {
-    const size_t smem = tck::Layout<NKV, NQ>::BYTES;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ><<<grid, tck::kThreads, smem, stream>>>(mk, mv, mq, t);
-    MSA_LAUNCH_CHECK();
-    return MSA_OK;
-}
-
-// Builds the tensor maps (Q rows; K and V over kv_tokens token rows) and
-// launches the tile kernel for t, one CTA per SM at most.
-int tiles_launch(const TcParams &t, const void *q, const void *k, const void *v, int64_t kv_tokens, int kv_format,
-                 cudaStream_t stream) {
-    const int64_t capacity = plan_capacity(t.B, t.Hkv, t.Sq, t.Skv, t.topk, t.qpk);
-    int grid = (int)std::min<int64_t>(capacity, (int64_t)num_sms());
-    if (grid < 1) grid = 1;
-    CUtensorMap mk, mv, mq;
-    memset(&mk, 0, sizeof mk);
-    memset(&mv, 0, sizeof mv);
-    const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, (int64_t)t.B * t.Sq * t.Hkv, t.qpk)
-                                 : make_q_map(&mq, q, (int64_t)t.B * t.Sq * t.Hq, 1);
-    if (!q_ok) return MSA_ERR_CUDA;
-    if (kv_format == MSA_KV_BF16) {
-        if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
-        // paged decode: every unit is one chunk with its own K/V block
-        if (t.unit_page) return launch_tiles<MSA_KV_BF16, 3, 1>(mk, mv, mq, t, grid, stream);
-        return launch_tiles<MSA_KV_BF16, 2, 3>(mk, mv, mq, t, grid, stream);
-    }
-    return launch_tiles<MSA_KV_NVFP4, 2, 3>(mk, mv, mq, t, grid, stream);
-}
-
-// Physical page of every plan unit (paged KV): unit row r = b*max_pages + j
-// is logical block j of sequence b, held by page page_table[b][j]; entries
-// outside [0, num_pages) give -1 and set MSA_STATUS_PAGE_RANGE.
-__global__ void __launch_bounds__(256) resolve_pages_kernel(const PlanHeader *__restrict__ plan,
-                                                            const int32_t *__restrict__ page_table, int max_pages,
-                                                            int num_pages, int32_t *__restrict__ unit_page,
-                                                            uint32_t *status) {
-    const PlanUnit *units = reinterpret_cast<const PlanUnit *>(plan + 1);
-    const int work = plan->work_count;
-    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < work; u += gridDim.x * blockDim.x) {
-        const int row = units[u].row, b = row / max_pages, j = row % max_pages;
-        int pg = page_table[(int64_t)b * max_pages + j];
-        if (pg < 0 || pg >= num_pages) {
-            set_status(status, MSA_STATUS_PAGE_RANGE);
-            pg = -1;
-        }
-        unit_page[u] = pg;
-    }
-}
-
-// Paged decode workspace: the k->q CSR over logical blocks (and its build
-// scratch), the work plan, each unit's physical page, and the split partials.
-struct PagedWorkspace {
-    size_t csr_ws, csr_ws_bytes, row_ptr, q_indices, qsplit, split_counts, plan, plan_bytes, unit_page, fwd,
-        fwd_bytes, bytes;
-};
-
-PagedWorkspace paged_workspace_layout(int B, int Sq, int Hq, int Hkv, int topk, int max_pages) {
-    PagedWorkspace w;
-    const int qpk = Hq / Hkv;
-    const int Skv = max_pages * kBlk;
-    const size_t nnz = (size_t)B * Sq * topk;
-    size_t o = 0;
-    w.csr_ws = o;
-    w.csr_ws_bytes = msa_k2q_csr_workspace_size(B, Hkv, Sq, Skv, topk, kBlk);
-    o = align_up(o + w.csr_ws_bytes, 256);
-    w.row_ptr = o;
-    o = align_up(o + sizeof(int32_t) * (size_t)Hkv * ((size_t)B * max_pages + 1), 256);
-    w.q_indices = o;
-    o = align_up(o + sizeof(int32_t) * (size_t)Hkv * nnz, 256);
-    w.qsplit = o;
-    o = align_up(o + sizeof(int32_t) * (size_t)Hkv * nnz, 256);
-    w.split_counts = o;
-    o = align_up(o + sizeof(int32_t) * (size_t)B * Sq * Hkv, 256);
-    w.plan = o;
-    w.plan_bytes = msa_plan_size(B, Hkv, Sq, Skv, topk, kBlk, qpk);
-    o = align_up(o + w.plan_bytes, 256);
-    w.unit_page = o;
-    o = align_up(o + sizeof(int32_t) * (size_t)plan_capacity(B, Hkv, Sq, Skv, topk, qpk), 256);
-    w.fwd = o;
-    w.fwd_bytes = fwd_workspace_layout(B, Sq, Hq, topk, kD).bytes;
-    o = align_up(o + w.fwd_bytes, 256);
-    w.bytes = o;
-    return w;
 }
 
 }  // namespace
@@ -207,7 +151,7 @@ extern "C" int msa_sparse_attn_fwd_partial(const void *q, const void *k, const v
     t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
     t.scale_log2 = t.scale * 1.4426950408889634f;
 
-    return tiles_launch(t, q, k, v, (int64_t)B * Skv, kv_format, stream);
+    return tiles_launch(t, plan_capacity(B, Hkv, Sq, Skv, topk, qpk), q, k, v, (int64_t)B * Skv, kv_format, stream);
 }
 
 extern "C" int msa_sparse_attn_combine(const int32_t *split_counts, int B, int Sq, int Hq, int Hkv, int D, int topk,
@@ -247,81 +191,4 @@ extern "C" int msa_sparse_attn_fwd(const void *q, const void *k, const void *v, 
                                          status_dev, stream);
     if (rc != MSA_OK) return rc;
     return msa_sparse_attn_combine(split_counts, B, Sq, Hq, Hkv, D, topk, o, lse, workspace, ws_bytes, stream);
-}
-
-// ---------------------------------------------------------------------------
-// Paged decode: the same KV-block-major pipeline over logical blocks.  The
-// k->q CSR is built over (KV head, sequence, logical block) with each
-// sequence's used length; every plan unit's physical page is looked up once;
-// the tile kernel then streams each unit's page and applies the causal limit
-// of each query's own position seqused[b] - Sq + i; the LSE combine merges.
-// ---------------------------------------------------------------------------
-extern "C" size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk,
-                                                           int max_pages) {
-    if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || D != kD || topk <= 0 || max_pages <= 0 || Hq % Hkv) return 0;
-    if (!supported_qpk(Hq / Hkv) || !supported_topk(topk) || max_pages > kMaxNblk) return 0;
-    if ((int64_t)B * Sq >= (1 << 24)) return 0;
-    return paged_workspace_layout(B, Sq, Hq, Hkv, topk, max_pages).bytes;
-}
-
-extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
-                                         const int32_t *page_table, int max_pages, const int32_t *seqused_k,
-                                         const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
-                                         int topk, int causal, float softmax_scale, void *o, float *lse,
-                                         void *workspace, size_t ws_bytes, uint32_t *status_dev,
-                                         cudaStream_t stream) {
-    if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !q2k || !o || !workspace) return MSA_ERR_INVALID_ARG;
-    if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages <= 0 || topk <= 0 || Hq % Hkv)
-        return MSA_ERR_INVALID_ARG;
-    const int qpk = Hq / Hkv;
-    if (D != kD || page_size != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
-    if (max_pages > kMaxNblk || (int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
-    if ((int64_t)num_pages * kBlk >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
-        return MSA_ERR_INVALID_ARG;
-    const PagedWorkspace w = paged_workspace_layout(B, Sq, Hq, Hkv, topk, max_pages);
-    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
-    char *ws = static_cast<char *>(workspace);
-    int32_t *row_ptr = reinterpret_cast<int32_t *>(ws + w.row_ptr);
-    int32_t *q_indices = reinterpret_cast<int32_t *>(ws + w.q_indices);
-    int32_t *qsplit = reinterpret_cast<int32_t *>(ws + w.qsplit);
-    int32_t *split_counts = reinterpret_cast<int32_t *>(ws + w.split_counts);
-    void *plan = ws + w.plan;
-    int32_t *unit_page = reinterpret_cast<int32_t *>(ws + w.unit_page);
-    const int Skv = max_pages * kBlk;
-
-    int rc = msa_build_k2q_csr(q2k, B, Hkv, Sq, Skv, topk, kBlk, qpk, seqused_k, row_ptr, q_indices, qsplit,
-                               split_counts, plan, w.plan_bytes, ws + w.csr_ws, w.csr_ws_bytes, status_dev, stream);
-    if (rc != MSA_OK) return rc;
-    const int64_t capacity = plan_capacity(B, Hkv, Sq, Skv, topk, qpk);
-    const int rblocks = (int)std::min<int64_t>(ceil_div(capacity, 256), (int64_t)4 * num_sms());
-    resolve_pages_kernel<<<rblocks < 1 ? 1 : rblocks, 256, 0, stream>>>(static_cast<const PlanHeader *>(plan),
-                                                                         page_table, max_pages, num_pages,
-                                                                         unit_page, status_dev);
-    MSA_LAUNCH_CHECK();
-
-    const FwdWorkspace fw = fwd_workspace_layout(B, Sq, Hq, topk, D);
-    char *fws = ws + w.fwd;
-    TcParams t;
-    t.k_packed = static_cast<const uint8_t *>(k_pool);
-    t.v_packed = static_cast<const uint8_t *>(v_pool);
-    t.k_scales = nullptr;
-    t.v_scales = nullptr;
-    t.qsplit = qsplit;
-    t.plan = static_cast<const PlanHeader *>(plan);
-    t.units = reinterpret_cast<const PlanUnit *>(t.plan + 1);
-    t.o_part = reinterpret_cast<__nv_bfloat16 *>(fws + fw.o_part);
-    t.stat_part = reinterpret_cast<float2 *>(fws + fw.stat_part);
-    t.seqused = seqused_k;
-    t.unit_page = unit_page;
-    t.status = status_dev;
-    t.B = B; t.Sq = Sq; t.Skv = Skv; t.Hq = Hq; t.Hkv = Hkv; t.qpk = qpk; t.topk = topk;
-    t.nblk = max_pages;
-    t.causal = causal ? 1 : 0;
-    t.cap = (int64_t)B * Sq * topk;
-    t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-    t.scale_log2 = t.scale * 1.4426950408889634f;
-    rc = tiles_launch(t, q, k_pool, v_pool, (int64_t)num_pages * kBlk, MSA_KV_BF16, stream);
-    if (rc != MSA_OK) return rc;
-    return msa_sparse_attn_combine(split_counts, B, Sq, Hq, Hkv, D, topk, o, lse, fws, w.fwd_bytes, stream);
 }

@@ -186,16 +186,25 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         // loaded into registers one chunk ahead and then hit in L2.  (Values
         // are never shuffled through a register ring: a move of a register
         // whose load is still in flight would wait for that load.)
+        // A cursor holds its unit and the next one, whose header is loaded a
+        // whole unit early (every decode chunk starts a unit).
         struct Cursor {
             int u, c;
-            Unit x;
+            Unit x, xn;
+        };
+        auto start = [&](Cursor &k) {
+            k.u = blockIdx.x;
+            k.c = 0;
+            if (k.u < work) k.x = load_unit(p, k.u);
+            if (k.u + G < work) k.xn = load_unit(p, k.u + G);
         };
         auto advance = [&](Cursor &k) {
             if (k.u >= work) return;
             if (++k.c == k.x.nch) {
                 k.u += G;
                 k.c = 0;
-                if (k.u < work) k.x = load_unit(p, k.u);
+                k.x = k.xn;
+                if (k.u + G < work) k.xn = load_unit(p, k.u + G);
             }
         };
         auto prefetch_ids = [&](const Cursor &k) {
@@ -204,10 +213,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::prefetch_l2(p.qsplit + (int64_t)k.x.h * p.cap + k.x.start + k.c * qc + idx);
         };
         // every plan entry this CTA will read, into L2 up front (16 bytes each)
-        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) tc::prefetch_l2(p.units + u);
+        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) {
+            tc::prefetch_l2(p.units + u);
+            if (p.unit_page) tc::prefetch_l2(p.unit_page + u);
+        }
         const uint64_t keep = tc::l2_policy_evict_last();  // gather4 Q rows
-        Cursor cur{(int)blockIdx.x, 0, Unit{}}, ahead{(int)blockIdx.x, 0, Unit{}};
-        if (cur.u < work) cur.x = ahead.x = load_unit(p, cur.u);
+        Cursor cur, ahead;
+        start(cur);
+        start(ahead);
         for (int d = 0; d < kIdAhead; ++d) {
             prefetch_ids(ahead);
             advance(ahead);
@@ -466,6 +479,21 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                if (__all_sync(0xffffffffu, !valid)) {
+                    // no row of this warp holds a query (padding of a short
+                    // chunk): its P and O rows are never stored, so skip them;
+                    // the barrier protocol (arrive after each wait) stays
+                    tc::fence_after_sync();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::P_FULL + wg));
+                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::O_EMPTY + wg));
+                    continue;
+                }
                 tc::fence_after_sync();
                 uint32_t r[128];
                 tc::tmem_ld128(s_addr, r);
