@@ -1,15 +1,19 @@
-// attn_tc.cuh -- the tcgen05 (5th-gen tensor core) block-sparse prefill tile
-// kernel: persistent, one CTA per SM, warp-specialised, 11 warps.
+// attn_tc.cuh -- the tcgen05 (5th-gen tensor core) block-sparse attention tile
+// kernel (prefill, and paged decode): persistent, one CTA per SM,
+// warp-specialised, 12 warps.
 //
+//   warp 11     feed: walks the CTA's chunks in plan order and copies each
+//               chunk's plan unit, page and query ids into a 4-entry shared
+//               memory ring with cp.async (the copies arrive on the slot's
+//               barrier as they land), so no global load sits on the
+//               loader's issue path.
 //   warp 0      loader: per work unit the K and V block by TMA (bf16, 128-byte
-//               swizzle, two buffers, one issuing lane); per chunk the 128
-//               gathered Q rows (128/qhead_per_kv queries x all heads of the
-//               GQA group) by TMA into a 3-stage ring: one 5D box per query
-//               (its whole 4 KB group) when qhead_per_kv >= 8, four rows per
+//               swizzle, one 4D copy each, one issuing lane); per chunk the
+//               128 gathered Q rows (128/qhead_per_kv queries x all heads of
+//               the GQA group) by TMA into the Q ring: one 5D box per query
+//               (its whole group) when qhead_per_kv >= 8, four rows per
 //               tile::gather4 copy otherwise.  The copy engine's cost is per
-//               request, so requests are kept few and large.  Query ids are
-//               prefetched into L2 four chunks ahead and loaded into
-//               registers one chunk ahead.
+//               request, so requests are kept few and large.
 //   warp 1      NVFP4 only: dequantises the K and V block into the same
 //               swizzled bf16 layout (exact products).
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
@@ -53,13 +57,16 @@ struct TcParams {
 
 namespace tck {
 
-constexpr int kIdAhead = 4;  // chunks of query ids the loader fetches ahead
-constexpr int kWarps = 11;
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3;
+constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3, kWarpFeed = 11;
+// Chunk ring between the feed warp and the loader: per chunk its plan unit
+// (16 B), the unit's page, and up to 128 query ids (qsplit entries).
+constexpr int kRing = 4;
+constexpr uint32_t kRingEntry = 32 + 128 * 4;
 
 // Shared memory of a kernel with NKV K/V stages and NQ Q stages (32 KB tiles):
-// K [NKV] | V [NKV] | Q [NQ] | mbarriers | TMEM slot | abort flag.
+// K [NKV] | V [NKV] | Q [NQ] | mbarriers | TMEM slot | abort flag | chunk ring.
 template <int NKV, int NQ>
 struct Layout {
     static constexpr uint32_t K = 0, V = NKV * 32768u, Q = 2u * NKV * 32768u, BAR = Q + NQ * 32768u;
@@ -72,10 +79,13 @@ struct Layout {
         P_FULL = S_FULL + 2,
         O_FULL = P_FULL + 2,
         O_EMPTY = O_FULL + 2,
-        DRAIN = O_EMPTY + 2,
+        RING_FULL = O_EMPTY + 2,
+        RING_EMPTY = RING_FULL + kRing,
+        DRAIN = RING_EMPTY + kRing,
         NBAR = DRAIN + 1
     };
-    static constexpr uint32_t TSLOT = BAR + 8 * NBAR, ABORT = TSLOT + 4, BYTES = ABORT + 4;
+    static constexpr uint32_t TSLOT = BAR + 8 * NBAR, ABORT = TSLOT + 4, RING = (ABORT + 4 + 15) & ~15u,
+                              BYTES = RING + kRing * kRingEntry;
     // The dynamic shared memory base is 1024-byte aligned (no static shared
     // memory); the kernel checks this instead of reserving slack.
     static_assert(BYTES <= 232448, "shared memory budget");
@@ -145,6 +155,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             tc::mbar_init(bar(L::Q_FULL + i), 1);
             tc::mbar_init(bar(L::Q_EMPTY + i), 1);
         }
+        for (int i = 0; i < kRing; ++i) {
+            tc::mbar_init(bar(L::RING_FULL + i), 32);  // one cp.async arrival per feed lane
+            tc::mbar_init(bar(L::RING_EMPTY + i), 1);
+        }
         tc::mbar_init(bar(L::DRAIN), 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
@@ -167,71 +181,37 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loader
-        int ci = 0, ui = 0;
+        // Walks the CTA's chunks in plan order, taking each chunk's unit and
+        // query ids from the feed warp's ring (shared memory), so no global
+        // load sits on its issue path; issues the unit's K/V on its first
+        // chunk and the chunk's Q rows.
+        int ci = 0, ui = 0, c = 0;
         int kv_armed[NKV];
         for (int i = 0; i < NKV; ++i) kv_armed[i] = -1;
         bool ok = true;
-        const int G = gridDim.x;
-        // query ids of chunk c of unit x: lane l holds queries l, l+32, l+64, l+96
-        auto fetch_ids = [&](const Unit &x, int c, int (&ids)[4]) {
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int qi = s * 32 + lane, idx = c * qc + qi;
-                ids[s] = (qi < qc && idx < x.count) ? (p.qsplit[(int64_t)x.h * p.cap + x.start + idx] & 0xFFFFFF)
-                                                    : -1;
-            }
-        };
-        // A second cursor runs kIdAhead chunks ahead of the issuing one and
-        // prefetches its query ids into L2; the ids of the next chunk are
-        // loaded into registers one chunk ahead and then hit in L2.  (Values
-        // are never shuffled through a register ring: a move of a register
-        // whose load is still in flight would wait for that load.)
-        // A cursor holds its unit and the next one, whose header is loaded a
-        // whole unit early (every decode chunk starts a unit).
-        struct Cursor {
-            int u, c;
-            Unit x, xn;
-        };
-        auto start = [&](Cursor &k) {
-            k.u = blockIdx.x;
-            k.c = 0;
-            if (k.u < work) k.x = load_unit(p, k.u);
-            if (k.u + G < work) k.xn = load_unit(p, k.u + G);
-        };
-        auto advance = [&](Cursor &k) {
-            if (k.u >= work) return;
-            if (++k.c == k.x.nch) {
-                k.u += G;
-                k.c = 0;
-                k.x = k.xn;
-                if (k.u + G < work) k.xn = load_unit(p, k.u + G);
-            }
-        };
-        auto prefetch_ids = [&](const Cursor &k) {
-            const int idx = lane * 32;  // one 128-byte line per 32 ids
-            if (k.u < work && idx < qc && k.c * qc + idx < k.x.count)
-                tc::prefetch_l2(p.qsplit + (int64_t)k.x.h * p.cap + k.x.start + k.c * qc + idx);
-        };
-        // every plan entry this CTA will read, into L2 up front (16 bytes each)
-        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) {
-            tc::prefetch_l2(p.units + u);
-            if (p.unit_page) tc::prefetch_l2(p.unit_page + u);
-        }
         const uint64_t keep = tc::l2_policy_evict_last();  // gather4 Q rows
-        Cursor cur, ahead;
-        start(cur);
-        start(ahead);
-        for (int d = 0; d < kIdAhead; ++d) {
-            prefetch_ids(ahead);
-            advance(ahead);
-        }
-        // One chunk: issue its Q (and, on a unit's first chunk, K/V) with the ids
-        // in `ids`, while loading the next chunk's ids into `nids`.  The loop
-        // below alternates two id buffers, so no register with a load in
-        // flight is ever copied.
-        auto step = [&](const int (&ids)[4], int (&nids)[4]) -> bool {
-            const Unit &x = cur.x;
-            const int c = cur.c;
+        for (int u = blockIdx.x; u < work && ok;) {
+            const int slot = ci % kRing;
+            ok = tc::mbar_wait(bar(L::RING_FULL + slot), (ci / kRing) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const int *e = reinterpret_cast<const int *>(gbase + L::RING + slot * kRingEntry);
+            Unit x;
+            x.h = e[0];
+            x.b = e[1] / p.nblk;
+            x.tok0 = (e[1] % p.nblk) * kBlk;
+            x.start = e[2];
+            x.count = e[3];
+            x.nch = (x.count + qc - 1) / qc;
+            x.page = e[4];
+            int ids[4];
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int qi = s4 * 32 + lane;
+                ids[s4] = (qi < qc && c * qc + qi < x.count) ? (e[8 + qi] & 0xFFFFFF) : -1;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(L::RING_EMPTY + slot));
             const int kb = ui % NKV;
             if (c == 0 && KV_FORMAT == MSA_KV_BF16) {
                 if (lane == 0) {
@@ -253,22 +233,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) return false;
+                if (!ok) break;
             }
-            // next chunk's ids (registers, one chunk ahead) and an L2 prefetch further out
-            Cursor nxt = cur;
-            advance(nxt);
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) nids[s4] = -1;
-            if (nxt.u < work) fetch_ids(nxt.x, nxt.c, nids);
-            prefetch_ids(ahead);
-            advance(ahead);
             const int qs = ci % NQ;
             if (lane == 0 && ci >= NQ)
                 ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((ci / NQ) - 1) & 1, abort_flag, p.status,
                                    MSA_STATUS_TIMEOUT);
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) return false;
+            if (!ok) break;
             // The chunk's 128 Q rows (row R = query R / qpk of the chunk, head
             // R % qpk of the group), 128-byte swizzled K-major.  qpk >= 8: one
             // 5D box per query holds its whole group (row octets 2048 bytes
@@ -292,8 +264,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             } else {
                 for (int j = 0; j < 32; ++j) {
                     int r[4];
-                    const int slot = ((4 * j) / p.qpk) >> 5;
-                    const int v = pick4(ids, slot);
+                    const int slot4 = ((4 * j) / p.qpk) >> 5;
+                    const int v = pick4(ids, slot4);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const int R = 4 * j + t, qi = R / p.qpk;
@@ -309,15 +281,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 }
             }
             ++ci;
-            const bool last_in_unit = (c + 1 == x.nch);
-            advance(cur);
-            if (last_in_unit) ++ui;
-            return cur.u < work;
-        };
-        int ids_a[4] = {-1, -1, -1, -1}, ids_b[4] = {-1, -1, -1, -1};
-        if (cur.u < work) {
-            fetch_ids(cur.x, 0, ids_a);
-            while (step(ids_a, ids_b) && step(ids_b, ids_a)) {
+            if (++c == x.nch) {
+                c = 0;
+                ++ui;
+                u += gridDim.x;
             }
         }
         // drain outstanding copies before the CTA can exit
@@ -326,6 +293,46 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             for (int i = 0; i < NKV; ++i)
                 if (kv_armed[i] >= 0) tc::mbar_wait(bar(L::KV_FULL + i), (uint32_t)kv_armed[i], &dummy, p.status, 0);
         }
+        __syncwarp();
+    } else if (warp == kWarpFeed) {
+        // ------------------------------------------------------------------ feed
+        // Walks the same chunk sequence and copies each chunk's plan unit, page
+        // and query ids into the ring with cp.async; every lane's copies arrive
+        // on the slot's barrier as they land, so this warp never waits on a
+        // global load and runs up to kRing chunks ahead of the loader.
+        int k = 0;
+        bool ok = true;
+        const int G = gridDim.x;
+        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) {
+            tc::prefetch_l2(p.units + u);
+            if (p.unit_page) tc::prefetch_l2(p.unit_page + u);
+        }
+        Unit xn{};
+        if (blockIdx.x < work) xn = load_unit(p, blockIdx.x);
+        for (int u = blockIdx.x; u < work && ok; u += G) {
+            const Unit x = xn;  // loaded one unit ahead
+            if (u + G < work) xn = load_unit(p, u + G);
+            for (int c = 0; c < x.nch; ++c, ++k) {
+                const int slot = k % kRing;
+                if (lane == 0 && k >= kRing)
+                    ok = tc::mbar_wait(bar(L::RING_EMPTY + slot), ((k / kRing) - 1) & 1, abort_flag, p.status,
+                                       MSA_STATUS_TIMEOUT);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const uint32_t e = base + L::RING + slot * kRingEntry;
+                if (lane == 0) {
+                    cp_async16(e, p.units + u);
+                    if (p.unit_page) cp_async4(e + 16, p.unit_page + u);
+                }
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const int qi = s4 * 32 + lane, idx = c * qc + qi;
+                    if (qi < qc && idx < x.count) cp_async4(e + 32 + qi * 4, p.qsplit + (int64_t)x.h * p.cap + x.start + idx);
+                }
+                tc::cp_async_mbar_arrive(bar(L::RING_FULL + slot));
+            }
+        }
+        cp_async_wait<0>();
         __syncwarp();
     } else if (warp == kWarpDequant) {
         // ------------------------------------------------------------------ NVFP4 K/V producer
