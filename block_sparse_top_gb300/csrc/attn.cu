@@ -68,8 +68,8 @@ int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void 
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
         if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
-        // paged decode: every unit is one chunk with its own K/V block
-        if (t.unit_page) return launch_tiles<MSA_KV_BF16, 3, 1>(mk, mv, mq, t, grid, stream);
+        // two K/V stages and three Q stages, for prefill and paged decode alike
+        // (measured better for decode too than three K/V stages and one Q)
         return launch_tiles<MSA_KV_BF16, 2, 3>(mk, mv, mq, t, grid, stream);
     }
     return launch_tiles<MSA_KV_NVFP4, 2, 3>(mk, mv, mq, t, grid, stream);

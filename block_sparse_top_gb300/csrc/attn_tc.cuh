@@ -118,9 +118,7 @@ __device__ __forceinline__ int pick4(const int (&v)[4], int s) {
 
 }  // namespace tck
 
-// NKV, NQ: K/V and Q stages -- 2 and 3 when units hold several chunks (the
-// K/V block is reused across them), 3 and 1 when every unit is one chunk
-// (paged decode: a new K/V block per chunk, few Q rows).
+// NKV, NQ: K/V and Q stages (32 KB tiles; 2 and 3 fill the shared memory).
 template <int KV_FORMAT, int NKV, int NQ>
 __global__ void __launch_bounds__(tck::kThreads, 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
