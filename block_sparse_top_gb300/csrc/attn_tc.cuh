@@ -19,7 +19,7 @@
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
 //               O_{i-1} = P_{i-1} V with P read from tensor memory.
 //   warps 3-6,  softmax + epilogue for even / odd chunks: each thread owns one
-//   warps 7-10  S row (TMEM lane), loads it whole (128 columns), applies the
+//   warps 7-10  S row (TMEM lane), reads it in two halves of 64 columns, applies the
 //               bottom-right causal limit, writes P = exp(S - m) as bf16 over
 //               S, then stores the split partial unnormalised -- O = P V as
 //               bf16 with its statistics (m * scale, l = sum P) -- so that the
@@ -500,8 +500,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     continue;
                 }
                 tc::fence_after_sync();
-                uint32_t r[128];
-                tc::tmem_ld128(s_addr, r);
+                // The S row is read 64 keys at a time: one pass for the max, one
+                // for P (a whole row in registers leaves the compiler no room).
+                uint32_t r[64];
+                tc::tmem_ld64(s_addr, r);
                 // row info while the load is in flight
                 const int gq = packed & 0xFFFFFF;
                 const int split = (packed >> 24) & 0xFF;
@@ -516,40 +518,57 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     const int64_t nv = limit - x.tok0 + 1;
                     nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                 }
-                tc::tmem_ld_wait();
                 // keys past the causal limit (diagonal block rows) become -inf
-                if (nvis < 128) {
+                auto mask_half = [&](int hf) {
+                    const int lim = nvis - 64 * hf;
+                    if (lim < 64) {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
-                        if (j >= nvis) r[j] = 0xff800000u;
-                }
+                        for (int j = 0; j < 64; ++j)
+                            if (j >= lim) r[j] = 0xff800000u;
+                    }
+                };
                 // row max: three-input max, four independent chains
                 float mm[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
+                    tc::tmem_ld_wait();
+                    mask_half(hf);
 #pragma unroll
-                    for (int a = 0; a < 4; ++a)
-                        mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
+                    for (int j = 0; j < 64; j += 8) {
+#pragma unroll
+                        for (int a = 0; a < 4; ++a)
+                            mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
+                    }
                 }
                 const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                // P = exp2(S * scale_log2 - m * scale_log2) packed to bf16 in place
-                // (r[j] <- keys 2j, 2j+1); row sum in packed f32x2 adds
+                // P = exp2(S * scale_log2 - m * scale_log2): each half is read
+                // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
+                // the half) and stored over columns the half has already read;
+                // row sum in packed f32x2 adds
                 const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                 const float2 nm2 = make_float2(-mc, -mc);
                 float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    tc::tmem_ld64(s_addr + 64 * hf, r);
+                    tc::tmem_ld_wait();
+                    mask_half(hf);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    float2 e = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
-                    e.x = ex2_approx(e.x);
-                    e.y = ex2_approx(e.y);
-                    ll[j & 1] = __fadd2_rn(ll[j & 1], e);
-                    r[j] = pack_bf16x2(e.x, e.y);
+                    for (int j = 0; j < 32; ++j) {
+                        float2 e =
+                            __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
+                        e.x = ex2_approx(e.x);
+                        e.y = ex2_approx(e.y);
+                        ll[j & 1] = __fadd2_rn(ll[j & 1], e);
+                        r[j] = pack_bf16x2(e.x, e.y);
+                    }
+                    tc::tmem_st32(s_addr + 32 * hf, r);
                 }
                 const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
-                tc::tmem_st64(s_addr, r);
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 tc::mbar_arrive(bar(L::P_FULL + wg));
@@ -558,27 +577,33 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc::fence_after_sync();
-                tc::tmem_ld128(o_addr, r);
-                tc::tmem_ld_wait();
-                tc::fence_before_sync();
-                tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is in registers: the next PV may start
-                if (valid) {
-                    // grouped layout: for a fixed (split, c) the heads of one group are
-                    // contiguous, so each store instruction writes whole runs
-                    const int64_t grp = (int64_t)gq * p.Hkv + x.h;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-#pragma unroll
-                    for (int v4 = 0; v4 < 16; ++v4) {
-                        uint4 o4;
-                        o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
-                        o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
-                        o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
-                        o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                        __stcs(dst + (int64_t)v4 * p.qpk, o4);  // streaming: evict first from L2
+                // grouped layout: for a fixed (split, c) the heads of one group are
+                // contiguous, so each store instruction writes whole runs
+                const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    tc::tmem_ld64(o_addr + 64 * hf, r);
+                    tc::tmem_ld_wait();
+                    if (hf == 1) {
+                        tc::fence_before_sync();
+                        tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: the next PV may start
                     }
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            uint4 o4;
+                            o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
+                            o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
+                            o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
+                            o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
+                            __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
+                        }
+                    }
+                }
+                if (valid) {
                     const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
-                    float2 *sdst = p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
-                    __stcs(sdst, st);
+                    __stcs(p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row), st);
                 }
             }
         }
