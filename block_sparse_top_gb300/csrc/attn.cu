@@ -41,13 +41,13 @@ int num_sms() {
 }
 
 namespace {
-template <int KV_FORMAT, int NKV, int NQ>
+template <int KV_FORMAT, int NKV, int NQ, bool WHOLE_ROW>
 int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
                  cudaStream_t stream) {
     const size_t smem = tck::Layout<NKV, NQ>::BYTES;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ>,
+    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ><<<grid, tck::kThreads, smem, stream>>>(mk, mv, mq, t);
+    sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW><<<grid, tck::kThreads, smem, stream>>>(mk, mv, mq, t);
     MSA_LAUNCH_CHECK();
     return MSA_OK;
 }
@@ -68,11 +68,13 @@ int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void 
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
         if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
-        // two K/V stages and three Q stages, for prefill and paged decode alike
-        // (measured better for decode too than three K/V stages and one Q)
-        return launch_tiles<MSA_KV_BF16, 2, 3>(mk, mv, mq, t, grid, stream);
+        // prefill: two K/V stages and three Q stages; paged decode (a unit is
+        // one chunk, its K/V block from HBM; a group's consecutive units share
+        // one Q tile): three K/V stages and one Q
+        if (t.unit_page) return launch_tiles<MSA_KV_BF16, 3, 1, true>(mk, mv, mq, t, grid, stream);
+        return launch_tiles<MSA_KV_BF16, 2, 3, false>(mk, mv, mq, t, grid, stream);
     }
-    return launch_tiles<MSA_KV_NVFP4, 2, 3>(mk, mv, mq, t, grid, stream);
+    return launch_tiles<MSA_KV_NVFP4, 2, 3, false>(mk, mv, mq, t, grid, stream);
 }
 
 namespace {

@@ -118,8 +118,13 @@ __device__ __forceinline__ int pick4(const int (&v)[4], int s) {
 
 }  // namespace tck
 
-// NKV, NQ: K/V and Q stages (32 KB tiles; 2 and 3 fill the shared memory).
-template <int KV_FORMAT, int NKV, int NQ>
+// NKV, NQ: K/V and Q stages (32 KB tiles; 2 and 3, or 3 and 1, fill the
+// shared memory).  PAGED (paged decode, the plan's units carry pages): each
+// CTA walks one contiguous run of units, consecutive units of a group share
+// one Q tile, and the softmax holds a whole S row in registers (one
+// tensor-memory load, 168 registers) instead of reading it in halves (133) --
+// the shorter chain suits decode, where one warp's rows gate each K/V stage.
+template <int KV_FORMAT, int NKV, int NQ, bool PAGED>
 __global__ void __launch_bounds__(tck::kThreads, 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
@@ -137,6 +142,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qc = 128 / p.qpk;
     const int work = p.plan->work_count;
+    // The CTA's units: every gridDim.x-th of the plan (prefill: consecutive
+    // units read the same K/V head close together in time), or one
+    // contiguous run (paged decode: consecutive units of a group share the Q
+    // tile).  Every role walks the same sequence.
+    constexpr bool contiguous = PAGED;
+    const int u_begin = contiguous ? (int)((int64_t)work * blockIdx.x / gridDim.x) : (int)blockIdx.x;
+    const int u_end = contiguous ? (int)((int64_t)work * (blockIdx.x + 1) / gridDim.x) : work;
+    const int u_step = contiguous ? 1 : (int)gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < NKV; ++i) {
@@ -184,11 +197,12 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         // load sits on its issue path; issues the unit's K/V on its first
         // chunk and the chunk's Q rows.
         int ci = 0, ui = 0, c = 0;
+        int qn = 0, q_key = -1;  // Q tiles loaded; resident group (paged): first query * Hkv + head
         int kv_armed[NKV];
         for (int i = 0; i < NKV; ++i) kv_armed[i] = -1;
         bool ok = true;
         const uint64_t keep = tc::l2_policy_evict_last();  // gather4 Q rows
-        for (int u = blockIdx.x; u < work && ok;) {
+        for (int u = u_begin; u < u_end && ok;) {
             const int slot = ci % kRing;
             ok = tc::mbar_wait(bar(L::RING_FULL + slot), (ci / kRing) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
             ok = __all_sync(0xffffffffu, ok);
@@ -233,12 +247,23 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
             }
-            const int qs = ci % NQ;
-            if (lane == 0 && ci >= NQ)
-                ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((ci / NQ) - 1) & 1, abort_flag, p.status,
-                                   MSA_STATUS_TIMEOUT);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            // Paged decode: a unit is one chunk holding all queries of its group
+            // (rows of queries that did not select the block are masked), so
+            // consecutive units of one group -- same first query, same KV head
+            // -- share the Q tile: it is loaded when the group changes.
+            const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
+            const int key = first * p.Hkv + x.h;
+            const bool load_q = !PAGED || key != q_key;
+            q_key = key;
+            const int qs = qn % NQ;
+            if (load_q) {
+                if (lane == 0 && qn >= NQ)
+                    ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((qn / NQ) - 1) & 1, abort_flag, p.status,
+                                       MSA_STATUS_TIMEOUT);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++qn;
+            }
             // The chunk's 128 Q rows (row R = query R / qpk of the chunk, head
             // R % qpk of the group), 128-byte swizzled K-major.  qpk >= 8: one
             // 5D box per query holds its whole group (row octets 2048 bytes
@@ -248,11 +273,11 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             // stale data; their keys are all masked, so they give P = 0);
             // gather4 rows of padding repeat the chunk's first query.
             const uint32_t qt = base + L::Q + qs * 32768;
-            const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
             const int nq = min(qc, x.count - c * qc);
-            if (lane == 0)
+            if (load_q && lane == 0)
                 tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs), p.qpk >= 8 ? (uint32_t)(nq * p.qpk * 256) : 32768u);
-            if (p.qpk >= 8) {
+            if (!load_q) {
+            } else if (p.qpk >= 8) {
                 for (int qi = 0; qi < nq; ++qi) {
                     const int gq = __shfl_sync(0xffffffffu, ids[0], qi);
                     if (lane == 0)
@@ -282,7 +307,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             if (++c == x.nch) {
                 c = 0;
                 ++ui;
-                u += gridDim.x;
+                u += u_step;
             }
         }
         // drain outstanding copies before the CTA can exit
@@ -300,16 +325,15 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         // global load and runs up to kRing chunks ahead of the loader.
         int k = 0;
         bool ok = true;
-        const int G = gridDim.x;
-        for (int u = blockIdx.x + lane * G; u < work; u += 32 * G) {
+        for (int u = u_begin + lane * u_step; u < u_end; u += 32 * u_step) {
             tc::prefetch_l2(p.units + u);
             if (p.unit_page) tc::prefetch_l2(p.unit_page + u);
         }
         Unit xn{};
-        if (blockIdx.x < work) xn = load_unit(p, blockIdx.x);
-        for (int u = blockIdx.x; u < work && ok; u += G) {
+        if (u_begin < u_end) xn = load_unit(p, u_begin);
+        for (int u = u_begin; u < u_end && ok; u += u_step) {
             const Unit x = xn;  // loaded one unit ahead
-            if (u + G < work) xn = load_unit(p, u + G);
+            if (u + u_step < u_end) xn = load_unit(p, u + u_step);
             for (int c = 0; c < x.nch; ++c, ++k) {
                 const int slot = k % kRing;
                 if (lane == 0 && k >= kRing)
@@ -337,7 +361,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         if (KV_FORMAT == MSA_KV_NVFP4) {
             int ui = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < work && ok; u += gridDim.x, ++ui) {
+            for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
                 const Unit x = load_unit(p, u);
                 const int kb = ui % NKV;
                 if (ui >= NKV)
@@ -397,8 +421,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::mma_commit(bar(L::O_FULL + b));
                 if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
-            auto issue_s = [&](int cj, int kbj) {
-                const int b = cj & 1, qs = cj % NQ;
+            // S_cj reads Q tile qn (its stage qn % NQ) and frees the stage when
+            // release_q (the tile's last chunk)
+            auto issue_s = [&](int cj, int kbj, int qn, bool release_q) {
+                const int b = cj & 1, qs = qn % NQ;
                 tc::fence_after_sync();
                 const uint32_t qt = base + L::Q + qs * 32768, ks = base + L::K + kbj * 32768;
 #pragma unroll
@@ -409,10 +435,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                                tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
                 }
                 tc::mma_commit(bar(L::S_FULL + b));
-                tc::mma_commit(bar(L::Q_EMPTY + qs));
+                if (release_q) tc::mma_commit(bar(L::Q_EMPTY + qs));
             };
             // polls until S_ci (if s_cj >= 0) and the pending PV are both issued
-            auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par) -> bool {
+            auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par, int qn, bool release_q) -> bool {
                 bool s_done = s_cj < 0, pv_done = pv_ci < 0, kv_ok = !need_kv;
                 const uint64_t t0 = tc::global_ns();
                 for (uint32_t i = 0;; ++i) {
@@ -421,8 +447,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     if (i > 0) __nanosleep(32);
                     if (!s_done) {
                         if (!kv_ok) kv_ok = tc::mbar_test(bar(L::KV_FULL + kbj), (uint32_t)kv_par);
-                        if (kv_ok && tc::mbar_test(bar(L::Q_FULL + s_cj % NQ), (s_cj / NQ) & 1)) {
-                            issue_s(s_cj, kbj);
+                        if (kv_ok && tc::mbar_test(bar(L::Q_FULL + qn % NQ), (qn / NQ) & 1)) {
+                            issue_s(s_cj, kbj, qn, release_q);
                             s_done = true;
                         }
                     }
@@ -440,20 +466,44 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 set_status(p.status, MSA_STATUS_TIMEOUT);
                 return false;
             };
+            // Q tiles as the loader issues them: one per chunk, or (paged
+            // decode) one per run of consecutive units of one group, told apart
+            // by first query * Hkv + head (read one unit ahead)
+            auto first_query = [&](const Unit &y) -> int {
+                return PAGED ? (__ldg(p.qsplit + (int64_t)y.h * p.cap + y.start) & 0xFFFFFF) * p.Hkv + y.h : 0;
+            };
+            int qn = -1, q_first = -1;
             Unit xnext{};
-            if (blockIdx.x < work) xnext = load_unit(p, blockIdx.x);
-            for (int u = blockIdx.x; u < work && ok; u += gridDim.x, ++ui) {
+            int fnext = -1;
+            if (u_begin < u_end) {
+                xnext = load_unit(p, u_begin);
+                fnext = first_query(xnext);
+            }
+            for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
                 const Unit x = xnext;
-                if (u + (int)gridDim.x < work) xnext = load_unit(p, u + gridDim.x);
+                const int fx = fnext;
+                const bool has_next = u + u_step < u_end;
+                if (has_next) {
+                    xnext = load_unit(p, u + u_step);
+                    fnext = first_query(xnext);
+                }
                 const int kb = ui % NKV;
                 for (int c = 0; c < x.nch && ok; ++c, ++ci) {
-                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1);
+                    bool release_q = true;
+                    if constexpr (!PAGED) {
+                        ++qn;
+                    } else {
+                        if (fx != q_first || c > 0) ++qn;  // (a paged unit is one chunk)
+                        q_first = fx;
+                        release_q = c < x.nch - 1 || !has_next || fnext != fx;
+                    }
+                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1, qn, release_q);
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
                 }
             }
-            if (ok && pv_ci >= 0) drive(-1, 0, false, 0);
+            if (ok && pv_ci >= 0) drive(-1, 0, false, 0, 0, false);
             // all issued MMAs complete before tensor memory is released
             tc::mma_commit(bar(L::DRAIN));
             volatile int dummy = 0;
@@ -470,17 +520,29 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         const int j_of_row = R % p.qpk;  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
+        // the unit and its sequence's key count (paged: seqused[b]), loaded one unit ahead
+        auto kv_len_of = [&](const Unit &y) -> int { return PAGED ? __ldg(p.seqused + y.b) : p.Skv; };
         Unit xnext{};
-        if (blockIdx.x < work) xnext = load_unit(p, blockIdx.x);
-        for (int u = blockIdx.x; u < work && ok; u += gridDim.x) {
-            const Unit x = xnext;  // loaded one unit ahead
-            if (u + (int)gridDim.x < work) xnext = load_unit(p, u + gridDim.x);
+        int kvnext = p.Skv;
+        if (u_begin < u_end) {
+            xnext = load_unit(p, u_begin);
+            kvnext = kv_len_of(xnext);
+        }
+        for (int u = u_begin; u < u_end && ok; u += u_step) {
+            const Unit x = xnext;
+            const int64_t kv_len = kvnext;
+            if (u + u_step < u_end) {
+                xnext = load_unit(p, u + u_step);
+                kvnext = kv_len_of(xnext);
+            }
             for (int c = 0; c < x.nch && ok; ++c, ++ci) {
                 if ((ci & 1) != wg) continue;
                 const uint32_t par = (ci >> 1) & 1;
                 const int qi = R / p.qpk, idx = c * qc + qi;
-                const bool valid = idx < x.count;
-                const int packed = valid ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
+                const bool in_chunk = idx < x.count;
+                const int packed = in_chunk ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
+                // split 255: a query of a paged unit's group that did not select the block
+                const bool valid = in_chunk && (!PAGED || ((uint32_t)packed >> 24) != 0xFFu);
                 ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -499,111 +561,193 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     tc::mbar_arrive(bar(L::O_EMPTY + wg));
                     continue;
                 }
-                tc::fence_after_sync();
-                // The S row is read 64 keys at a time: one pass for the max, one
-                // for P (a whole row in registers leaves the compiler no room).
-                uint32_t r[64];
-                tc::tmem_ld64(s_addr, r);
-                // row info while the load is in flight
-                const int gq = packed & 0xFFFFFF;
-                const int split = (packed >> 24) & 0xFF;
-                int nvis = 0;
-                if (valid && (!p.unit_page || x.page >= 0)) {
-                    // keys visible to query sq of a sequence of kv_len keys
-                    // (bottom-right causal: up to key sq + kv_len - Sq)
-                    const int sq = gq % p.Sq;
-                    const int64_t kv_len = p.seqused ? (int64_t)__ldg(p.seqused + x.b) : (int64_t)p.Skv;
-                    int64_t limit = kv_len - 1;
-                    if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
-                    const int64_t nv = limit - x.tok0 + 1;
-                    nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
-                }
-                // keys past the causal limit (diagonal block rows) become -inf
-                auto mask_half = [&](int hf) {
-                    const int lim = nvis - 64 * hf;
-                    if (lim < 64) {
-#pragma unroll
-                        for (int j = 0; j < 64; ++j)
-                            if (j >= lim) r[j] = 0xff800000u;
+                if constexpr (PAGED) {
+                    tc::fence_after_sync();
+                    uint32_t r[128];
+                    tc::tmem_ld128(s_addr, r);
+                    // row info while the load is in flight
+                    const int gq = packed & 0xFFFFFF;
+                    const int split = (packed >> 24) & 0xFF;
+                    int nvis = 0;
+                    if (valid && (!p.unit_page || x.page >= 0)) {
+                        // keys visible to query sq of a sequence of kv_len keys
+                        // (bottom-right causal: up to key sq + kv_len - Sq)
+                        const int sq = gq % p.Sq;
+                        int64_t limit = kv_len - 1;
+                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
+                        const int64_t nv = limit - x.tok0 + 1;
+                        nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                     }
-                };
-                // row max: three-input max, four independent chains
-                float mm[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
                     tc::tmem_ld_wait();
-                    mask_half(hf);
-#pragma unroll
-                    for (int j = 0; j < 64; j += 8) {
-#pragma unroll
+                    // keys past the causal limit (diagonal block rows) become -inf
+                    if (nvis < 128) {
+    #pragma unroll
+                        for (int j = 0; j < 128; ++j)
+                            if (j >= nvis) r[j] = 0xff800000u;
+                    }
+                    // row max: three-input max, four independent chains
+                    float mm[4];
+    #pragma unroll
+                    for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+    #pragma unroll
+                    for (int j = 0; j < 128; j += 8) {
+    #pragma unroll
                         for (int a = 0; a < 4; ++a)
                             mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                     }
-                }
-                const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                // P = exp2(S * scale_log2 - m * scale_log2): each half is read
-                // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
-                // the half) and stored over columns the half has already read;
-                // row sum in packed f32x2 adds
-                const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
-                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                const float2 nm2 = make_float2(-mc, -mc);
-                float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    tc::tmem_ld64(s_addr + 64 * hf, r);
-                    tc::tmem_ld_wait();
-                    mask_half(hf);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        float2 e =
-                            __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
+                    const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                    // P = exp2(S * scale_log2 - m * scale_log2) packed to bf16 in place
+                    // (r[j] <- keys 2j, 2j+1); row sum in packed f32x2 adds
+                    const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
+                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nm2 = make_float2(-mc, -mc);
+                    float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        float2 e = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
                         e.x = ex2_approx(e.x);
                         e.y = ex2_approx(e.y);
                         ll[j & 1] = __fadd2_rn(ll[j & 1], e);
                         r[j] = pack_bf16x2(e.x, e.y);
                     }
-                    tc::tmem_st32(s_addr + 32 * hf, r);
-                }
-                const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
-                tc::tmem_st_wait();
-                tc::fence_before_sync();
-                tc::mbar_arrive(bar(L::P_FULL + wg));
-                // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
-                ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc::fence_after_sync();
-                // grouped layout: for a fixed (split, c) the heads of one group are
-                // contiguous, so each store instruction writes whole runs
-                const int64_t grp = (int64_t)gq * p.Hkv + x.h;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    tc::tmem_ld64(o_addr + 64 * hf, r);
+                    const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
+                    tc::tmem_st64(s_addr, r);
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::P_FULL + wg));
+                    // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
+                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    tc::tmem_ld128(o_addr, r);
                     tc::tmem_ld_wait();
-                    if (hf == 1) {
-                        tc::fence_before_sync();
-                        tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: the next PV may start
-                    }
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is in registers: the next PV may start
                     if (valid) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
+                        // grouped layout: for a fixed (split, c) the heads of one group are
+                        // contiguous, so each store instruction writes whole runs
+                        const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
+    #pragma unroll
+                        for (int v4 = 0; v4 < 16; ++v4) {
                             uint4 o4;
                             o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
                             o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
                             o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
                             o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                            __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
+                            __stcs(dst + (int64_t)v4 * p.qpk, o4);  // streaming: evict first from L2
+                        }
+                        const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
+                        float2 *sdst = p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
+                        __stcs(sdst, st);
+                    }
+                } else {
+                    tc::fence_after_sync();
+                    // The S row is read 64 keys at a time: one pass for the max, one
+                    // for P (a whole row in registers leaves the compiler no room).
+                    uint32_t r[64];
+                    tc::tmem_ld64(s_addr, r);
+                    // row info while the load is in flight
+                    const int gq = packed & 0xFFFFFF;
+                    const int split = (packed >> 24) & 0xFF;
+                    int nvis = 0;
+                    if (valid && (!p.unit_page || x.page >= 0)) {
+                        // keys visible to query sq of a sequence of kv_len keys
+                        // (bottom-right causal: up to key sq + kv_len - Sq)
+                        const int sq = gq % p.Sq;
+                        int64_t limit = kv_len - 1;
+                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
+                        const int64_t nv = limit - x.tok0 + 1;
+                        nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
+                    }
+                    // keys past the causal limit (diagonal block rows) become -inf
+                    auto mask_half = [&](int hf) {
+                        const int lim = nvis - 64 * hf;
+                        if (lim < 64) {
+    #pragma unroll
+                            for (int j = 0; j < 64; ++j)
+                                if (j >= lim) r[j] = 0xff800000u;
+                        }
+                    };
+                    // row max: three-input max, four independent chains
+                    float mm[4];
+    #pragma unroll
+                    for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+    #pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
+                        tc::tmem_ld_wait();
+                        mask_half(hf);
+    #pragma unroll
+                        for (int j = 0; j < 64; j += 8) {
+    #pragma unroll
+                            for (int a = 0; a < 4; ++a)
+                                mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                         }
                     }
-                }
-                if (valid) {
-                    const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
-                    __stcs(p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row), st);
+                    const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                    // P = exp2(S * scale_log2 - m * scale_log2): each half is read
+                    // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
+                    // the half) and stored over columns the half has already read;
+                    // row sum in packed f32x2 adds
+                    const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
+                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nm2 = make_float2(-mc, -mc);
+                    float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    #pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tc::tmem_ld64(s_addr + 64 * hf, r);
+                        tc::tmem_ld_wait();
+                        mask_half(hf);
+    #pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            float2 e =
+                                __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
+                            e.x = ex2_approx(e.x);
+                            e.y = ex2_approx(e.y);
+                            ll[j & 1] = __fadd2_rn(ll[j & 1], e);
+                            r[j] = pack_bf16x2(e.x, e.y);
+                        }
+                        tc::tmem_st32(s_addr + 32 * hf, r);
+                    }
+                    const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::P_FULL + wg));
+                    // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
+                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    // grouped layout: for a fixed (split, c) the heads of one group are
+                    // contiguous, so each store instruction writes whole runs
+                    const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
+    #pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tc::tmem_ld64(o_addr + 64 * hf, r);
+                        tc::tmem_ld_wait();
+                        if (hf == 1) {
+                            tc::fence_before_sync();
+                            tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: the next PV may start
+                        }
+                        if (valid) {
+    #pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4) {
+                                uint4 o4;
+                                o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
+                                o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
+                                o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
+                                o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
+                                __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
+                            }
+                        }
+                    }
+                    if (valid) {
+                        const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
+                        __stcs(p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row), st);
+                    }
                 }
             }
         }

@@ -10,7 +10,10 @@
 //   2. scan:  exclusive prefixes of the groups' union sizes and selection
 //      counts -> one global unit list and one global query list;
 //   3. write: one plan unit per union block (its page looked up once), and
-//      the unit's queries (packed query id | split << 24) in ascending order.
+//      the unit's query table: every query of the group, packed query id |
+//      split << 24, split 255 for a query that did not select the block (the
+//      tile kernel masks its rows and keeps the group's Q tile for all of the
+//      group's units).
 // The tcgen05 tile kernel then streams each unit's page and applies the
 // causal limit of each query's own position seqused[b] - Sq + i, and the LSE
 // combine merges every query head's splits.
@@ -49,7 +52,7 @@ struct PlanArgs {
     int2 *ucount;          // [groups + 1] (union size, valid selections), then exclusive prefixes
     int32_t *slot_split;   // [B][Hkv][Sq][topk] split id of each slot, -1 for padding and repeats
     int32_t *split_counts; // [B*Sq][Hkv]
-    int32_t *qlist;        // [B*Sq*Hkv*topk] packed query id | split << 24, per unit
+    int32_t *qlist;        // [groups * maxu][qg] per unit: packed query id | split << 24 (255: not selected)
     PlanHeader *plan;
     PlanUnit *units;
     int32_t *unit_page;
@@ -224,65 +227,40 @@ __global__ void __launch_bounds__(1024) paged_scan_kernel(PlanArgs a) {
 }
 
 // ---------------------------------------------------------------- 3. write
-// One unit per union block of group g (global index ucount[g].x + e); its
-// queries go to qlist[start .. start + count) in ascending order.
+// One unit per union block of group g (global index u = ucount[g].x + e); its
+// query table (all queries of the group, ascending) is qlist[u*qg .. + nq).
 __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
-    __shared__ int32_t warp_tot[4];
-    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.x;
     const Group x = group_of(a, g);
-    const int2 off = a.ucount[g];
-    const int nu = a.ucount[g + 1].x - off.x;
-    int carry = 0;
-    for (int base = 0; base < nu; base += blockDim.x) {
-        const int e = base + tid;
+    const int off = a.ucount[g].x;
+    const int nu = a.ucount[g + 1].x - off;
+    for (int e = threadIdx.x; e < nu; e += blockDim.x) {
         const uint32_t *mk = a.umask + ((int64_t)g * a.maxu + e) * a.wq;
-        int cnt = 0;
-        if (e < nu)
-            for (int w = 0; w < a.wq; ++w) cnt += __popc(mk[w]);
-        int v = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += y;
+        const int j = a.ulist[(int64_t)g * a.maxu + e];
+        const int64_t u = off + e;
+        const int start = (int)(u * a.qg);
+        PlanUnit pu;
+        pu.head = x.h;
+        pu.row = x.b * a.max_pages + j;
+        pu.start = start;
+        pu.count = x.nq;
+        a.units[u] = pu;
+        int pg = a.page_table[(int64_t)x.b * a.max_pages + j];
+        if (pg < 0 || pg >= a.num_pages) {
+            set_status(a.status, MSA_STATUS_PAGE_RANGE);
+            pg = -1;  // the tile kernel skips the block
         }
-        if (lane == 31) warp_tot[warp] = v;
-        __syncthreads();
-        int pre = carry + v - cnt;
-        for (int w = 0; w < warp; ++w) pre += warp_tot[w];
-        const int pass_total = warp_tot[0] + warp_tot[1] + warp_tot[2] + warp_tot[3];
-        if (e < nu) {
-            const int j = a.ulist[(int64_t)g * a.maxu + e];
-            const int64_t u = off.x + e;
-            const int start = off.y + pre;
-            PlanUnit pu;
-            pu.head = x.h;
-            pu.row = x.b * a.max_pages + j;
-            pu.start = start;
-            pu.count = cnt;
-            a.units[u] = pu;
-            int pg = a.page_table[(int64_t)x.b * a.max_pages + j];
-            if (pg < 0 || pg >= a.num_pages) {
-                set_status(a.status, MSA_STATUS_PAGE_RANGE);
-                pg = -1;  // the tile kernel skips the block
+        a.unit_page[u] = pg;
+        for (int qi = 0; qi < x.nq; ++qi) {
+            int split = 255;
+            if ((mk[qi >> 5] >> (qi & 31)) & 1u) {
+                const int64_t slot0 = (((int64_t)x.b * a.Hkv + x.h) * a.Sq + x.q0 + qi) * a.topk;
+                split = 0;
+                for (int t = 0; t < a.topk; ++t)
+                    if (a.q2k[slot0 + t] == j && a.slot_split[slot0 + t] >= 0) split = a.slot_split[slot0 + t];
             }
-            a.unit_page[u] = pg;
-            int r = 0;
-            for (int w = 0; w < a.wq; ++w) {
-                uint32_t m = mk[w];
-                while (m) {
-                    const int qi = w * 32 + __ffs(m) - 1;
-                    m &= m - 1;
-                    const int64_t slot0 = (((int64_t)x.b * a.Hkv + x.h) * a.Sq + x.q0 + qi) * a.topk;
-                    int split = 0;
-                    for (int t = 0; t < a.topk; ++t)
-                        if (a.q2k[slot0 + t] == j && a.slot_split[slot0 + t] >= 0) split = a.slot_split[slot0 + t];
-                    const int gq = x.b * a.Sq + x.q0 + qi;
-                    a.qlist[start + r++] = gq | (split << 24);
-                }
-            }
+            a.qlist[start + qi] = (x.b * a.Sq + x.q0 + qi) | (split << 24);
         }
-        carry += pass_total;
-        __syncthreads();  // warp_tot is rewritten by the next pass
     }
 }
 
@@ -306,7 +284,7 @@ PagedWorkspace paged_workspace_layout(const PagedShape &d, int B, int Sq, int Hq
     w.split_counts = o;
     o = align_up(o + sizeof(int32_t) * (size_t)B * Sq * Hkv, 256);
     w.qlist = o;
-    o = align_up(o + sizeof(int32_t) * slots, 256);
+    o = align_up(o + sizeof(int32_t) * (size_t)d.groups * d.maxu * d.qg, 256);
     w.plan = o;
     o = align_up(o + sizeof(PlanHeader) + sizeof(PlanUnit) * (size_t)d.groups * d.maxu, 256);
     w.unit_page = o;
