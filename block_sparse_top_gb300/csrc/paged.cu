@@ -5,10 +5,11 @@
 // launches turn the selections into the tile kernel's work plan directly:
 //   1. union: per group, the ascending union of the blocks its queries
 //      selected (ids >= ceil(seqused/page) are padding, repeats count once),
-//      the bitmask of the queries that selected each block, every valid
-//      slot's split id and every query's split count;
+//      every valid slot's split id, every query's split count, and the split
+//      id of each (union block, query of the group), 255 where the query did
+//      not select the block;
 //   2. scan:  exclusive prefixes of the groups' union sizes and selection
-//      counts -> one global unit list and one global query list;
+//      counts -> one global unit list;
 //   3. write: one plan unit per union block (its page looked up once), and
 //      the unit's query table: every query of the group, packed query id |
 //      split << 24, split 255 for a query that did not select the block (the
@@ -32,7 +33,7 @@ namespace msa {
 namespace {
 
 struct PagedShape {
-    int qg, qgroups, groups, maxu, wq;
+    int qg, qgroups, groups, maxu;
 };
 
 PagedShape paged_shape(int B, int Sq, int Hkv, int qpk, int topk, int max_pages) {
@@ -41,14 +42,13 @@ PagedShape paged_shape(int B, int Sq, int Hkv, int qpk, int topk, int max_pages)
     d.qgroups = (int)ceil_div(Sq, d.qg);
     d.groups = B * Hkv * d.qgroups;
     d.maxu = std::min(std::min(Sq, d.qg) * topk, max_pages);
-    d.wq = (d.qg + 31) / 32;
     return d;
 }
 
 struct PlanArgs {
     const int32_t *q2k, *seqused, *page_table;
     int32_t *ulist;        // [groups][maxu] union block ids, ascending
-    uint32_t *umask;       // [groups][maxu][wq] queries of the group that selected the block
+    uint8_t *usplit;       // [groups][maxu][qg] split id of (union block, query of the group), 255: not selected
     int2 *ucount;          // [groups + 1] (union size, valid selections), then exclusive prefixes
     int32_t *slot_split;   // [B][Hkv][Sq][topk] split id of each slot, -1 for padding and repeats
     int32_t *split_counts; // [B*Sq][Hkv]
@@ -57,7 +57,7 @@ struct PlanArgs {
     PlanUnit *units;
     int32_t *unit_page;
     uint32_t *status;
-    int B, Sq, Hkv, qpk, topk, num_pages, max_pages, qg, qgroups, groups, maxu, wq;
+    int B, Sq, Hkv, qpk, topk, num_pages, max_pages, qg, qgroups, groups, maxu;
 };
 
 struct Group {
@@ -82,14 +82,12 @@ __global__ void __launch_bounds__(256) paged_union_kernel(PlanArgs a) {
     const int nwords = (a.max_pages + 31) / 32;
     uint32_t *bitmap = dsm;                                        // [nwords]
     int32_t *ul = reinterpret_cast<int32_t *>(bitmap + nwords);    // [maxu]
-    uint32_t *mk = reinterpret_cast<uint32_t *>(ul + a.maxu);      // [maxu * wq]
-    int32_t *spl = reinterpret_cast<int32_t *>(mk + a.maxu * a.wq);  // [qg * topk]
+    int32_t *spl = ul + a.maxu;                                    // [qg * topk]
     __shared__ int32_t warp_tot[8];
     __shared__ int32_t s_nu, s_nsel;
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const Group x = group_of(a, g);
     for (int i = tid; i < nwords; i += blockDim.x) bitmap[i] = 0u;
-    for (int i = tid; i < a.maxu * a.wq; i += blockDim.x) mk[i] = 0u;
     if (tid == 0) s_nsel = 0;
     __syncthreads();
     // split id of a slot: the number of distinct valid ids in the earlier slots
@@ -158,7 +156,11 @@ __global__ void __launch_bounds__(256) paged_union_kernel(PlanArgs a) {
     }
     __syncthreads();
     const int nu = s_nu;
-    // selection masks: the union position of each valid slot's block
+    // split table: 255 (not selected) for every (union block, query), then each
+    // valid slot's split id at its block's union position
+    uint8_t *us = a.usplit + (int64_t)g * a.maxu * a.qg;
+    for (int i = tid; i < nu * a.qg; i += blockDim.x) us[i] = 255;
+    __syncthreads();
     for (int i = tid; i < nslots; i += blockDim.x) {
         if (spl[i] < 0) continue;
         const int qi = i / a.topk;
@@ -169,11 +171,9 @@ __global__ void __launch_bounds__(256) paged_union_kernel(PlanArgs a) {
             if (ul[mid] < j) lo = mid + 1;
             else hi = mid;
         }
-        atomicOr(&mk[lo * a.wq + (qi >> 5)], 1u << (qi & 31));
+        us[lo * a.qg + qi] = (uint8_t)spl[i];
     }
-    __syncthreads();
     for (int e = tid; e < nu; e += blockDim.x) a.ulist[(int64_t)g * a.maxu + e] = ul[e];
-    for (int i = tid; i < nu * a.wq; i += blockDim.x) a.umask[(int64_t)g * a.maxu * a.wq + i] = mk[i];
     if (tid == 0) a.ucount[g] = make_int2(nu, s_nsel);
 }
 
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
     const int off = a.ucount[g].x;
     const int nu = a.ucount[g + 1].x - off;
     for (int e = threadIdx.x; e < nu; e += blockDim.x) {
-        const uint32_t *mk = a.umask + ((int64_t)g * a.maxu + e) * a.wq;
+        const uint8_t *us = a.usplit + ((int64_t)g * a.maxu + e) * a.qg;
         const int j = a.ulist[(int64_t)g * a.maxu + e];
         const int64_t u = off + e;
         const int start = (int)(u * a.qg);
@@ -252,13 +252,7 @@ __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
         }
         a.unit_page[u] = pg;
         for (int qi = 0; qi < x.nq; ++qi) {
-            int split = 255;
-            if ((mk[qi >> 5] >> (qi & 31)) & 1u) {
-                const int64_t slot0 = (((int64_t)x.b * a.Hkv + x.h) * a.Sq + x.q0 + qi) * a.topk;
-                split = 0;
-                for (int t = 0; t < a.topk; ++t)
-                    if (a.q2k[slot0 + t] == j && a.slot_split[slot0 + t] >= 0) split = a.slot_split[slot0 + t];
-            }
+            const int split = us[qi];
             a.qlist[start + qi] = (x.b * a.Sq + x.q0 + qi) | (split << 24);
         }
     }
@@ -266,7 +260,7 @@ __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
 
 // Workspace of msa_sparse_attn_paged_fwd: the union plan, then the split partials.
 struct PagedWorkspace {
-    size_t ulist, umask, ucount, slot_split, split_counts, qlist, plan, unit_page, fwd, fwd_bytes, bytes;
+    size_t ulist, usplit, ucount, slot_split, split_counts, qlist, plan, unit_page, fwd, fwd_bytes, bytes;
 };
 
 PagedWorkspace paged_workspace_layout(const PagedShape &d, int B, int Sq, int Hq, int Hkv, int topk) {
@@ -275,8 +269,8 @@ PagedWorkspace paged_workspace_layout(const PagedShape &d, int B, int Sq, int Hq
     size_t o = 0;
     w.ulist = o;
     o = align_up(o + sizeof(int32_t) * (size_t)d.groups * d.maxu, 256);
-    w.umask = o;
-    o = align_up(o + sizeof(uint32_t) * (size_t)d.groups * d.maxu * d.wq, 256);
+    w.usplit = o;
+    o = align_up(o + (size_t)d.groups * d.maxu * d.qg, 256);
     w.ucount = o;
     o = align_up(o + sizeof(int2) * ((size_t)d.groups + 1), 256);
     w.slot_split = o;
@@ -336,7 +330,7 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     a.seqused = seqused_k;
     a.page_table = page_table;
     a.ulist = reinterpret_cast<int32_t *>(ws + w.ulist);
-    a.umask = reinterpret_cast<uint32_t *>(ws + w.umask);
+    a.usplit = reinterpret_cast<uint8_t *>(ws + w.usplit);
     a.ucount = reinterpret_cast<int2 *>(ws + w.ucount);
     a.slot_split = reinterpret_cast<int32_t *>(ws + w.slot_split);
     a.split_counts = reinterpret_cast<int32_t *>(ws + w.split_counts);
@@ -347,10 +341,9 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     a.status = status_dev;
     a.B = B; a.Sq = Sq; a.Hkv = Hkv; a.qpk = qpk; a.topk = topk; a.num_pages = num_pages;
     a.max_pages = max_pages; a.qg = d.qg; a.qgroups = d.qgroups; a.groups = d.groups; a.maxu = d.maxu;
-    a.wq = d.wq;
 
     const size_t usmem = sizeof(uint32_t) * (((size_t)max_pages + 31) / 32) + sizeof(int32_t) * (size_t)d.maxu +
-                         sizeof(uint32_t) * (size_t)d.maxu * d.wq + sizeof(int32_t) * (size_t)d.qg * topk;
+                         sizeof(int32_t) * (size_t)d.qg * topk;
     MSA_CUDA_TRY(cudaFuncSetAttribute(paged_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)usmem));
     paged_union_kernel<<<d.groups, 256, usmem, stream>>>(a);
     MSA_LAUNCH_CHECK();
