@@ -169,14 +169,19 @@ int msa_sparse_attn_combine(const int32_t *split_counts, int B, int Sq, int Hq, 
  *   seqused_k  [B] int32, device (1 <= seqused_k[b] <= max_pages*page_size).
  *   q2k        [B][Hkv][Sq][topk] int32, device; ids >= ceil(seqused_k/page) are padding.
  *   o          [B*Sq][Hq][D] bf16; lse [B*Sq][Hq] fp32 or NULL.
- *   workspace  msa_sparse_attn_paged_fwd_workspace_size() bytes: the k->q
- *              CSR over logical blocks and its plan, each plan unit's page,
- *              and the split partials (topk per query head).
- * The work is the prefill's: msa_build_k2q_csr over (KV head, sequence,
- * logical block) with Skv = max_pages*page_size and seqused_k, a lookup of
- * each unit's physical page, the attention tiles over the pool (page entries
- * outside [0, num_pages) set MSA_STATUS_PAGE_RANGE and their block is
- * skipped), then the LSE combine.  Max max_pages: 8192.
+ *   workspace  msa_sparse_attn_paged_fwd_workspace_size() bytes: per group
+ *              its union of selected blocks and split table, the work plan
+ *              (one unit per union block with its page and query table), and
+ *              the split partials (topk per query head).
+ * The work: per group (sequence b, KV head h, 128/(Hq/Hkv) consecutive
+ * queries) the ascending union of the blocks its queries selected (ids at or
+ * past ceil(seqused_k[b]/page) are padding; repeats set MSA_STATUS_DUPLICATE
+ * and count once), each query's split ids and counts; then one attention tile
+ * per union block holding all the group's queries (rows of queries that did
+ * not select the block are masked; consecutive blocks of a group share the Q
+ * tile) over the block's physical page (entries outside [0, num_pages) set
+ * MSA_STATUS_PAGE_RANGE and the block is skipped); then the LSE combine.
+ * Max max_pages: 8192.
  */
 size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
 int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
