@@ -55,6 +55,9 @@ EDGE = [
     D("qpk8_sq1", qpk=8, Sq=1, topk=16, kv_len=16384),
     D("short_kv", qpk=16, Sq=8, topk=16, kv_len=128, trim=123),   # seqused 5 < Sq: early queries see nothing
     D("trim_zero", qpk=16, Sq=8, topk=4, kv_len=1024, trim=0),
+    # three query groups per (sequence, KV head), the last one partial: consecutive
+    # groups of one head share nothing, their Q tiles must not be reused
+    D("qpk16_three_groups", qpk=16, Sq=20, topk=8, kv_len=4096, Hkv=3),
 ]
 
 
