@@ -18,8 +18,7 @@
 //      no atomics on positions (bit-deterministic).
 // The plan then cuts every row into units of at most 8 chunks of 128 rows,
 // ordered by KV head, then by wave: wave w holds the queries [w*W, (w+1)*W)
-// with W sized so that one (head, wave) pass writes about 32 MiB of split
-// partials, which stay in L2 until they are combined.
+// (W: wave_queries in common.cuh).
 #include <algorithm>
 
 #include "common.cuh"
@@ -254,8 +253,8 @@ __device__ __forceinline__ int32_t lower_bound(const int32_t *a, int32_t lo, int
 
 // Segment (head h, wave w, row r) = the queries of row r in [w*W, (w+1)*W);
 // the flat index is head-major, then wave-major, so the unit list runs one
-// KV head at a time (its K/V stays in L2) and, within it, wave by wave (each
-// wave's split partials are all written within one short stretch).
+// KV head at a time (its K/V stays in L2) and, within it, wave by wave (the
+// CTAs read the Q rows of one wave's queries at a time).
 struct PlanShape {
     int64_t W, nwaves;
     int qpu;
