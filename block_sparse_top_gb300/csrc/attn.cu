@@ -105,6 +105,91 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4 *__restrict
     if (c == 0 && lse) lse[orow] = l;
 }
 
+// The combine for qhead_per_kv 16 (a group's pieces = 256 threads): one
+// persistent CTA per SM walks groups blockIdx.x, + gridDim.x, ...; thread 0
+// copies each group's split partials (n x 4 KB, contiguous) and statistics
+// (n x 128 B) into a ring of kRingBufs shared-memory buffers with bulk copies,
+// kRingBufs groups ahead, so that the bytes in flight do not live in
+// registers; the 256 threads merge from shared memory (same arithmetic as
+// combine_kernel) and release the buffer warp by warp.
+constexpr int kRingBufs = 3;
+__host__ __device__ constexpr uint32_t ring_buf_bytes(int topk) { return (uint32_t)topk * (4096u + 128u); }
+__global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__restrict__ o_part,
+                                                              const float2 *__restrict__ stat_part,
+                                                              const int32_t *__restrict__ split_counts,
+                                                              int64_t groups, int topk, uint4 *__restrict__ o,
+                                                              float *__restrict__ lse, uint32_t *status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const uint32_t base = smem_u32(smem), bb = ring_buf_bytes(topk);
+    const uint32_t bars = base + kRingBufs * bb;  // FULL[kRingBufs], EMPTY[kRingBufs]
+    auto full = [&](int b) { return bars + 8u * b; };
+    auto empty = [&](int b) { return bars + 8u * (kRingBufs + b); };
+    __shared__ int abort_flag_s;
+    volatile int *abort_flag = &abort_flag_s;
+    const int t = threadIdx.x, c = t >> 4, j = t & 15, warp = t >> 5, lane = t & 31;
+    if (t == 0) {
+        for (int b = 0; b < kRingBufs; ++b) {
+            tc::mbar_init(full(b), 1);
+            tc::mbar_init(empty(b), 8);  // one arrival per warp
+        }
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    const int64_t G = gridDim.x;
+    // thread 0: copy the k-th group of this CTA into buffer k % kRingBufs
+    auto issue = [&](int64_t k) -> bool {
+        const int64_t grp = blockIdx.x + k * G;
+        const int b = (int)(k % kRingBufs);
+        if (k >= kRingBufs &&
+            !tc::mbar_wait(empty(b), (uint32_t)(((k / kRingBufs) - 1) & 1), abort_flag, status, MSA_STATUS_TIMEOUT))
+            return false;
+        int n = split_counts[grp];
+        n = n < topk ? n : topk;
+        if (n > 0) {
+            tc::mbar_arrive_expect_tx(full(b), (uint32_t)n * (4096u + 128u));
+            tc::bulk_load(base + b * bb, o_part + grp * topk * 256, (uint32_t)n * 4096u, full(b));
+            tc::bulk_load(base + b * bb + topk * 4096u, stat_part + grp * topk * 16, (uint32_t)n * 128u, full(b));
+        } else {
+            tc::mbar_arrive(full(b));
+        }
+        return true;
+    };
+    bool ok = true;
+    int64_t issued = 0, k = 0;  // groups copied (thread 0), groups merged
+    if (t == 0)
+        for (; issued < kRingBufs && blockIdx.x + issued * G < groups && ok; ++issued) ok = issue(issued);
+    for (; blockIdx.x + k * G < groups; ++k) {
+        const int64_t grp = blockIdx.x + k * G;
+        const int b = (int)(k % kRingBufs);
+        ok = tc::mbar_wait(full(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status, MSA_STATUS_TIMEOUT);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        int n = split_counts[grp];
+        n = n < topk ? n : topk;
+        uint4 out;
+        float l;
+        combine_piece<16, 16, true>(reinterpret_cast<const uint4 *>(smem + b * bb),
+                                    reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096), 0, n, topk, 16, c, j,
+                                    out, l);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(empty(b));
+        const int64_t orow = grp * 16 + j;
+        o[orow * 16 + c] = out;
+        if (c == 0 && lse) lse[orow] = l;
+        if (t == 0 && blockIdx.x + (k + kRingBufs) * G < groups && ok) {
+            ok = issue(k + kRingBufs);
+            if (ok) ++issued;
+        }
+    }
+    // after an abort, copies still in flight land before the CTA exits
+    if (t == 0) {
+        volatile int dummy = 0;
+        for (int64_t kk = k; kk < issued; ++kk)
+            tc::mbar_wait(full((int)(kk % kRingBufs)), (uint32_t)((kk / kRingBufs) & 1), &dummy, status, 0);
+    }
+    (void)warp;
+}
+
 }  // namespace
 }  // namespace msa
 
@@ -172,7 +257,13 @@ extern "C" int msa_sparse_attn_combine(const int32_t *split_counts, int B, int S
     const uint4 *op = reinterpret_cast<const uint4 *>(ws + w.o_part);
     const float2 *sp = reinterpret_cast<const float2 *>(ws + w.stat_part);
     uint4 *ob = static_cast<uint4 *>(o);
-    if (topk <= 16)
+    if (qpk == 16 && topk <= 16) {
+        // staged through a shared-memory ring, one persistent CTA per SM
+        const size_t smem = kRingBufs * ring_buf_bytes(topk) + 16u * kRingBufs;
+        MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
+        combine_ring_kernel<<<grid, 256, smem, stream>>>(op, sp, split_counts, groups, topk, ob, lse, nullptr);
+    } else if (topk <= 16)
         combine_kernel<16><<<(unsigned)blocks, 256, 0, stream>>>(op, sp, split_counts, groups, qpk, topk, ob, lse);
     else
         combine_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(op, sp, split_counts, groups, qpk, topk, ob, lse);

@@ -27,8 +27,10 @@ __host__ __device__ inline int64_t part_stat_index(int64_t grp, int topk, int qp
 // Merges the first n of topk splits of piece (group grp, 8-dim chunk c, head j
 // of the group) into out (8 bf16) and lse_out.  Every load of a batch of BATCH
 // splits is issued before any is used (all topk slots are read, those at or
-// past n are ignored); batches merge online with a running max.
-template <int MAXS, int BATCH = 16>
+// past n are ignored); batches merge online with a running max.  SMEM: the
+// group's partials and statistics were staged in shared memory (o_part and
+// stat_part point at the copy, grp 0).
+template <int MAXS, int BATCH = 16, bool SMEM = false>
 __device__ __forceinline__ void combine_piece(const uint4 *__restrict__ o_part, const float2 *__restrict__ stat_part,
                                               int64_t grp, int n, int topk, int qpk, int c, int j, uint4 &out,
                                               float &lse_out) {
@@ -43,10 +45,11 @@ __device__ __forceinline__ void combine_piece(const uint4 *__restrict__ o_part, 
         float2 sv[BATCH];
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)
-            if (s0 + t < topk) v[t] = __ldcs(src + (s0 + t) * o_stride);  // read once: evict first
+            if (s0 + t < topk) v[t] = SMEM ? src[(s0 + t) * o_stride] : __ldcs(src + (s0 + t) * o_stride);
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)
-            sv[t] = (s0 + t < topk) ? __ldg(st + (int64_t)(s0 + t) * qpk) : make_float2(-INFINITY, 0.f);
+            sv[t] = (s0 + t < topk) ? (SMEM ? st[(s0 + t) * qpk] : __ldg(st + (int64_t)(s0 + t) * qpk))
+                                    : make_float2(-INFINITY, 0.f);
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)
             if (s0 + t >= n) sv[t].x = -INFINITY;

@@ -164,6 +164,13 @@ __device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(pol)
         : "memory");
 }
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned) completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
