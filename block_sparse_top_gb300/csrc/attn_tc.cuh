@@ -12,8 +12,9 @@
 //               128 gathered Q rows (128/qhead_per_kv queries x all heads of
 //               the GQA group) by TMA into the Q ring: one 5D box per query
 //               (its whole group) when qhead_per_kv >= 8, four rows per
-//               tile::gather4 copy otherwise.  The copy engine's cost is per
-//               request, so requests are kept few and large.
+//               tile::gather4 copy otherwise.  Requests are kept few and
+//               large, and each lane issues one of them, so that one
+//               instruction issues a chunk's copies.
 //   warp 1      NVFP4 only: dequantises the K and V block into the same
 //               swizzled bf16 layout (exact products).
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
@@ -110,10 +111,6 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
     x.nch = (pu.count + qc - 1) / qc;
     x.page = p.unit_page ? p.unit_page[u] : 0;
     return x;
-}
-
-__device__ __forceinline__ int pick4(const int (&v)[4], int s) {
-    return s == 0 ? v[0] : s == 1 ? v[1] : s == 2 ? v[2] : v[3];
 }
 
 }  // namespace tck
@@ -278,30 +275,28 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs), p.qpk >= 8 ? (uint32_t)(nq * p.qpk * 256) : 32768u);
             if (!load_q) {
             } else if (p.qpk >= 8) {
-                for (int qi = 0; qi < nq; ++qi) {
-                    const int gq = __shfl_sync(0xffffffffu, ids[0], qi);
-                    if (lane == 0)
-                        tc::tma_load_5d(qt + (uint32_t)(qi * p.qpk * 256), &tm_q, bar(L::Q_FULL + qs), 0, 0, 0, 0,
-                                        gq * p.Hkv + x.h);
-                }
+                // lane l issues query slot l's box: one instruction issues them all
+                if (lane < nq)
+                    tc::tma_load_5d(qt + (uint32_t)(lane * p.qpk * 256), &tm_q, bar(L::Q_FULL + qs), 0, 0, 0, 0,
+                                    ids[0] * p.Hkv + x.h);
             } else {
-                for (int j = 0; j < 32; ++j) {
-                    int r[4];
-                    const int slot4 = ((4 * j) / p.qpk) >> 5;
-                    const int v = pick4(ids, slot4);
+                // lane j issues the gather4 pair of rows 4j .. 4j+3
+                int r[4];
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int R = 4 * j + t, qi = R / p.qpk;
-                        int gq = __shfl_sync(0xffffffffu, v, qi & 31);
-                        if (gq < 0) gq = first;
-                        r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
-                    }
-                    if (lane == 0) {
-                        tc::tma_gather4_hint(qt + j * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
-                        tc::tma_gather4_hint(qt + 16384 + j * 512, &tm_q, bar(L::Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
-                                             keep);
-                    }
+                for (int t = 0; t < 4; ++t) {
+                    const int R = 4 * lane + t, qi = R / p.qpk;
+                    const int g0 = __shfl_sync(0xffffffffu, ids[0], qi & 31);
+                    const int g1 = __shfl_sync(0xffffffffu, ids[1], qi & 31);
+                    const int g2 = __shfl_sync(0xffffffffu, ids[2], qi & 31);
+                    const int g3 = __shfl_sync(0xffffffffu, ids[3], qi & 31);
+                    const int sl = qi >> 5;
+                    int gq = sl == 0 ? g0 : sl == 1 ? g1 : sl == 2 ? g2 : g3;
+                    if (gq < 0) gq = first;
+                    r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
                 }
+                tc::tma_gather4_hint(qt + lane * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
+                tc::tma_gather4_hint(qt + 16384 + lane * 512, &tm_q, bar(L::Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
+                                     keep);
             }
             ++ci;
             if (++c == x.nch) {
