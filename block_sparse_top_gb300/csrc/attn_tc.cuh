@@ -223,26 +223,26 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             if (lane == 0) tc::mbar_arrive(bar(L::RING_EMPTY + slot));
             const int kb = ui % NKV;
             if (c == 0 && KV_FORMAT == MSA_KV_BF16) {
-                if (lane == 0) {
-                    if (ui >= NKV)
-                        ok = tc::mbar_wait(bar(L::KV_EMPTY + kb), ((ui / NKV) - 1) & 1, abort_flag, p.status,
-                                           MSA_STATUS_TIMEOUT);
-                    if (ok) {
-                        // token row: dense [B][Skv] layout, or the unit's page of the pool
-                        const int row = p.unit_page ? x.page * kBlk : x.b * p.Skv + x.tok0;
-                        if (!p.unit_page || x.page >= 0) {
-                            tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), 65536);
-                            const uint32_t ks = base + L::K + kb * 32768, vs = base + L::V + kb * 32768;
-                            tc::tma_load_4d(ks, &tm_k, bar(L::KV_FULL + kb), 0, row, 0, x.h);
-                            tc::tma_load_4d(vs, &tm_v, bar(L::KV_FULL + kb), 0, row, 0, x.h);
-                        } else {
-                            tc::mbar_arrive(bar(L::KV_FULL + kb));  // invalid page: no copy, keys masked
-                        }
-                        kv_armed[kb] = (ui / NKV) & 1;
-                    }
-                }
+                if (lane == 0 && ui >= NKV)
+                    ok = tc::mbar_wait(bar(L::KV_EMPTY + kb), ((ui / NKV) - 1) & 1, abort_flag, p.status,
+                                       MSA_STATUS_TIMEOUT);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                // token row: dense [B][Skv] layout, or the unit's page of the pool
+                const int row = p.unit_page ? x.page * kBlk : x.b * p.Skv + x.tok0;
+                const bool copy = !p.unit_page || x.page >= 0;
+                if (lane == 0) {
+                    if (copy)
+                        tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), 65536);
+                    else
+                        tc::mbar_arrive(bar(L::KV_FULL + kb));  // invalid page: no copy, keys masked
+                    kv_armed[kb] = (ui / NKV) & 1;
+                }
+                __syncwarp();
+                // lane 0 copies K, lane 1 V, in one instruction
+                if (copy && lane < 2)
+                    tc::tma_load_4d(base + (lane ? L::V : L::K) + kb * 32768, lane ? &tm_v : &tm_k,
+                                    bar(L::KV_FULL + kb), 0, row, 0, x.h);
             }
             // Paged decode: a unit is one chunk holding all queries of its group
             // (rows of queries that did not select the block are masked), so
@@ -576,17 +576,17 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     tc::tmem_ld_wait();
                     // keys past the causal limit (diagonal block rows) become -inf
                     if (nvis < 128) {
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 128; ++j)
                             if (j >= nvis) r[j] = 0xff800000u;
                     }
                     // row max: three-input max, four independent chains
                     float mm[4];
-    #pragma unroll
+#pragma unroll
                     for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 128; j += 8) {
-    #pragma unroll
+#pragma unroll
                         for (int a = 0; a < 4; ++a)
                             mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                     }
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                     const float2 nm2 = make_float2(-mc, -mc);
                     float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < 64; ++j) {
                         float2 e = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
                         e.x = ex2_approx(e.x);
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         // contiguous, so each store instruction writes whole runs
                         const int64_t grp = (int64_t)gq * p.Hkv + x.h;
                         uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-    #pragma unroll
+#pragma unroll
                         for (int v4 = 0; v4 < 16; ++v4) {
                             uint4 o4;
                             o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
@@ -660,23 +660,23 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     auto mask_half = [&](int hf) {
                         const int lim = nvis - 64 * hf;
                         if (lim < 64) {
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 64; ++j)
                                 if (j >= lim) r[j] = 0xff800000u;
                         }
                     };
                     // row max: three-input max, four independent chains
                     float mm[4];
-    #pragma unroll
+#pragma unroll
                     for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-    #pragma unroll
+#pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
                         tc::tmem_ld_wait();
                         mask_half(hf);
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 64; j += 8) {
-    #pragma unroll
+#pragma unroll
                             for (int a = 0; a < 4; ++a)
                                 mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                         }
@@ -690,12 +690,12 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                     const float2 nm2 = make_float2(-mc, -mc);
                     float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    #pragma unroll 1
+#pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         tc::tmem_ld64(s_addr + 64 * hf, r);
                         tc::tmem_ld_wait();
                         mask_half(hf);
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             float2 e =
                                 __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     // contiguous, so each store instruction writes whole runs
                     const int64_t grp = (int64_t)gq * p.Hkv + x.h;
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-    #pragma unroll 1
+#pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         tc::tmem_ld64(o_addr + 64 * hf, r);
                         tc::tmem_ld_wait();
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                             tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: the next PV may start
                         }
                         if (valid) {
-    #pragma unroll
+#pragma unroll
                             for (int v4 = 0; v4 < 8; ++v4) {
                                 uint4 o4;
                                 o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
