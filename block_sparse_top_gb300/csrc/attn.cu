@@ -47,8 +47,8 @@ int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap
     const size_t smem = tck::Layout<NKV, NQ>::BYTES;
     MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW><<<grid, tck::kThreads, smem, stream>>>(mk, mv, mq, t);
-    MSA_LAUNCH_CHECK();
+    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>, dim3(grid), dim3(tck::kThreads), smem,
+                            stream, mk, mv, mq, t));
     return MSA_OK;
 }
 }  // namespace
@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4 *__restrict
                                                          const int32_t *__restrict__ split_counts, int64_t groups,
                                                          int qpk, int topk, uint4 *__restrict__ o,
                                                          float *__restrict__ lse) {
+    grid_dependency_wait();  // the partials come from the previous kernel
+    grid_dependents_launch();
     const int64_t item = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int per_g = 16 * qpk;
     if (item >= groups * per_g) return;
@@ -135,6 +137,8 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
+    grid_dependency_wait();  // the partials come from the previous kernel
+    grid_dependents_launch();
     __syncthreads();
     const int64_t G = gridDim.x;
     // thread 0: copy the k-th group of this CTA into buffer k % kRingBufs
@@ -262,12 +266,15 @@ extern "C" int msa_sparse_attn_combine(const int32_t *split_counts, int B, int S
         const size_t smem = kRingBufs * ring_buf_bytes(topk) + 16u * kRingBufs;
         MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
-        combine_ring_kernel<<<grid, 256, smem, stream>>>(op, sp, split_counts, groups, topk, ob, lse, nullptr);
-    } else if (topk <= 16)
-        combine_kernel<16><<<(unsigned)blocks, 256, 0, stream>>>(op, sp, split_counts, groups, qpk, topk, ob, lse);
-    else
-        combine_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(op, sp, split_counts, groups, qpk, topk, ob, lse);
-    MSA_LAUNCH_CHECK();
+        MSA_CUDA_TRY(launch_pdl(combine_ring_kernel, dim3(grid), dim3(256), smem, stream, op, sp, split_counts, groups,
+                                topk, ob, lse, (uint32_t *)nullptr));
+    } else if (topk <= 16) {
+        MSA_CUDA_TRY(launch_pdl(combine_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, split_counts,
+                                groups, qpk, topk, ob, lse));
+    } else {
+        MSA_CUDA_TRY(launch_pdl(combine_kernel<32>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, split_counts,
+                                groups, qpk, topk, ob, lse));
+    }
     return MSA_OK;
 }
 

@@ -138,15 +138,6 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qc = 128 / p.qpk;
-    const int work = p.plan->work_count;
-    // The CTA's units: every gridDim.x-th of the plan (prefill: consecutive
-    // units read the same K/V head close together in time), or one
-    // contiguous run (paged decode: consecutive units of a group share the Q
-    // tile).  Every role walks the same sequence.
-    constexpr bool contiguous = PAGED;
-    const int u_begin = contiguous ? (int)((int64_t)work * blockIdx.x / gridDim.x) : (int)blockIdx.x;
-    const int u_end = contiguous ? (int)((int64_t)work * (blockIdx.x + 1) / gridDim.x) : work;
-    const int u_step = contiguous ? 1 : (int)gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < NKV; ++i) {
@@ -186,6 +177,18 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + L::TSLOT);
+    // the plan (and, in decode, the query tables) come from the previous kernel
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int work = p.plan->work_count;
+    // The CTA's units: every gridDim.x-th of the plan (prefill: consecutive
+    // units read the same K/V head close together in time), or one
+    // contiguous run (paged decode: consecutive units of a group share the Q
+    // tile).  Every role walks the same sequence.
+    constexpr bool contiguous = PAGED;
+    const int u_begin = contiguous ? (int)((int64_t)work * blockIdx.x / gridDim.x) : (int)blockIdx.x;
+    const int u_end = contiguous ? (int)((int64_t)work * (blockIdx.x + 1) / gridDim.x) : work;
+    const int u_step = contiguous ? 1 : (int)gridDim.x;
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loader

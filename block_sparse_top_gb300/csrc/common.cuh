@@ -36,6 +36,34 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  A kernel launched by launch_pdl may be
+// scheduled while the previous kernel on its stream is still finishing: it
+// runs its prologue (barrier set-up, tensor-memory allocation), then
+// grid_dependency_wait() blocks until the previous kernel has completed and
+// its writes are visible, so nothing that kernel produces may be read, and
+// nothing it reads may be written, before that call (a kernel launched the
+// ordinary way returns from it at once).  grid_dependents_launch() lets the
+// next kernel on the stream be scheduled in the same way.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              A &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<A &&>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Work plan shared by the CSR builder (writer) and the prefill kernel (reader)
 // ---------------------------------------------------------------------------

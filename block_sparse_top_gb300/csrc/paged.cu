@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(256) paged_union_kernel(PlanArgs a) {
     __shared__ int32_t warp_tot[8];
     __shared__ int32_t s_nu, s_nsel;
     const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependency_wait();  // the previous call's kernels may still read this workspace
+    grid_dependents_launch();
     const Group x = group_of(a, g);
     for (int i = tid; i < nwords; i += blockDim.x) bitmap[i] = 0u;
     if (tid == 0) s_nsel = 0;
@@ -185,6 +187,8 @@ __global__ void __launch_bounds__(1024) paged_scan_kernel(PlanArgs a) {
     __shared__ int2 carry_s;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) carry_s = make_int2(0, 0);
+    grid_dependency_wait();
+    grid_dependents_launch();
     __syncthreads();
     for (int base = 0; base < a.groups; base += blockDim.x) {
         const int i = base + threadIdx.x;
@@ -231,6 +235,8 @@ __global__ void __launch_bounds__(1024) paged_scan_kernel(PlanArgs a) {
 // query table (all queries of the group, ascending) is qlist[u*qg .. + nq).
 __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
     const int g = blockIdx.x;
+    grid_dependency_wait();
+    grid_dependents_launch();
     const Group x = group_of(a, g);
     const int off = a.ucount[g].x;
     const int nu = a.ucount[g + 1].x - off;
@@ -345,12 +351,9 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     const size_t usmem = sizeof(uint32_t) * (((size_t)max_pages + 31) / 32) + sizeof(int32_t) * (size_t)d.maxu +
                          sizeof(int32_t) * (size_t)d.qg * topk;
     MSA_CUDA_TRY(cudaFuncSetAttribute(paged_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)usmem));
-    paged_union_kernel<<<d.groups, 256, usmem, stream>>>(a);
-    MSA_LAUNCH_CHECK();
-    paged_scan_kernel<<<1, 1024, 0, stream>>>(a);
-    MSA_LAUNCH_CHECK();
-    paged_write_kernel<<<d.groups, 128, 0, stream>>>(a);
-    MSA_LAUNCH_CHECK();
+    MSA_CUDA_TRY(launch_pdl(paged_union_kernel, dim3(d.groups), dim3(256), usmem, stream, a));
+    MSA_CUDA_TRY(launch_pdl(paged_scan_kernel, dim3(1), dim3(1024), 0, stream, a));
+    MSA_CUDA_TRY(launch_pdl(paged_write_kernel, dim3(d.groups), dim3(128), 0, stream, a));
 
     const FwdWorkspace fw = fwd_workspace_layout(B, Sq, Hq, topk, D);
     char *fws = ws + w.fwd;

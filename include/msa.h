@@ -18,6 +18,11 @@
  *     caller owns every buffer (inputs, outputs, plan, workspace);
  *   - calls are asynchronous on `stream`, never synchronise the device and
  *     never allocate memory;
+ *   - the attention, combine and paged-plan kernels are launched with
+ *     programmatic stream serialization: one may start its prologue while the
+ *     previous kernel on `stream` drains, but reads and writes nothing in
+ *     global memory before that kernel has completed, so stream order holds
+ *     for the caller's own work on either side of a call;
  *   - the return value is an MSA_* status; on any error nothing is launched;
  *   - workspaces are caller-allocated, 256-byte aligned, sized by the
  *     matching *_workspace_size() query;
