@@ -245,7 +245,7 @@ def oracle_rate(spec: synth.PrefillSpec, x_cpu: dict, budget_s: float, seed: int
 # ---------------------------------------------------------------------------
 
 WORKLOADS = {
-    "causal_sink_32k": synth.C2_SINK32K,
+    "causal_sink_32k": synth.CAUSAL_SINK_32K,
     # smaller case of the same kernel for ncu captures (partials ~1.1 GB on the device)
     "causal_sink_16k_1kv": synth.PrefillSpec("causal_sink_16k_1kv", B=1, Sq=16384, Skv=16384, Hkv=1, qpk=16,
                                              topk=16, causal=True, pattern="sink"),
@@ -412,7 +412,7 @@ def decode_sweep(args, dev, peaks, peak_src):
     import block_sparse_top_gb300 as msa
     out = []
     for L in args.decode_L:
-        spec = synth.c3_decode(L)
+        spec = synth.paged_decode_spec(L)
         first = synth.make_decode_inputs(spec, device=dev)
         nbytes = decode_bytes(spec, first["q2k"], first["seqused"])
         nsets = max(1, math.ceil(600e6 / nbytes))
@@ -464,7 +464,7 @@ def decode_sweep(args, dev, peaks, peak_src):
 # ---------------------------------------------------------------------------
 
 def run_reference(args, world, rank):
-    spec = synth.C2_SINK32K
+    spec = synth.CAUSAL_SINK_32K
     x_cpu = synth.make_prefill_inputs(spec, device="cuda" if torch.cuda.is_available() else "cpu")
     x_cpu = {k_: v_.cpu() for k_, v_ in x_cpu.items()}
     per_step = max(0.2, args.ref_budget / max(1, args.steps + args.warmup))

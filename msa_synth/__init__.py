@@ -351,21 +351,22 @@ class DecodeSpec:
         return max(1, self.kv_len - self.trim)
 
 
-# The five workloads named by the build's measurement plan.
-C1_TINY = PrefillSpec("tiny_noncausal_1k", B=1, Sq=1024, Skv=1024, Hkv=1, qpk=2, topk=4,
-                      causal=False, pattern="perm_prefix")
-C2_SINK32K = PrefillSpec("causal_sink_32k", B=1, Sq=32768, Skv=32768, Hkv=4, qpk=16, topk=16,
-                         causal=True, pattern="sink")
-C4_UNIFORM48K = PrefillSpec("causal_uniform_48k", B=1, Sq=49152, Skv=49152, Hkv=1, qpk=16, topk=16,
-                            causal=True, pattern="uniform")
-C5_SINK384K = PrefillSpec("causal_sink_384k", B=1, Sq=393216, Skv=393216, Hkv=1, qpk=2, topk=16,
-                          causal=True, pattern="sink")
-C5_SINK384K_NVFP4 = PrefillSpec("causal_sink_384k_nvfp4", B=1, Sq=393216, Skv=393216, Hkv=1, qpk=2,
-                                topk=16, causal=True, pattern="sink", kv_format="nvfp4")
+# The prefill workloads: a tiny non-causal case, then causal 32K, 48K and 384K
+# cases (the last also with NVFP4 K/V).  paged_decode_spec gives the decode sweep.
+TINY_NONCAUSAL_1K = PrefillSpec("tiny_noncausal_1k", B=1, Sq=1024, Skv=1024, Hkv=1, qpk=2, topk=4,
+                                causal=False, pattern="perm_prefix")
+CAUSAL_SINK_32K = PrefillSpec("causal_sink_32k", B=1, Sq=32768, Skv=32768, Hkv=4, qpk=16, topk=16,
+                              causal=True, pattern="sink")
+CAUSAL_UNIFORM_48K = PrefillSpec("causal_uniform_48k", B=1, Sq=49152, Skv=49152, Hkv=1, qpk=16, topk=16,
+                                 causal=True, pattern="uniform")
+CAUSAL_SINK_384K = PrefillSpec("causal_sink_384k", B=1, Sq=393216, Skv=393216, Hkv=1, qpk=2, topk=16,
+                               causal=True, pattern="sink")
+CAUSAL_SINK_384K_NVFP4 = PrefillSpec("causal_sink_384k_nvfp4", B=1, Sq=393216, Skv=393216, Hkv=1, qpk=2,
+                                     topk=16, causal=True, pattern="sink", kv_format="nvfp4")
 DECODE_SWEEP_L = tuple(1024 << i for i in range(8))   # 1K .. 128K
 
 
-def c3_decode(kv_len: int) -> DecodeSpec:
+def paged_decode_spec(kv_len: int) -> DecodeSpec:
     return DecodeSpec(f"paged_decode_{kv_len // 1024}k", B=32, Sq=8, Hkv=4, qpk=16, topk=16,
                       kv_len=kv_len, trim=17)
 

@@ -1,6 +1,6 @@
 """Shared comparison helpers for the GPU parity tests (tests only).
 
-Tolerances (stated by the build's target): attention output max |err| <= 2e-2
+Tolerances (the accuracy bar for bf16 output): attention output max |err| <= 2e-2
 and mean |err| <= 2e-3 against the float64 oracle; LSE relative error <= 1e-3
 where finite; -inf rows must match exactly.  Integer/index work is bit-exact.
 """

@@ -52,11 +52,11 @@ def test_visible_key_count_matches_the_workload_figures():
     import bench
     import msa_synth as synth
     # 32K causal sink: 4 * 128 * 16 * visible keys = 2.0664e12 effective FLOP
-    spec = synth.C2_SINK32K
+    spec = synth.CAUSAL_SINK_32K
     q2k = synth.make_prefill_q2k(spec)
     assert abs(bench.prefill_flops(spec, q2k) - 2.0664e12) / 2.0664e12 < 1e-3
     # tiny non-causal: every selected block fully visible
-    t = synth.C1_TINY
+    t = synth.TINY_NONCAUSAL_1K
     q2k = synth.make_prefill_q2k(t)
     assert bench.prefill_flops(t, q2k) == 4 * 128 * 2 * 1024 * 4 * 128
     # a duplicate and an out-of-range id add nothing

@@ -52,7 +52,7 @@ def P(name, **kw):
 
 
 SMALL = [
-    synth.C1_TINY,
+    synth.TINY_NONCAUSAL_1K,
     P("sink_qpk16_ragged", Sq=700, Skv=1024),
     P("sink_qpk8_topk16", qpk=8, topk=16, Sq=1500, Skv=2048),
     P("uniform_qpk4", qpk=4, pattern="uniform", Sq=2100, Skv=2048, topk=16),
@@ -138,7 +138,7 @@ def test_prefill_mid_size_sampled(spec):
     check_spec(spec, rows=rows)
 
 
-FULL = [synth.C2_SINK32K, synth.C4_UNIFORM48K, synth.C5_SINK384K]
+FULL = [synth.CAUSAL_SINK_32K, synth.CAUSAL_UNIFORM_48K, synth.CAUSAL_SINK_384K]
 
 
 @pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
@@ -186,7 +186,7 @@ def test_nvfp4_kv_matches_oracle_and_dequantised_bf16_exactly(spec):
 
 def test_nvfp4_full_size_sampled():
     import block_sparse_top_gb300 as msa
-    spec = synth.C5_SINK384K_NVFP4
+    spec = synth.CAUSAL_SINK_384K_NVFP4
     x = synth.make_prefill_inputs(spec, device=DEV)
     kp, ks = msa.nvfp4_quantize(x["k"])
     vp, vs = msa.nvfp4_quantize(x["v"])

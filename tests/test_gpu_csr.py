@@ -53,7 +53,7 @@ def _check_plan(csr):
 
 
 CASES = [
-    ("tiny_noncausal", synth.C1_TINY),
+    ("tiny_noncausal", synth.TINY_NONCAUSAL_1K),
     ("sink_small", synth.PrefillSpec("s", B=2, Sq=1000, Skv=2048, Hkv=3, qpk=16, topk=16, causal=True,
                                      pattern="sink")),
     ("uniform_small", synth.PrefillSpec("u", B=1, Sq=3000, Skv=2500, Hkv=1, qpk=2, topk=8, causal=True,
@@ -96,7 +96,7 @@ def test_csr_block_selected_by_no_query_and_empty_queries():
     _check_plan(csr)
 
 
-@pytest.mark.parametrize("spec", [synth.C2_SINK32K, synth.C4_UNIFORM48K, synth.C5_SINK384K],
+@pytest.mark.parametrize("spec", [synth.CAUSAL_SINK_32K, synth.CAUSAL_UNIFORM_48K, synth.CAUSAL_SINK_384K],
                          ids=lambda s: s.name)
 def test_csr_bit_exact_full_size(spec):
     q2k = synth.make_prefill_q2k(spec, device=DEV)

@@ -31,13 +31,13 @@ def run_case(spec, rows=None, mutate=None):
 
 @pytest.mark.parametrize("L", [1024, 2048, 4096, 8192])
 def test_decode_sweep_small_full_parity(L):
-    st, _, _ = run_case(synth.c3_decode(L))
+    st, _, _ = run_case(synth.paged_decode_spec(L))
     assert st == 0
 
 
 @pytest.mark.parametrize("L", [32768, 131072])
 def test_decode_sweep_large_sampled(L):
-    spec = synth.c3_decode(L)
+    spec = synth.paged_decode_spec(L)
     rows = synth.sample_query_rows(spec.B * spec.Sq, 24, must=[0, 7, 255])
     run_case(spec, rows=rows)
 
@@ -90,7 +90,7 @@ def test_decode_bad_page_entry_sets_status_and_skips_block():
 
 def test_decode_repeat_calls_identical():
     import block_sparse_top_gb300 as msa
-    spec = synth.c3_decode(4096)
+    spec = synth.paged_decode_spec(4096)
     d = synth.make_decode_inputs(spec, device=DEV)
     a = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], d["q2k"])
     b = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], d["q2k"])

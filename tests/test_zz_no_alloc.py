@@ -49,7 +49,7 @@ def _close(a_o, a_l, b_o, b_l):
 def test_noalloc_decode_matches_allocating_entry_point_twice(L_kv):
     import block_sparse_top_gb300 as msa
     L = msa.lib()
-    spec = synth.c3_decode(L_kv)
+    spec = synth.paged_decode_spec(L_kv)
     d = synth.make_decode_inputs(spec, device=DEV)
     ref_o, ref_l = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"],
                                              d["q2k"])
