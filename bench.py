@@ -46,7 +46,7 @@ KERNELS_PER_PAGED = 5    # union, scan, plan write, attention tiles, LSE combine
 # the 32K causal sink workload from one single-pass ncu capture
 # (dram__bytes_read.sum 2.47 GB + dram__bytes_write.sum 8.54 GB), keyed by the
 # hash of the source it was measured on (stale -> reported as null).
-PROFILED_TRAFFIC: dict = {"ba6811be1481a4e2": 1.101e10}
+PROFILED_TRAFFIC: dict = {"b5ee4a9835e4ca32": 1.101e10}
 
 
 # ---------------------------------------------------------------------------

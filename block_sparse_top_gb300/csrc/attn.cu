@@ -47,8 +47,8 @@ int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap
     const size_t smem = tck::Layout<NKV, NQ>::BYTES;
     MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>, dim3(grid), dim3(tck::kThreads), smem,
-                            stream, mk, mv, mq, t));
+    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>, dim3(grid),
+                            dim3(tck::threads_for(WHOLE_ROW)), smem, stream, mk, mv, mq, t));
     return MSA_OK;
 }
 }  // namespace

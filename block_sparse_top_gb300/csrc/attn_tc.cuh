@@ -1,6 +1,6 @@
 // attn_tc.cuh -- the tcgen05 (5th-gen tensor core) block-sparse attention tile
 // kernel (prefill, and paged decode): persistent, one CTA per SM,
-// warp-specialised, 12 warps.
+// warp-specialised, 16 warps in prefill and 12 in paged decode.
 //
 //   warp 11     feed: walks the CTA's chunks in plan order and copies each
 //               chunk's plan unit, page and query ids into a 4-entry shared
@@ -19,14 +19,18 @@
 //               swizzled bf16 layout (exact products).
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
 //               O_{i-1} = P_{i-1} V with P read from tensor memory.
-//   warps 3-6,  softmax + epilogue for even / odd chunks: each thread owns one
-//   warps 7-10  S row (TMEM lane), reads it in two halves of 64 columns, applies the
+//   warps 3-6,  softmax for even / odd chunks: each thread owns one S row
+//   warps 7-10  (TMEM lane), reads it in two halves of 64 columns, applies the
 //               bottom-right causal limit, writes P = exp(S - m) as bf16 over
-//               S, then stores the split partial unnormalised -- O = P V as
-//               bf16 with its statistics (m * scale, l = sum P) -- so that the
-//               combine applies each split's weight and 1/l in one product.
-//               Packed f32x2 FMA/add and three-input max halve the per-element
+//               S and stores the split's statistics (m * scale, l = sum P);
+//               the split partial is kept unnormalised so that the combine
+//               applies each split's weight and 1/l in one product.  Packed
+//               f32x2 FMA/add and three-input max halve the per-element
 //               instruction count of the row pass.
+//   warps 12-15 prefill epilogue: once PV has run, each chunk's O = P V (TMEM
+//               lanes of the warp) -> bf16 split partial, so the softmax warps
+//               never wait for PV.  In paged decode (12 warps, whole-row
+//               softmax) the softmax warps store O themselves.
 //
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 // Every wait is bounded; on a timeout the CTA raises MSA_STATUS_TIMEOUT,
@@ -60,7 +64,10 @@ namespace tck {
 
 constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3, kWarpFeed = 11;
+constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3, kWarpFeed = 11, kWarpEpi0 = 12;
+// Threads of an instance: prefill adds an epilogue warpgroup (warps 12-15)
+// that stores each chunk's O; in paged decode the softmax warps store it.
+constexpr int threads_for(bool paged) { return paged ? kThreads : kThreads + 128; }
 // Chunk ring between the feed warp and the loader: per chunk its plan unit
 // (16 B), the unit's page, and up to 128 query ids (qsplit entries).
 constexpr int kRing = 4;
@@ -122,7 +129,7 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
 // tensor-memory load, 168 registers) instead of reading it in halves (133) --
 // the shorter chain suits decode, where one warp's rows gate each K/V stage.
 template <int KV_FORMAT, int NKV, int NQ, bool PAGED>
-__global__ void __launch_bounds__(tck::kThreads, 1)
+__global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
     using namespace tck;
@@ -508,8 +515,67 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             tc::mbar_wait(bar(L::DRAIN), 0, &dummy, p.status, MSA_STATUS_TIMEOUT);
         }
         __syncwarp();
+    } else if (!PAGED && warp >= kWarpEpi0) {
+        // ------------------------------------------------------------------ epilogue (prefill)
+        // Chunk ci's O (TMEM lanes of this warp, buffer ci % 2) -> bf16 split
+        // partial, once PV has run; frees the O buffer for the chunk two later.
+        // The softmax warps store the statistics, so they never wait for PV.
+        const int R = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int j_of_row = R % p.qpk, qi = R / p.qpk;
+        int ci = 0;
+        bool ok = true;
+        Unit xnext{};
+        if (u_begin < u_end) xnext = load_unit(p, u_begin);
+        for (int u = u_begin; u < u_end && ok; u += u_step) {
+            const Unit x = xnext;
+            if (u + u_step < u_end) xnext = load_unit(p, u + u_step);
+            for (int c = 0; c < x.nch && ok; ++c, ++ci) {
+                const int b = ci & 1;
+                const uint32_t par = (ci >> 1) & 1;
+                const uint32_t o_addr = tmem + lane_base + 256 + b * 128;
+                const int idx = c * qc + qi;
+                const bool valid = idx < x.count;
+                const int packed = valid ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
+                ok = tc::mbar_wait(bar(L::O_FULL + b), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__all_sync(0xffffffffu, !valid)) {  // padding rows only: nothing to store
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::O_EMPTY + b));
+                    continue;
+                }
+                // grouped layout: for a fixed (split, c) the heads of one group are
+                // contiguous, so each store instruction writes whole runs
+                const int gq = packed & 0xFFFFFF, split = (packed >> 24) & 0xFF;
+                const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
+                uint32_t r[64];
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    tc::tmem_ld64(o_addr + 64 * hf, r);
+                    tc::tmem_ld_wait();
+                    if (hf == 1) {
+                        tc::fence_before_sync();
+                        tc::mbar_arrive(bar(L::O_EMPTY + b));  // O is read: the next PV may start
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            uint4 o4;
+                            o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
+                            o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
+                            o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
+                            o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
+                            __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
+                        }
+                    }
+                }
+            }
+        }
     } else {
-        // ------------------------------------------------------------------ softmax + epilogue
+        // ------------------------------------------------------------------ softmax (+ epilogue in decode)
         const int wg = (warp - kWarpSoftmax0) >> 2;  // 0: even chunks, 1: odd chunks
         const int R = 32 * (warp & 3) + lane;        // chunk row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -551,12 +617,14 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     tc::fence_after_sync();
                     tc::fence_before_sync();
                     tc::mbar_arrive(bar(L::P_FULL + wg));
-                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    tc::fence_before_sync();
-                    tc::mbar_arrive(bar(L::O_EMPTY + wg));
+                    if constexpr (PAGED) {
+                        ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        tc::fence_before_sync();
+                        tc::mbar_arrive(bar(L::O_EMPTY + wg));
+                    }
                     continue;
                 }
                 if constexpr (PAGED) {
@@ -713,36 +781,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     tc::tmem_st_wait();
                     tc::fence_before_sync();
                     tc::mbar_arrive(bar(L::P_FULL + wg));
-                    // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
-                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    // grouped layout: for a fixed (split, c) the heads of one group are
-                    // contiguous, so each store instruction writes whole runs
-                    const int64_t grp = (int64_t)gq * p.Hkv + x.h;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tc::tmem_ld64(o_addr + 64 * hf, r);
-                        tc::tmem_ld_wait();
-                        if (hf == 1) {
-                            tc::fence_before_sync();
-                            tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: the next PV may start
-                        }
-                        if (valid) {
-#pragma unroll
-                            for (int v4 = 0; v4 < 8; ++v4) {
-                                uint4 o4;
-                                o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
-                                o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
-                                o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
-                                o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                                __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
-                            }
-                        }
-                    }
+                    // the split statistics (m * scale, l); the epilogue warpgroup
+                    // stores the unnormalised O once PV has run
                     if (valid) {
+                        const int64_t grp = (int64_t)gq * p.Hkv + x.h;
                         const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
                         __stcs(p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row), st);
                     }
