@@ -464,7 +464,7 @@ def decode_sweep(args, dev, peaks, peak_src):
 # ---------------------------------------------------------------------------
 
 def run_reference(args, world, rank):
-    spec = synth.CAUSAL_SINK_32K
+    spec = WORKLOADS[args.workload]  # the same workload as the library's arm
     x_cpu = synth.make_prefill_inputs(spec, device="cuda" if torch.cuda.is_available() else "cpu")
     x_cpu = {k_: v_.cpu() for k_, v_ in x_cpu.items()}
     per_step = max(0.2, args.ref_budget / max(1, args.steps + args.warmup))
@@ -483,7 +483,8 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
-                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "causal": True, "pattern": "sink"},
+                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": spec.causal,
+                   "pattern": spec.pattern},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
                          "sample": f"per step: {last['sample']}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
