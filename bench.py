@@ -99,6 +99,22 @@ def decode_bytes(spec: synth.DecodeSpec, q2k: torch.Tensor, seqused: torch.Tenso
     return float(kv_bytes + q_o + B * Sq * spec.Hq * 4 + q2k.numel() * 4 + entries * 4)
 
 
+def decode_gathered_bytes(spec: synth.DecodeSpec, q2k: torch.Tensor, seqused: torch.Tensor) -> float:
+    """K+V bytes a per-query gather would read (no dedup across the queries of a
+    (b, h)): each query's distinct valid blocks, tokens < seqused."""
+    B, Hkv, Sq, topk = q2k.shape
+    ids = q2k.to(torch.int64).cpu()
+    su = seqused.to(torch.int64).cpu()
+    tokens = 0
+    for b in range(B):
+        nvalid = (int(su[b]) + 127) // 128
+        for h in range(Hkv):
+            for s in range(Sq):
+                for j in {int(j) for j in ids[b, h, s].tolist() if 0 <= j < nvalid}:
+                    tokens += min(128, int(su[b]) - 128 * j)
+    return float(tokens * spec.D * 2 * 2)
+
+
 # ---------------------------------------------------------------------------
 # environment helpers
 # ---------------------------------------------------------------------------
@@ -415,6 +431,7 @@ def decode_sweep(args, dev, peaks, peak_src):
         spec = synth.paged_decode_spec(L)
         first = synth.make_decode_inputs(spec, device=dev)
         nbytes = decode_bytes(spec, first["q2k"], first["seqused"])
+        gathered = decode_gathered_bytes(spec, first["q2k"], first["seqused"])
         nsets = max(1, math.ceil(600e6 / nbytes))
         sets = [first] + [synth.make_decode_inputs(
             synth.DecodeSpec(**{**spec.__dict__, "seed": spec.seed + 1000 + i}), device=dev) for i in range(1, nsets)]
@@ -451,7 +468,7 @@ def decode_sweep(args, dev, peaks, peak_src):
         us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
         gbs = nbytes / (us * 1e-6) / 1e9
         out.append({"L": L, "us": round(us, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                    "bytes": nbytes, "input_sets": nsets})
+                    "bytes": nbytes, "gathered_kv_bytes_no_dedup": gathered, "input_sets": nsets})
         del sets, outs, first, graph
         torch.cuda.empty_cache()
     return {"unit": "GB/s", "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,

@@ -63,3 +63,19 @@ def test_visible_key_count_matches_the_workload_figures():
     q = torch.tensor([[[[0, 0, 9, -1]]]], dtype=torch.int32)
     kv = torch.tensor([1024])
     assert int(bench.visible_keys(q, 1, kv, False).sum()) == 128
+
+
+def test_decode_unique_and_gathered_bytes_on_a_hand_case():
+    import torch
+    import bench
+    import msa_synth as synth
+    # one sequence of 200 used keys (block 0: 128 tokens, block 1: 72), one KV
+    # head, two queries selecting {0, 1} and {1} (with padding and a repeat)
+    spec = synth.DecodeSpec("hand", B=1, Sq=2, Hkv=1, qpk=1, topk=3, kv_len=217, trim=17)
+    q2k = torch.tensor([[[[0, 1, -1], [1, 1, -1]]]], dtype=torch.int32)
+    su = torch.tensor([200], dtype=torch.int32)
+    row = spec.D * 2 * 2  # K and V bytes of one token of one head
+    assert bench.decode_gathered_bytes(spec, q2k, su) == (128 + 72 + 72) * row
+    unique_kv = (128 + 72) * row
+    other = 2 * 2 * spec.Hq * spec.D * 2 + 2 * spec.Hq * 4 + q2k.numel() * 4 + 2 * 4
+    assert bench.decode_bytes(spec, q2k, su) == unique_kv + other
