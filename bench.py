@@ -5,9 +5,11 @@ One step = one pass of the prefill hot path over the 32K causal 'sink'
 workload (B=1, Sq=Skv=32768, Hkv=4, qhead_per_kv=16, topk=16, D=128): k->q CSR
 build + work plan, attention tiles, LSE combine, inputs resident in HBM.
 The metric is effective TFLOP/s = 4 * D * sum over (query, head) of visible
-keys / step time.  The paged-decode sweep (B=32, Sq=8, Hkv=4, qpk=16, topk=16,
-L = 1K..128K, seqused = L-17) is reported alongside in GB/s of algorithmic
-bytes.
+keys / step time.  Reported alongside, each with its own roofline fraction:
+the other prefill workloads (tiny non-causal 1K, 48K uniform with one KV
+head, 384K sink with qhead_per_kv 2 in bf16 and with NVFP4 K/V) and the
+paged-decode sweep (B=32, Sq=8, Hkv=4, qpk=16, topk=16, L = 1K..128K,
+seqused = L-17) in GB/s of algorithmic bytes.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
@@ -37,7 +39,9 @@ import msa_synth as synth  # noqa: E402
 
 METRIC = "sparse-attn fwd effective TFLOP/s & % bf16 peak; paged decode GB/s & % HBM"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_CSR = 8      # hist, column scan, row scan, scatter, tail fill, plan count, plan scan, plan write
+# hist, column scan, row scan, scatter, tail fill, plan count, plan scan, plan
+# write (plus one cudaMemset2DAsync of the row_ptr heads, not counted)
+KERNELS_PER_CSR = 8
 KERNELS_PER_PARTIAL = 1  # attention tiles
 KERNELS_PER_COMBINE = 1  # LSE combine
 KERNELS_PER_PAGED = 5    # union, scan, plan write, attention tiles, LSE combine
@@ -183,6 +187,37 @@ def source_hash(*names) -> str:
     return h.hexdigest()[:16]
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def workload_config(spec: synth.PrefillSpec) -> dict:
+    """The JSON `config` of a prefill workload (both arms print the same one)."""
+    q_mib = spec.B * spec.Sq * spec.Hq * spec.D * 2 / 2 ** 20
+    part_gb = spec.B * spec.Sq * spec.topk * spec.Hq * (spec.D * 2 + 8) / 1e9
+    return {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
+            "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": spec.causal,
+            "pattern": spec.pattern, "per_rank_problem": "independent (seed + rank)",
+            "l2": f"inputs larger than L2 (Q {q_mib:.0f} MiB; split partials {part_gb:.1f} GB per step); "
+                  "no flush"}
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -252,7 +287,8 @@ def oracle_rate(spec: synth.PrefillSpec, x_cpu: dict, budget_s: float, seed: int
             break
         n = min(total_q, max(n * 2, int(n * budget_s / max(dt, 1e-3) * 1.05)))
     fl = rows_flops(rows)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"{len(rows)} of {total_q} query rows (all {spec.Hq} heads), float64, {dt:.1f} s"}
 
 
@@ -277,8 +313,6 @@ def run_ours(args, world, rank):
     x = synth.make_prefill_inputs(spec_r, device=dev)
     flops = prefill_flops(spec_r, x["q2k"])
     nominal = 4.0 * spec.D * spec.Hq * spec.Sq * spec.B * spec.topk * 128
-    q_mib = spec.B * spec.Sq * spec.Hq * spec.D * 2 / 2 ** 20
-    part_gb = spec.B * spec.Sq * spec.topk * spec.Hq * (spec.D * 2 + 8) / 1e9
     csr, csr_ws = msa.csr_buffers(spec.B, spec.Hkv, spec.Sq, spec.Skv, spec.topk, spec.qpk, dev)
     fwd_ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, dev)
     out = torch.empty_like(x["q"])
@@ -389,11 +423,7 @@ def run_ours(args, world, rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
-                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": True,
-                   "pattern": spec.pattern, "per_rank_problem": "independent (seed + rank)",
-                   "l2": f"inputs larger than L2 (Q {q_mib:.0f} MiB; split partials {part_gb:.1f} GB per step); "
-                         "no flush"},
+        "config": workload_config(spec),
         "breakdown_ms": {"csr_build_and_plan": round(csr_ms, 4), "attention_tiles": round(attn_ms, 4),
                          "lse_combine": round(comb_ms, 4)},
         "effective_flop_per_step": flops, "nominal_tflops": round(nominal / (step_ms_max * 1e-3) / 1e12, 3),
@@ -409,12 +439,86 @@ def run_ours(args, world, rank):
                      "peak_source": f"{peak_src} bf16 {'sustained' if long_region else 'burst'}",
                      "kernel_source_hash": khash},
     }
+    x_cpu = {k_: v_.cpu() for k_, v_ in x.items()}
+    del x, csr, csr_ws, fwd_ws, out, lse, host, out_h, lse_h, dev_in, dev_out
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        result["configs"] = {c.name: measure_config(c, dev, args.config_steps, args.warmup, peaks, peak_src)
+                             for c in OTHER_CONFIGS}
     if not args.no_decode:
         result["decode"] = decode_sweep(args, dev, peaks, peak_src)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        x_cpu = {k_: v_.cpu() for k_, v_ in x.items()}
         result["cpu_baseline"] = oracle_rate(spec, x_cpu, args.cpu_budget)
     return result
+
+
+OTHER_CONFIGS = [synth.TINY_NONCAUSAL_1K, synth.CAUSAL_UNIFORM_48K, synth.CAUSAL_SINK_384K,
+                 synth.CAUSAL_SINK_384K_NVFP4]
+
+
+def measure_config(spec, dev, steps, warmup, peaks, peak_src):
+    """One prefill workload: CSR + plan, tiles and combine timed per step with
+    CUDA events; effective TFLOP/s of the step and of the tile kernel alone.
+    Workloads whose inputs and partials fit in L2 get an L2 flush (a 256 MiB
+    write) before every step, outside the events."""
+    import block_sparse_top_gb300 as msa
+    x = synth.make_prefill_inputs(spec, device=dev)
+    flops = prefill_flops(spec, x["q2k"])
+    k, v, kw = x["k"], x["v"], {}
+    if spec.kv_format == "nvfp4":
+        k, ks = msa.nvfp4_quantize(x["k"])
+        v, vs = msa.nvfp4_quantize(x["v"])
+        kw = {"kv_format": "nvfp4", "k_scales": ks, "v_scales": vs}
+    csr, csr_ws = msa.csr_buffers(spec.B, spec.Hkv, spec.Sq, spec.Skv, spec.topk, spec.qpk, dev)
+    fwd_ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, dev)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((spec.B, spec.Sq, spec.Hq), dtype=torch.float32, device=dev)
+    small = x["q"].numel() * 2 + fwd_ws.numel() < 256 * 2 ** 20
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev) if small else None
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if flush is not None:
+            flush.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
+        msa.build_k2q_csr(x["q2k"], spec.Skv, spec.qpk, out=csr, workspace=csr_ws)
+        if ev is not None:
+            ev[1].record(stream)
+        msa.sparse_attn_fwd_partial(x["q"], k, v, csr, causal=spec.causal, workspace=fwd_ws, **kw)
+        if ev is not None:
+            ev[2].record(stream)
+        msa.sparse_attn_combine(csr, spec.Hq, out, lse, fwd_ws)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    csr_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    step_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+    peak = peaks["bf16_tflops"]
+    tiles = flops / (attn_ms * 1e-3) / 1e12
+    res = {"config": {**workload_config(spec), "kv_format": spec.kv_format,
+                      "l2": "L2 flushed (256 MiB write) before every step, outside the events" if small
+                      else workload_config(spec)["l2"]},
+           "effective_flop_per_step": flops, "steps": steps, "ms_per_step": round(step_ms, 4),
+           "TFLOP/s": round(flops / (step_ms * 1e-3) / 1e12, 3),
+           "breakdown_ms": {"csr_build_and_plan": round(csr_ms, 4), "attention_tiles": round(attn_ms, 4),
+                            "lse_combine": round(comb_ms, 4)},
+           "roofline": {"bound": "tensor", "kernel": "attention tiles", "achieved": round(tiles, 2), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(tiles / peak, 4),
+                        "peak_source": f"{peak_src} bf16 burst"},
+           "step_frac_of_peak": round(flops / (step_ms * 1e-3) / 1e12 / peak, 4)}
+    del x, k, v, csr, csr_ws, fwd_ws, out, lse, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def decode_sweep(args, dev, peaks, peak_src):
@@ -499,11 +603,9 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
-                   "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": spec.causal,
-                   "pattern": spec.pattern},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
-                         "sample": f"per step: {last['sample']}"},
+        "config": workload_config(spec),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "cpu_model": last["cpu_model"],
+                         "kind": "oracle", "sample": f"per step: {last['sample']}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -515,8 +617,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal_sink_32k", choices=sorted(WORKLOADS))
-    ap.add_argument("--decode-L", type=int, nargs="*", default=[1024, 8192, 32768, 131072])
+    ap.add_argument("--decode-L", type=int, nargs="*", default=list(synth.DECODE_SWEEP_L))
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--config-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=150.0, help="seconds for the whole reference arm")

@@ -211,6 +211,12 @@ def new_status(device) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device)
 
 
+def check_status(word: int) -> int:
+    """msa_check_status on a status word already read back to the host: 0 (MSA_OK) or -5 (MSA_ERR_DEVICE)."""
+    w = ctypes.c_uint32(int(word) & 0xFFFFFFFF)
+    return int(lib().msa_check_status(ctypes.cast(ctypes.pointer(w), ctypes.c_void_p)))
+
+
 def read_status(status: torch.Tensor, stream=None) -> int:
     """msa_read_status: synchronises the stream and returns the status bits."""
     host = ctypes.c_uint32(0)

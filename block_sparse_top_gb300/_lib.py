@@ -59,6 +59,8 @@ def lib():
     L.msa_status_string.argtypes = [I]
     L.msa_status_string.restype = ctypes.c_char_p
     L.msa_version.restype = I
+    L.msa_check_status.argtypes = [P]
+    L.msa_check_status.restype = I
     L.msa_read_status.argtypes = [P, P, P]
     L.msa_read_status.restype = I
     L.msa_k2q_csr_workspace_size.argtypes = [I, I, I, I, I, I]

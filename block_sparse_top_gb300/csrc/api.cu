@@ -13,7 +13,12 @@ extern "C" const char *msa_status_string(int status) {
     }
 }
 
-extern "C" int msa_version(void) { return 100; }
+extern "C" int msa_version(void) { return 101; }
+
+extern "C" int msa_check_status(const uint32_t *status_word) {
+    if (!status_word) return MSA_ERR_INVALID_ARG;
+    return (*status_word & MSA_STATUS_FATAL_MASK) ? MSA_ERR_DEVICE : MSA_OK;
+}
 
 extern "C" int msa_read_status(const uint32_t *status_dev, uint32_t *status_host, cudaStream_t stream) {
     if (!status_dev || !status_host) return MSA_ERR_INVALID_ARG;

@@ -610,7 +610,7 @@ int union_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int n
         return MSA_ERR_INVALID_ARG;
     const int qpk = Hq / Hkv;
     if (D != kD || page_size != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
-    if (max_pages > kMaxPagesDecode) return MSA_ERR_UNSUPPORTED;
+    if (max_pages > kMaxPagesDecode || (int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
     if ((int64_t)num_pages * kBlk >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
         return MSA_ERR_INVALID_ARG;
@@ -711,7 +711,18 @@ extern "C" int msa_sparse_attn_paged_fwd_noalloc(const void *q, const void *k_po
                                                  int Hq, int Hkv, int D, int page_size, int topk, int causal,
                                                  float softmax_scale, void *o, float *lse, uint32_t *status_dev,
                                                  cudaStream_t stream) {
-    size_t need = msa::union_paged_fwd_scratch(B, Sq, Hq, Hkv, D, topk, max_pages);
+    // the argument and support checks of the allocating entry point come
+    // first, so that a bad argument is reported as such whatever its size
+    if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !q2k || !o) return MSA_ERR_INVALID_ARG;
+    if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages <= 0 || topk <= 0 || Hq % Hkv)
+        return MSA_ERR_INVALID_ARG;
+    if (D != msa::kD || page_size != msa::kBlk || !msa::supported_topk(topk) || !msa::supported_qpk(Hq / Hkv))
+        return MSA_ERR_UNSUPPORTED;
+    if (max_pages > msa::kMaxPagesDecode || (int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
+    if ((int64_t)num_pages * msa::kBlk >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
+    if (!msa::aligned(q, 16) || !msa::aligned(k_pool, 16) || !msa::aligned(v_pool, 16) || !msa::aligned(o, 16))
+        return MSA_ERR_INVALID_ARG;
+    const size_t need = msa::union_paged_fwd_scratch(B, Sq, Hq, Hkv, D, topk, max_pages);
     if (need == 0) return MSA_ERR_UNSUPPORTED;
     if (need > msa::kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // shape needs more than the static scratch
     void *scratch = msa::paged_scratch_for_current_device();

@@ -27,7 +27,9 @@
  *   - workspaces are caller-allocated, 256-byte aligned, sized by the
  *     matching *_workspace_size() query;
  *   - `status_dev` (may be NULL) is a device uint32 the kernels OR MSA_STATUS_*
- *     bits into; the caller zeroes it and reads it with msa_read_status();
+ *     bits into; the caller zeroes it before the call and, once the stream is
+ *     synchronised, checks the word with msa_check_status() (or reads and
+ *     checks it in one call with msa_read_status());
  *   - layouts are dense row-major C arrays in the shapes given;
  *   - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
  */
@@ -49,7 +51,7 @@ extern "C" {
                                     topk not in {4,8,16,32}, page_size != blk_kv != 128 */
 #define MSA_ERR_WORKSPACE (-3)   /* workspace or plan buffer too small or misaligned */
 #define MSA_ERR_CUDA (-4)        /* a kernel launch or CUDA runtime call failed */
-#define MSA_ERR_DEVICE (-5)      /* msa_read_status found a fatal device status bit */
+#define MSA_ERR_DEVICE (-5)      /* msa_check_status found a fatal device status bit */
 
 /* ---- device status bits (ORed into *status_dev by the kernels) ---- */
 #define MSA_STATUS_INDEX_RANGE 0x1u  /* a q2k id >= the sequence's block count: treated as padding */
@@ -71,9 +73,20 @@ const char *msa_status_string(int status);
 int msa_version(void);
 
 /*
- * Copies *status_dev to *status_host after synchronising `stream`.  Returns
- * MSA_ERR_DEVICE if a bit of MSA_STATUS_FATAL_MASK is set, else MSA_OK.
- * This is a diagnostic call, not part of the hot path.
+ * Checks a status word that the caller has already brought back: a host copy
+ * of *status_dev taken after the stream was synchronised, or the word itself
+ * when status_dev lives in host-mapped or managed memory.  Makes no CUDA
+ * call and does not synchronise.  Returns MSA_ERR_DEVICE if a bit of
+ * MSA_STATUS_FATAL_MASK is set, MSA_ERR_INVALID_ARG for NULL, else MSA_OK
+ * (the non-fatal bits MSA_STATUS_INDEX_RANGE / MSA_STATUS_DUPLICATE only
+ * report that padding rules were applied).
+ */
+int msa_check_status(const uint32_t *status_word);
+
+/*
+ * Convenience form: copies *status_dev to *status_host on `stream`,
+ * synchronises the stream, then returns msa_check_status(status_host).
+ * A diagnostic call, not part of the hot path.
  */
 int msa_read_status(const uint32_t *status_dev, uint32_t *status_host, cudaStream_t stream);
 
@@ -207,10 +220,14 @@ int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_p
  *   - The first call on a device looks up the array's address on that
  *     device (make it before any stream capture); later calls allocate
  *     nothing and call no allocating routine.
- *   - Returns MSA_ERR_WORKSPACE when the shape's union scratch needs more
- *     than 32 MiB (8 bytes per (sequence, KV head, group of 128/qhead_per_kv
- *     queries, selectable block), plus 128 KB per SM); other arguments and
- *     errors are those of msa_sparse_attn_paged_fwd.
+ *   - Argument and support checks are those of msa_sparse_attn_paged_fwd
+ *     and come first.  Then MSA_ERR_WORKSPACE is returned when the shape's
+ *     union scratch needs more than 32 MiB.  With n = min(Sq,
+ *     128/qhead_per_kv) queries per group, G = B * Hkv * ceil(Sq / n) groups
+ *     and U = min(n * topk, max_pages) union slots per group, the scratch is
+ *     G * U * (4 + 4 * ceil(n / 32)) bytes (block ids and query masks), plus
+ *     8 bytes per group, plus 129 KB per SM (cut-group partials), each part
+ *     rounded up to 256 bytes.
  *   - All calls share the one array: it keeps the last call's contents, the
  *     split counters are cleared on `stream` at the start of each call, and
  *     calls that overlap on the GPU (other streams, other host threads) race.

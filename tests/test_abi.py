@@ -37,9 +37,22 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.msa_version() == 100
+    assert L.msa_version() == 101
     for code in (0, -1, -2, -3, -4, -5):
         assert L.msa_status_string(code).startswith(b"MSA_")
+
+
+def test_check_status_reads_a_host_word_without_cuda(L):
+    """msa_check_status classifies a status word the caller already holds on the host."""
+    from block_sparse_top_gb300 import _lib
+    cases = {0: 0, _lib.MSA_STATUS_INDEX_RANGE: 0, _lib.MSA_STATUS_DUPLICATE: 0,
+             _lib.MSA_STATUS_INDEX_RANGE | _lib.MSA_STATUS_DUPLICATE: 0,
+             _lib.MSA_STATUS_PAGE_RANGE: -5, _lib.MSA_STATUS_PLAN_OVERFLOW: -5, _lib.MSA_STATUS_TIMEOUT: -5,
+             _lib.MSA_STATUS_LAUNCH: -5, _lib.MSA_STATUS_DUPLICATE | _lib.MSA_STATUS_TIMEOUT: -5}
+    for word, want in cases.items():
+        w = ctypes.c_uint32(word)
+        assert L.msa_check_status(ctypes.cast(ctypes.pointer(w), ctypes.c_void_p)) == want, hex(word)
+    assert L.msa_check_status(None) == -1
 
 
 def test_size_queries(L):

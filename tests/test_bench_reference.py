@@ -34,6 +34,11 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == "causal_sink_16k_1kv"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    # the same config dict as the library's arm prints for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == bench.workload_config(bench.WORKLOADS["causal_sink_16k_1kv"])
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -195,7 +195,9 @@ def test_nvfp4_full_size_sampled():
     rows = synth.sample_query_rows(total, 32, must=[0, 128, total - 1])
     kq, kqs = oracle.nvfp4_quantize(x["k"].cpu())
     vq, vqs = oracle.nvfp4_quantize(x["v"].cpu())
-    assert np.array_equal(kp.cpu().numpy(), kq) and np.array_equal(vs.cpu().numpy(), vqs)
+    # the whole quantiser output, codes and scales of both K and V, is bit-exact
+    assert np.array_equal(kp.cpu().numpy(), kq) and np.array_equal(ks.cpu().numpy(), kqs)
+    assert np.array_equal(vp.cpu().numpy(), vq) and np.array_equal(vs.cpu().numpy(), vqs)
     kd = torch.from_numpy(oracle.nvfp4_dequantize(kq, kqs).view(np.int16)).view(torch.bfloat16)
     vd = torch.from_numpy(oracle.nvfp4_dequantize(vq, vqs).view(np.int16)).view(torch.bfloat16)
     o_ref, l_ref = oracle.sparse_attn(x["q"].cpu(), kd, vd, x["q2k"].cpu(), causal=True, rows=rows)

@@ -35,7 +35,7 @@ def test_decode_sweep_small_full_parity(L):
     assert st == 0
 
 
-@pytest.mark.parametrize("L", [32768, 131072])
+@pytest.mark.parametrize("L", [16384, 32768, 65536, 131072])
 def test_decode_sweep_large_sampled(L):
     spec = synth.paged_decode_spec(L)
     rows = synth.sample_query_rows(spec.B * spec.Sq, 24, must=[0, 7, 255])
