@@ -37,6 +37,7 @@ then the rest ascending) and pads with -1.  Rows with ``V == 0`` are all -1.
 
 from __future__ import annotations
 
+import itertools
 import math
 from dataclasses import dataclass, field
 from typing import Optional
@@ -399,6 +400,62 @@ def make_decode_inputs(spec: DecodeSpec, device="cpu") -> dict:
     seqused = torch.full((spec.B,), spec.seqused, dtype=torch.int32, device=device)
     q2k = q2k_decode(spec.B, spec.Hkv, spec.Sq, seqused, spec.topk, spec.page, spec.seed, device)
     return {"q": q, "k_pool": k, "v_pool": v, "page_table": pt, "seqused": seqused, "q2k": q2k}
+
+
+@dataclass
+class VarlenSpec:
+    """Ragged prefill batch: sequence b has q_lens[b] queries and k_lens[b] keys.
+
+    Q [total_q,Hq,D], K/V [total_k,Hkv,D], q2k [Hkv,total_q,topk] with block ids
+    local to each sequence; cu_seqlens_q / cu_seqlens_k are the prefix sums.
+    """
+    name: str
+    q_lens: tuple
+    k_lens: tuple
+    Hkv: int
+    qpk: int
+    topk: int
+    causal: bool
+    pattern: str            # "perm_prefix" | "sink" | "uniform"
+    D: int = 128
+    blk: int = BLK
+    seed: int = DEFAULT_SEED
+
+    @property
+    def B(self) -> int:
+        return len(self.q_lens)
+
+    @property
+    def Hq(self) -> int:
+        return self.Hkv * self.qpk
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.q_lens))
+
+    @property
+    def total_k(self) -> int:
+        return int(sum(self.k_lens))
+
+
+def make_varlen_inputs(spec: VarlenSpec, device="cpu") -> dict:
+    """Q, K, V (bf16), q2k [Hkv,total_q,topk] and cu_seqlens_q/k (int32).
+
+    Each sequence's selections follow the pattern of a batch-1 prefill of its
+    own lengths (seed + 7919 * b, so sequences differ)."""
+    q = normal_bf16((spec.total_q, spec.Hq, spec.D), spec.seed, STREAM_Q, device)
+    k = normal_bf16((spec.total_k, spec.Hkv, spec.D), spec.seed, STREAM_K, device)
+    v = normal_bf16((spec.total_k, spec.Hkv, spec.D), spec.seed, STREAM_V, device)
+    parts = []
+    for b, (sq, sk) in enumerate(zip(spec.q_lens, spec.k_lens)):
+        ps = PrefillSpec(f"{spec.name}_{b}", B=1, Sq=int(sq), Skv=int(sk), Hkv=spec.Hkv, qpk=spec.qpk,
+                         topk=spec.topk, causal=spec.causal, pattern=spec.pattern, D=spec.D, blk=spec.blk,
+                         seed=spec.seed + 7919 * b)
+        parts.append(make_prefill_q2k(ps, device)[0])          # [Hkv, sq, topk]
+    q2k = torch.cat(parts, dim=1).contiguous()
+    cu = lambda lens: torch.tensor([0] + list(itertools.accumulate(int(x) for x in lens)), dtype=torch.int32,
+                                   device=device)
+    return {"q": q, "k": k, "v": v, "q2k": q2k, "cu_seqlens_q": cu(spec.q_lens), "cu_seqlens_k": cu(spec.k_lens)}
 
 
 def sample_query_rows(total_q: int, n: int, seed: int = DEFAULT_SEED, must=()) -> list:

@@ -36,6 +36,11 @@ def lib():
         L.oracle_sparse_attn_paged.restype = I
         L.oracle_build_k2q_csr.argtypes = [P, I, I, I, I, I, I, P, P, P, P, P]
         L.oracle_build_k2q_csr.restype = I
+        L.oracle_sparse_attn_varlen.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, I, D, D, P, I64, P,
+                                                P, P, I]
+        L.oracle_sparse_attn_varlen.restype = I
+        L.oracle_build_k2q_csr_varlen.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P]
+        L.oracle_build_k2q_csr_varlen.restype = I
         L.oracle_nvfp4_quantize.argtypes = [P, I64, I, P, P]
         L.oracle_nvfp4_dequantize.argtypes = [P, P, I64, I, P]
         L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
@@ -127,6 +132,66 @@ def sparse_attn_paged(q, k_pool, v_pool, page_table, seqused, q2k, *, causal: bo
                                         B, Sq, Hq, Hkv, D, page, topk, int(bool(causal)), float(scale),
                                         _ptr(r), n, _ptr(o), _ptr(lse), int(nthreads))
     return (o, lse, th) if return_threads else (o, lse)
+
+
+def sparse_attn_varlen(q, k, v, q2k, cu_seqlens_q, cu_seqlens_k=None, *, causal: bool,
+                       scale: Optional[float] = None, temperature: Optional[float] = None, blk: int = 128,
+                       page_table=None, seqused=None, rows: Optional[Sequence[int]] = None, nthreads: int = 0):
+    """Varlen / paged / every-block oracle (oracle.c ``oracle_sparse_attn_varlen``).
+
+    q [total_q,Hq,D]; dense k/v [total_k,Hkv,D] with cu_seqlens_k, or pools
+    [num_pages,blk,Hkv,D] with page_table [B,max_pages]; q2k [Hkv,total_q,topk]
+    (sequence-local ids) or None for every block.  Returns (O [n,Hq,D],
+    LSE [n,Hq]) and, when ``temperature`` is given, the temperature LSE [n,Hq].
+    """
+    total_q, Hq, D = q.shape
+    Hkv = k.shape[-2]
+    cq = _i32(cu_seqlens_q)
+    B = cq.size - 1
+    ck = None if cu_seqlens_k is None else _i32(cu_seqlens_k)
+    pt = None if page_table is None else _i32(page_table)
+    max_pages = 0 if pt is None else pt.shape[1]
+    if pt is None and ck is None:
+        raise ValueError("dense K/V needs cu_seqlens_k")
+    topk = 0 if q2k is None else q2k.shape[-1]
+    sel = None if q2k is None else _i32(q2k)
+    su = None if seqused is None else _i32(seqused)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = total_q if r is None else r.size
+    o = np.zeros((n, Hq, D), dtype=np.float64)
+    lse = np.zeros((n, Hq), dtype=np.float64)
+    lt = np.zeros((n, Hq), dtype=np.float64) if temperature is not None else None
+    lib().oracle_sparse_attn_varlen(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sel), _ptr(cq), _ptr(ck), _ptr(pt),
+                                    max_pages, _ptr(su), B, Hq, Hkv, D, blk, topk, int(bool(causal)), float(scale),
+                                    float(temperature) if temperature is not None else 0.0, _ptr(r), n, _ptr(o),
+                                    _ptr(lse), _ptr(lt), int(nthreads))
+    return (o, lse) if lt is None else (o, lse, lt)
+
+
+def build_k2q_csr_varlen(q2k, cu_seqlens_q, cu_seqlens_k, blk: int = 128, seqused=None):
+    """Varlen k->q CSR oracle (oracle.c ``oracle_build_k2q_csr_varlen``).
+
+    q2k [Hkv,total_q,topk] (sequence-local ids).  Returns dict(row_ptr
+    [Hkv,total_rows+1], q_indices, qsplit [Hkv,total_q*topk], split_counts
+    [total_q,Hkv]); total_rows = sum of ceil(kv_len_b / blk).
+    """
+    Hkv, total_q, topk = q2k.shape
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    B = cq.size - 1
+    rows = int(sum((int(ck[b + 1]) - int(ck[b]) + blk - 1) // blk for b in range(B)))
+    cap = total_q * topk
+    sel = _i32(q2k)
+    su = None if seqused is None else _i32(seqused)
+    row_ptr = np.zeros((Hkv, rows + 1), dtype=np.int32)
+    qi = np.zeros((Hkv, cap), dtype=np.int32)
+    qs = np.zeros((Hkv, cap), dtype=np.int32)
+    sc = np.zeros((total_q, Hkv), dtype=np.int32)
+    lib().oracle_build_k2q_csr_varlen(_ptr(sel), _ptr(cq), _ptr(ck), B, Hkv, topk, blk, _ptr(su), _ptr(row_ptr),
+                                      _ptr(qi), _ptr(qs), _ptr(sc))
+    return {"row_ptr": row_ptr, "q_indices": qi, "qsplit": qs, "split_counts": sc}
 
 
 def build_k2q_csr(q2k, Skv: int, blk: int = 128, seqused=None):

@@ -19,6 +19,11 @@
  *     CSR (row_ptr [Hkv][rows+1], q_indices [Hkv][total_q*topk]) and the
  *     scheduler test (test_scheduler_builds_packed_qsplit_metadata): qsplit
  *     packs q | split << 24 and a query's split ids are 0..count-1.
+ *   - varlen batches (interface.py sparse_atten_func: cu_seqlens_q/k, q2k
+ *     [Hkv][total_q][topK]; test_sparse_atten.py _reference_varlen_forward:
+ *     each sequence is its own batch-1 problem), the temperature LSE
+ *     (sparse_attention_ref, lse_temperature_scale branch) and the dense
+ *     decode selection (sparse_decode_atten_func, q2k_indices = None).
  *   - NVFP4 (interface.py sparse_atten_nvfp4_kv_func docstring; vLLM
  *     sparse-MLA test page, _E2M1_TABLE and unpack_e2m1): e2m1 codes with
  *     magnitudes {0,.5,1,1.5,2,3,4,6}, bit 3 the sign, element 2i in the low
@@ -307,6 +312,156 @@ int oracle_sparse_attn_paged(const uint16_t *q, const uint16_t *k_pool, const ui
 }
 
 /* ---------------------------------------------------------------------- */
+/* varlen batches, temperature LSE, every-block selection                  */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * Ragged batches as the interface page's sparse_atten_func takes them
+ * (cu_seqlens_q / cu_seqlens_k prefix sums, q [total_q][Hq][D], k and v
+ * [total_k][Hkv][D], q2k [Hkv][total_q][topk] with block ids local to each
+ * sequence), and as the test page's varlen reference computes them: each
+ * sequence is an independent batch-1 problem of sparse_attention_ref on its
+ * own slice, so query s of sequence b sees key t (local) iff t lies in one of
+ * its blocks, t < kv_len_b and, when causal, t <= s + (kv_len_b - Sq_b).
+ *
+ * Also, from sparse_attention_ref's lse_temperature_scale branch: a second
+ * LSE over the same visible scores divided by the temperature T,
+ * lse_T = log sum_t exp(s_t / T), s_t = scale * q . k_t (-inf for an empty row).
+ *
+ * q2k == NULL selects every block of the sequence (the interface page's
+ * dense decode mode, sparse_decode_atten_func with q2k_indices = None).
+ * page_table != NULL: k and v are pools [num_pages][blk][Hkv][D] and logical
+ * block j of sequence b is page page_table[b][j] (kv_len_b = seqused[b], or
+ * max_pages * blk); cu_k is then unused.
+ */
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int32_t *q2k, *cu_q, *cu_k, *page_table, *seqused;
+    int B, Hq, Hkv, D, blk, topk, causal, max_pages;
+    int64_t total_q;
+    double scale, temp;
+    const int64_t *rows;
+    double *o, *lse, *lse_temp;
+} varlen_ctx;
+
+/* Sequence holding global query gq: the largest b with cu_q[b] <= gq. */
+static int seq_of(const int32_t *cu_q, int B, int64_t gq) {
+    int b = 0;
+    while (b + 1 < B && cu_q[b + 1] <= gq) ++b;
+    return b;
+}
+
+static void attn_item_varlen(void *vctx, int64_t item) {
+    const varlen_ctx *c = (const varlen_ctx *)vctx;
+    int64_t ri = item / c->Hkv;
+    int h = (int)(item % c->Hkv);
+    int64_t gq = c->rows ? c->rows[ri] : ri;
+    int b = seq_of(c->cu_q, c->B, gq);
+    int64_t s = gq - c->cu_q[b];
+    int64_t sq_b = c->cu_q[b + 1] - c->cu_q[b];
+    int64_t kv_alloc = c->page_table ? (int64_t)c->max_pages * c->blk : (int64_t)(c->cu_k[b + 1] - c->cu_k[b]);
+    int64_t kv_len = c->seqused ? c->seqused[b] : kv_alloc;
+    int nblk = (int)((kv_alloc + c->blk - 1) / c->blk);
+    int qpk = c->Hq / c->Hkv, D = c->D;
+
+    /* 1. the set J of distinct valid block ids (every block when q2k is NULL) */
+    int *J = (int *)malloc(sizeof(int) * (size_t)(nblk > 0 ? nblk : 1));
+    int nJ = 0;
+    if (!c->q2k) {
+        for (int j = 0; j < nblk; ++j) J[nJ++] = j;
+    } else {
+        const int32_t *sel = c->q2k + ((int64_t)h * c->total_q + gq) * c->topk;
+        for (int t = 0; t < c->topk; ++t) {
+            int j = sel[t];
+            if (j < 0 || j >= nblk) continue;
+            int dup = 0;
+            for (int u = 0; u < nJ; ++u) dup |= (J[u] == j);
+            if (!dup) J[nJ++] = j;
+        }
+    }
+    /* 2. visible tokens */
+    int64_t limit = kv_len - 1;
+    if (c->causal && s + (kv_len - sq_b) < limit) limit = s + (kv_len - sq_b);
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)((int64_t)nJ * c->blk + 1));
+    int64_t ntok = 0;
+    for (int u = 0; u < nJ; ++u)
+        for (int i = 0; i < c->blk; ++i) {
+            int64_t t = (int64_t)J[u] * c->blk + i;
+            if (t <= limit) tok[ntok++] = t;
+        }
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(ntok > 0 ? ntok : 1));
+    for (int g = 0; g < qpk; ++g) {
+        int hq = h * qpk + g;
+        const uint16_t *qr = c->q + (gq * c->Hq + hq) * (int64_t)D;
+        double *orow = c->o + (ri * c->Hq + hq) * (int64_t)D;
+        double *lrow = c->lse + ri * c->Hq + hq;
+        double *trow = c->lse_temp ? c->lse_temp + ri * c->Hq + hq : NULL;
+        for (int d = 0; d < D; ++d) orow[d] = 0.0;
+        if (ntok == 0) {
+            *lrow = -INFINITY;
+            if (trow) *trow = -INFINITY;
+            continue;
+        }
+        /* 3. scores and their max */
+        double m = -INFINITY;
+        for (int64_t i = 0; i < ntok; ++i) {
+            const uint16_t *kr;
+            if (c->page_table) {
+                int64_t page = c->page_table[(int64_t)b * c->max_pages + tok[i] / c->blk];
+                kr = c->k + ((page * c->blk + tok[i] % c->blk) * c->Hkv + h) * (int64_t)D;
+            } else {
+                kr = c->k + (((int64_t)c->cu_k[b] + tok[i]) * c->Hkv + h) * (int64_t)D;
+            }
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += bf16_to_double(qr[d]) * bf16_to_double(kr[d]);
+            sc[i] = c->scale * acc;
+            if (sc[i] > m) m = sc[i];
+        }
+        /* 4. softmax, LSE, output; the temperature LSE over s_t / T */
+        double l = 0.0, lt = 0.0;
+        for (int64_t i = 0; i < ntok; ++i) {
+            const uint16_t *vr;
+            if (c->page_table) {
+                int64_t page = c->page_table[(int64_t)b * c->max_pages + tok[i] / c->blk];
+                vr = c->v + ((page * c->blk + tok[i] % c->blk) * c->Hkv + h) * (int64_t)D;
+            } else {
+                vr = c->v + (((int64_t)c->cu_k[b] + tok[i]) * c->Hkv + h) * (int64_t)D;
+            }
+            double p = exp(sc[i] - m);
+            l += p;
+            if (trow) lt += exp((sc[i] - m) / c->temp);
+            for (int d = 0; d < D; ++d) orow[d] += p * bf16_to_double(vr[d]);
+        }
+        for (int d = 0; d < D; ++d) orow[d] /= l;
+        *lrow = m + log(l);
+        if (trow) *trow = m / c->temp + log(lt);
+    }
+    free(sc);
+    free(tok);
+    free(J);
+}
+
+/*
+ * Varlen (and, with page_table, paged) sparse attention.  temp > 0 and
+ * lse_temp != NULL also give the temperature LSE.  Returns the threads used.
+ */
+int oracle_sparse_attn_varlen(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *q2k,
+                              const int32_t *cu_q, const int32_t *cu_k, const int32_t *page_table, int max_pages,
+                              const int32_t *seqused, int B, int Hq, int Hkv, int D, int blk, int topk,
+                              int causal, double scale, double temp, const int64_t *rows, int64_t nrows,
+                              double *o, double *lse, double *lse_temp, int nthreads) {
+    varlen_ctx c;
+    memset(&c, 0, sizeof c);
+    c.q = q; c.k = k; c.v = v; c.q2k = q2k; c.cu_q = cu_q; c.cu_k = cu_k; c.page_table = page_table;
+    c.seqused = seqused; c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.D = D; c.blk = blk; c.topk = topk;
+    c.causal = causal; c.max_pages = max_pages; c.total_q = cu_q[B]; c.scale = scale;
+    c.temp = temp; c.rows = rows; c.o = o; c.lse = lse;
+    c.lse_temp = (temp > 0.0) ? lse_temp : NULL;
+    int64_t n = rows ? nrows : c.total_q;
+    return parallel_for(n * Hkv, nthreads, attn_item_varlen, &c);
+}
+
+/* ---------------------------------------------------------------------- */
 /* k -> q CSR                                                              */
 /* ---------------------------------------------------------------------- */
 
@@ -374,6 +529,73 @@ int oracle_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, in
     }
     free(rank);
     free(cursor);
+    return 0;
+}
+
+/*
+ * Varlen k -> q CSR (interface page, sparse_atten_func: q2k [Hkv][total_q][topK]
+ * with sequence-local block ids is inverted into k2q_row_ptr
+ * [Hkv][total_rows + 1] and k2q_q_indices [Hkv][total_q * topK]).  Sequence b
+ * owns rows row_off[b] .. row_off[b] + nblk_b - 1, nblk_b = ceil(kv_b / blk),
+ * kv_b = cu_k[b+1] - cu_k[b]; row_off is the prefix of the nblk_b.  Valid ids:
+ * 0 <= j < ceil(kv_len_b / blk), kv_len_b = seqused[b] or kv_b.  Within a
+ * row the global query ids are ascending; qsplit, split_counts and the -1
+ * tails as in oracle_build_k2q_csr.  total_rows = row_off[B].
+ */
+int oracle_build_k2q_csr_varlen(const int32_t *q2k, const int32_t *cu_q, const int32_t *cu_k, int B, int Hkv,
+                                int topk, int blk, const int32_t *seqused, int32_t *row_ptr, int32_t *q_indices,
+                                int32_t *qsplit, int32_t *split_counts) {
+    int64_t total_q = cu_q[B];
+    int64_t *row_off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(B + 1));
+    row_off[0] = 0;
+    for (int b = 0; b < B; ++b) row_off[b + 1] = row_off[b] + (cu_k[b + 1] - cu_k[b] + blk - 1) / blk;
+    int64_t rows = row_off[B];
+    int64_t cap = total_q * topk;
+    int32_t *rank = (int32_t *)malloc(sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1));
+    int64_t *cursor = (int64_t *)malloc(sizeof(int64_t) * (size_t)(rows + 1));
+    for (int h = 0; h < Hkv; ++h) {
+        int32_t *rp = row_ptr + (int64_t)h * (rows + 1);
+        int32_t *qi = q_indices + (int64_t)h * cap;
+        int32_t *qs = qsplit + (int64_t)h * cap;
+        for (int64_t r = 0; r <= rows; ++r) rp[r] = 0;
+        for (int b = 0; b < B; ++b) {
+            int64_t nblk_b = row_off[b + 1] - row_off[b];
+            int64_t kv_len = seqused ? seqused[b] : (cu_k[b + 1] - cu_k[b]);
+            int64_t nvalid = (kv_len + blk - 1) / blk;
+            if (nvalid > nblk_b) nvalid = nblk_b;
+            for (int64_t gq = cu_q[b]; gq < cu_q[b + 1]; ++gq) {
+                const int32_t *sel = q2k + ((int64_t)h * total_q + gq) * topk;
+                int32_t *rk = rank + gq * topk;
+                int cnt = 0;
+                for (int t = 0; t < topk; ++t) {
+                    int j = sel[t];
+                    int ok = (j >= 0 && j < nvalid);
+                    for (int u = 0; ok && u < t; ++u)
+                        if (sel[u] == j) ok = 0;
+                    rk[t] = ok ? cnt++ : -1;
+                    if (ok) rp[row_off[b] + j + 1] += 1;
+                }
+                split_counts[gq * Hkv + h] = cnt;
+            }
+        }
+        for (int64_t r = 0; r < rows; ++r) rp[r + 1] += rp[r];
+        for (int64_t r = 0; r < rows; ++r) cursor[r] = rp[r];
+        for (int64_t i = 0; i < cap; ++i) { qi[i] = -1; qs[i] = -1; }
+        for (int b = 0; b < B; ++b)
+            for (int64_t gq = cu_q[b]; gq < cu_q[b + 1]; ++gq) {
+                const int32_t *sel = q2k + ((int64_t)h * total_q + gq) * topk;
+                const int32_t *rk = rank + gq * topk;
+                for (int t = 0; t < topk; ++t) {
+                    if (rk[t] < 0) continue;
+                    int64_t pos = cursor[row_off[b] + sel[t]]++;
+                    qi[pos] = (int32_t)gq;
+                    qs[pos] = (int32_t)(gq | ((int64_t)rk[t] << 24));
+                }
+            }
+    }
+    free(rank);
+    free(cursor);
+    free(row_off);
     return 0;
 }
 
