@@ -223,18 +223,56 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t c) {
     return (c & 8) ? -v : v;
 }
 
-// Dequantises 16 NVFP4 values (8 packed bytes, one e4m3 scale) into 16 bf16
-// (two 16-byte chunks).  Each product is exact in bf16.
-__device__ __forceinline__ void nvfp4_group_to_bf16(uint2 packed, uint32_t scale_byte, uint4 &lo, uint4 &hi) {
-    float s = e4m3_to_float(scale_byte);
-    uint32_t w[8];
+// e4m3 byte -> its value as bf16 in both halves of a word.  The seven
+// magnitude bits placed at bit 20 of an f32 (exponent field low four bits,
+// mantissa top three) read as 2^-120 times the e4m3 value, subnormal codes
+// included, so one exact multiply by 2^120 gives the value; it has at most
+// four significant bits, so the bf16 truncation is exact too.
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t b) {
+    const float f = __uint_as_float(((b & 0x7Fu) << 20) | ((b & 0x80u) << 24)) * 0x1p120f;
+    const uint32_t h = __float_as_uint(f) >> 16;
+    return h | (h << 16);
+}
+
+// Eight e2m1 codes (code i in nibble i of x) -> eight bf16, element 2i in the
+// low half of w[i].  The bf16 bytes of the eight magnitudes {0, .5, 1, 1.5, 2,
+// 3, 4, 6} are two byte tables (low bytes 00 00 80 c0 00 40 80 c0, high bytes
+// 00 3f 3f 3f 40 40 40 40) that one byte permute each looks up for four codes
+// at a time; two more permutes interleave low and high bytes, and the codes'
+// sign bits (bit 3 of each nibble) become the bf16 sign bits.  Integer ops
+// only: nothing on the special-function pipe the softmax uses.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t x, uint32_t (&w)[4]) {
+    const uint32_t mag = x & 0x77777777u, sg = x & 0x88888888u;
+    const uint32_t lo03 = __byte_perm(0xC0800000u, 0xC0804000u, mag);
+    const uint32_t hi03 = __byte_perm(0x3F3F3F00u, 0x40404040u, mag);
+    const uint32_t lo47 = __byte_perm(0xC0800000u, 0xC0804000u, mag >> 16);
+    const uint32_t hi47 = __byte_perm(0x3F3F3F00u, 0x40404040u, mag >> 16);
+    w[0] = __byte_perm(lo03, hi03, 0x5140) | ((sg << 12) & 0x8000u) | ((sg << 24) & 0x80000000u);
+    w[1] = __byte_perm(lo03, hi03, 0x7362) | ((sg << 4) & 0x8000u) | ((sg << 16) & 0x80000000u);
+    w[2] = __byte_perm(lo47, hi47, 0x5140) | ((sg >> 4) & 0x8000u) | ((sg << 8) & 0x80000000u);
+    w[3] = __byte_perm(lo47, hi47, 0x7362) | ((sg >> 12) & 0x8000u) | (sg & 0x80000000u);
+}
+
+// bf16x2 product, round to nearest (exact for e2m1 x e4m3: at most six
+// significant bits).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 32 NVFP4 values (16 packed bytes, two groups of 16) and their two e4m3
+// scales (low byte: first group) -> 32 bf16 in four 16-byte chunks.
+__device__ __forceinline__ void nvfp4_piece_to_bf16(uint4 packed, uint32_t scales2, uint4 (&out)[4]) {
+    const uint32_t s0 = e4m3_to_bf16x2(scales2 & 0xFFu), s1 = e4m3_to_bf16x2((scales2 >> 8) & 0xFFu);
+    const uint32_t words[4] = {packed.x, packed.y, packed.z, packed.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t byte = ((i < 4 ? packed.x : packed.y) >> (8 * (i & 3))) & 0xFF;
-        w[i] = pack_bf16x2(e2m1_to_float(byte & 0xF) * s, e2m1_to_float(byte >> 4) * s);
+    for (int c = 0; c < 4; ++c) {
+        uint32_t w[4];
+        e2m1x8_to_bf16(words[c], w);
+        const uint32_t s = c < 2 ? s0 : s1;
+        out[c] = make_uint4(bf16x2_mul(w[0], s), bf16x2_mul(w[1], s), bf16x2_mul(w[2], s), bf16x2_mul(w[3], s));
     }
-    lo = make_uint4(w[0], w[1], w[2], w[3]);
-    hi = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 }  // namespace msa

@@ -374,25 +374,38 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                // 128 tokens x 8 groups of 16 values, for K and for V
-#pragma unroll 4
-                for (int it = lane; it < 2 * 128 * 8; it += 32) {
-                    const int isv = it >> 10, r = (it >> 3) & 127, g = it & 7;
-                    const int t = x.tok0 + r;
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                    if (t < p.Skv) {
-                        const int64_t rr = ((int64_t)x.b * p.Skv + t) * p.Hkv + x.h;
-                        const uint8_t *pk = isv ? p.v_packed : p.k_packed;
-                        const uint8_t *sc = isv ? p.v_scales : p.k_scales;
-                        uint2 w = *reinterpret_cast<const uint2 *>(pk + rr * 64 + g * 8);
-                        nvfp4_group_to_bf16(w, sc[rr * 8 + g], lo, hi);
+                // 128 tokens x 4 pieces of 32 values (16 packed bytes, two
+                // scales), for K and then for V.  Lane l converts piece l % 4
+                // of tokens l / 4 + 8 i: lanes 4i..4i+3 read one token's 64
+                // bytes.  Eight 16-byte loads are in flight before any is used.
+                const int pc = lane & 3, r0 = lane >> 2;
+#pragma unroll 1
+                for (int k0 = 0; k0 < 32; k0 += 8) {
+                    const int isv = k0 >> 4, rb = r0 + 8 * (k0 & 15);
+                    const uint8_t *pbase = isv ? p.v_packed : p.k_packed;
+                    const uint8_t *sbase = isv ? p.v_scales : p.k_scales;
+                    const int64_t row0 = ((int64_t)x.b * p.Skv + x.tok0 + rb) * p.Hkv + x.h;
+                    uint4 pk[8];
+                    uint32_t sc2[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int64_t rr = row0 + (int64_t)(8 * i) * p.Hkv;
+                        const bool in = x.tok0 + rb + 8 * i < p.Skv;
+                        pk[i] = in ? __ldg(reinterpret_cast<const uint4 *>(pbase + rr * 64) + pc) : make_uint4(0, 0, 0, 0);
+                        sc2[i] = in ? __ldg(reinterpret_cast<const uint16_t *>(sbase + rr * 8) + pc) : 0u;
                     }
-                    const uint32_t tile = base + (isv ? L::V : L::K) + kb * 32768 + (g >> 2) * 16384;
-                    const int cch = (g & 3) * 2;
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(tile + tc::sw128_off(r, cch)),
-                                 "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w));
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(tile + tc::sw128_off(r, cch + 1)),
-                                 "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w));
+                    // values 32 pc .. 32 pc + 31: column half pc / 2, chunks 4 (pc % 2) ..
+                    const uint32_t tile = base + (isv ? L::V : L::K) + kb * 32768 + (pc >> 1) * 16384;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4 o4[4];
+                        nvfp4_piece_to_bf16(pk[i], sc2[i], o4);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                                             tile + tc::sw128_off(rb + 8 * i, (pc & 1) * 4 + c)),
+                                         "r"(o4[c].x), "r"(o4[c].y), "r"(o4[c].z), "r"(o4[c].w));
+                    }
                 }
                 tc::fence_proxy_async();
                 tc::mbar_arrive(bar(L::KV_FULL + kb));
