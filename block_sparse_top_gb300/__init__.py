@@ -14,9 +14,10 @@ from typing import Optional
 
 import torch
 
-from ._lib import (MSA_KV_BF16, MSA_KV_NVFP4, MSA_STATUS_DUPLICATE, MSA_STATUS_FATAL_MASK,  # noqa: F401
-                   MSA_STATUS_INDEX_RANGE, MSA_STATUS_LAUNCH, MSA_STATUS_PAGE_RANGE, MSA_STATUS_PLAN_OVERFLOW,
-                   MSA_STATUS_TIMEOUT, MsaError, check, lib)
+from ._lib import (MSA_KV_BF16, MSA_KV_FP8, MSA_KV_NVFP4, MSA_PARTIAL_BF16, MSA_PARTIAL_FP16, MSA_PARTIAL_FP32,  # noqa: F401
+                   MSA_STATUS_DUPLICATE, MSA_STATUS_FATAL_MASK, MSA_STATUS_INDEX_RANGE, MSA_STATUS_LAUNCH,
+                   MSA_STATUS_PAGE_RANGE, MSA_STATUS_PLAN_OVERFLOW, MSA_STATUS_SHAPE, MSA_STATUS_TIMEOUT, FwdOptions,
+                   MsaError, check, lib)
 
 BLK = 128
 
@@ -38,6 +39,27 @@ def _ws(nbytes: int, device) -> torch.Tensor:
 def _need(t: torch.Tensor, dtype, name: str):
     if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+_FP8 = getattr(torch, "float8_e4m3fn", None)
+
+
+def _kv_format(kv_format: str, k, v, k_scales, v_scales) -> int:
+    """Checks the K/V tensors of a format name and returns its MSA_KV_* code."""
+    if kv_format == "bf16":
+        _need(k, torch.bfloat16, "k")
+        _need(v, torch.bfloat16, "v")
+        return MSA_KV_BF16
+    if kv_format == "fp8":
+        for t, n in ((k, "k"), (v, "v")):
+            if not (t.is_cuda and t.is_contiguous() and t.dtype in (torch.uint8, _FP8)):
+                raise ValueError(f"{n} must be a contiguous CUDA tensor of e4m3 bytes (float8_e4m3fn or uint8)")
+        return MSA_KV_FP8
+    if kv_format == "nvfp4":
+        for t, n in ((k, "k"), (v, "v"), (k_scales, "k_scales"), (v_scales, "v_scales")):
+            _need(t, torch.uint8, n)
+        return MSA_KV_NVFP4
+    raise ValueError(f"unknown kv_format {kv_format!r}")
 
 
 @dataclass
@@ -92,6 +114,110 @@ def build_k2q_csr(q2k: torch.Tensor, Skv: int, qhead_per_kv: int, seqused: Optio
     return out
 
 
+@dataclass
+class K2qCsrVarlen:
+    """Output of msa_build_k2q_csr_varlen plus the work plan (ragged batch)."""
+    row_ptr: torch.Tensor       # [Hkv, total_rows+1] int32
+    q_indices: torch.Tensor     # [Hkv, total_q*topk] int32
+    qsplit: torch.Tensor        # [Hkv, total_q*topk] int32
+    split_counts: torch.Tensor  # [total_q, Hkv] int32
+    plan: torch.Tensor          # opaque uint8 buffer
+    cu_seqlens_q: torch.Tensor  # [B+1] int32
+    cu_seqlens_k: torch.Tensor  # [B+1] int32
+    B: int
+    Hkv: int
+    total_q: int
+    topk: int
+    qhead_per_kv: int
+
+
+def build_k2q_csr_varlen(q2k: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                         max_seqlen_q: int, max_seqlen_k: int, qhead_per_kv: int, total_rows: Optional[int] = None,
+                         seqused: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                         stream=None) -> K2qCsrVarlen:
+    """msa_build_k2q_csr_varlen: q2k [Hkv,total_q,topk] int32 + cu_seqlens -> K2qCsrVarlen.
+
+    ``total_rows`` (the row capacity) defaults to sum_b ceil(keys_b / 128), read
+    from cu_seqlens_k on the host."""
+    _need(q2k, torch.int32, "q2k")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    Hkv, total_q, topk = q2k.shape
+    B = cu_seqlens_q.numel() - 1
+    if total_rows is None:
+        lens = cu_seqlens_k.cpu().diff()
+        total_rows = int(((lens + BLK - 1) // BLK).sum())
+    total_rows = max(1, int(total_rows))
+    L = lib()
+    plan_bytes = L.msa_plan_varlen_size(Hkv, total_q, total_rows, topk, BLK, qhead_per_kv)
+    ws_bytes = L.msa_k2q_csr_varlen_workspace_size(B, Hkv, total_q, max_seqlen_q, max_seqlen_k, total_rows, topk, BLK)
+    if plan_bytes == 0 or ws_bytes == 0:
+        raise ValueError("unsupported varlen CSR shape")
+    dev = q2k.device
+    out = K2qCsrVarlen(
+        row_ptr=torch.empty((Hkv, total_rows + 1), dtype=torch.int32, device=dev),
+        q_indices=torch.empty((Hkv, total_q * topk), dtype=torch.int32, device=dev),
+        qsplit=torch.empty((Hkv, total_q * topk), dtype=torch.int32, device=dev),
+        split_counts=torch.empty((total_q, Hkv), dtype=torch.int32, device=dev),
+        plan=torch.empty(plan_bytes, dtype=torch.uint8, device=dev),
+        cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, B=B, Hkv=Hkv, total_q=total_q, topk=topk,
+        qhead_per_kv=qhead_per_kv)
+    ws = _ws(ws_bytes, dev)
+    if seqused is not None:
+        _need(seqused, torch.int32, "seqused")
+    rc = L.msa_build_k2q_csr_varlen(_p(q2k), _p(cu_seqlens_q), _p(cu_seqlens_k), B, Hkv, total_q, max_seqlen_q,
+                                    max_seqlen_k, total_rows, topk, BLK, qhead_per_kv, _p(seqused), _p(out.row_ptr),
+                                    _p(out.q_indices), _p(out.qsplit), _p(out.split_counts), _p(out.plan),
+                                    out.plan.numel(), _p(ws), ws.numel(), _p(status), _stream(stream))
+    check(rc, "msa_build_k2q_csr_varlen")
+    out._workspace = ws  # kept alive until the stream has used it
+    return out
+
+
+def _opts(partial_dtype: int, lse_temperature_scale: float, lse_temperature: Optional[torch.Tensor]):
+    o = FwdOptions()
+    o.partial_dtype = int(partial_dtype)
+    o.lse_temperature_scale = float(lse_temperature_scale)
+    o.lse_temperature = None if lse_temperature is None else lse_temperature.data_ptr()
+    return o
+
+
+def sparse_attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, csr: K2qCsrVarlen, *, causal: bool,
+                           softmax_scale: Optional[float] = None, kv_format: str = "bf16",
+                           k_scales: Optional[torch.Tensor] = None, v_scales: Optional[torch.Tensor] = None,
+                           partial_dtype: int = MSA_PARTIAL_BF16, lse_temperature_scale: Optional[float] = None,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                           stream=None):
+    """msa_sparse_attn_fwd_varlen: q [total_q,Hq,D], k/v [total_k,Hkv,D] -> (O, LSE[, temperature LSE])."""
+    _need(q, torch.bfloat16, "q")
+    total_q, Hq, D = q.shape
+    fmt = _kv_format(kv_format, k, v, k_scales, v_scales)
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    lse_t = None
+    if lse_temperature_scale is not None:
+        lse_t = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    opts = _opts(partial_dtype, 1.0 if lse_temperature_scale is None else lse_temperature_scale, lse_t)
+    L = lib()
+    if workspace is None:
+        n = L.msa_sparse_attn_fwd_varlen_workspace_size(total_q, Hq, csr.topk, D, ctypes.byref(opts))
+        if n == 0:
+            raise ValueError("unsupported varlen forward shape or options")
+        workspace = _ws(n, q.device)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = L.msa_sparse_attn_fwd_varlen(_p(q), _p(k), _p(v), fmt, _p(k_scales), _p(v_scales), _p(csr.q_indices),
+                                      _p(csr.qsplit), _p(csr.split_counts), _p(csr.plan), _p(csr.cu_seqlens_q),
+                                      _p(csr.cu_seqlens_k), csr.B, total_q, total_k, Hq, Hkv, D, BLK, csr.topk,
+                                      int(bool(causal)), scale, ctypes.byref(opts), _p(out), _p(lse),
+                                      _p(workspace), workspace.numel(), _p(status), _stream(stream))
+    check(rc, "msa_sparse_attn_fwd_varlen")
+    return (out, lse) if lse_t is None else (out, lse, lse_t)
+
+
 def fwd_workspace(B: int, Sq: int, Hq: int, topk: int, device) -> torch.Tensor:
     n = lib().msa_sparse_attn_fwd_workspace_size(B, Sq, Hq, topk, 128)
     if n == 0:
@@ -108,13 +234,7 @@ def sparse_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, csr: K2qC
     """msa_sparse_attn_fwd: q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] (or NVFP4 packed) -> (O, LSE)."""
     _need(q, torch.bfloat16, "q")
     B, Sq, Hq, D = q.shape
-    fmt = MSA_KV_BF16 if kv_format == "bf16" else MSA_KV_NVFP4
-    if fmt == MSA_KV_BF16:
-        _need(k, torch.bfloat16, "k")
-        _need(v, torch.bfloat16, "v")
-    else:
-        for t, n in ((k, "k"), (v, "v"), (k_scales, "k_scales"), (v_scales, "v_scales")):
-            _need(t, torch.uint8, n)
+    fmt = _kv_format(kv_format, k, v, k_scales, v_scales)
     Skv, Hkv = k.shape[1], k.shape[2]
     if out is None:
         out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=q.device)
@@ -138,7 +258,7 @@ def sparse_attn_fwd_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
     """msa_sparse_attn_fwd_partial: the attention tiles only (split partials into ``workspace``)."""
     B, Sq, Hq, D = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
-    fmt = MSA_KV_BF16 if kv_format == "bf16" else MSA_KV_NVFP4
+    fmt = _kv_format(kv_format, k, v, k_scales, v_scales)
     scale = -1.0 if softmax_scale is None else float(softmax_scale)
     rc = lib().msa_sparse_attn_fwd_partial(_p(q), _p(k), _p(v), fmt, _p(k_scales), _p(v_scales), _p(csr.q_indices),
                                            _p(csr.qsplit), _p(csr.plan), B, Sq, Skv, Hq, Hkv, D, BLK, csr.topk,
@@ -192,6 +312,43 @@ def sparse_attn_paged_fwd(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                                          scale, _p(out), _p(lse), _p(workspace), workspace.numel(), _p(status),
                                          _stream(stream))
     check(rc, "msa_sparse_attn_paged_fwd")
+    return out, lse
+
+
+def paged_attn_fwd(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor,
+                   seqused: torch.Tensor, q2k: Optional[torch.Tensor] = None, *, kv_format: str = "bf16",
+                   causal: bool = True, softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None):
+    """msa_paged_attn_fwd: paged decode over bf16 or e4m3 pools [num_pages,page,Hkv,D]; q2k None is the
+    dense mode (every block of each sequence)."""
+    _need(q, torch.bfloat16, "q")
+    _need(page_table, torch.int32, "page_table")
+    _need(seqused, torch.int32, "seqused")
+    fmt = _kv_format(kv_format, k_pool, v_pool, None, None)
+    total_q, Hq, D = q.shape
+    num_pages, page, Hkv, _ = k_pool.shape
+    B, max_pages = page_table.shape
+    Sq = total_q // B
+    topk = 0
+    if q2k is not None:
+        _need(q2k, torch.int32, "q2k")
+        topk = q2k.shape[-1]
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    L = lib()
+    if workspace is None:
+        n = L.msa_paged_attn_fwd_workspace_size(B, Sq, Hq, Hkv, D, topk, max_pages)
+        if n == 0:
+            raise ValueError("unsupported paged decode shape")
+        workspace = _ws(n, q.device)
+    scale = -1.0 if softmax_scale is None else float(softmax_scale)
+    rc = L.msa_paged_attn_fwd(_p(q), _p(k_pool), _p(v_pool), fmt, num_pages, _p(page_table), max_pages, _p(seqused),
+                              _p(q2k), B, Sq, Hq, Hkv, D, page, topk, int(bool(causal)), scale, _p(out), _p(lse),
+                              _p(workspace), workspace.numel(), _p(status), _stream(stream))
+    check(rc, "msa_paged_attn_fwd")
     return out, lse
 
 

@@ -25,10 +25,23 @@ MSA_STATUS_PAGE_RANGE = 0x4
 MSA_STATUS_PLAN_OVERFLOW = 0x8
 MSA_STATUS_TIMEOUT = 0x10
 MSA_STATUS_LAUNCH = 0x20
-MSA_STATUS_FATAL_MASK = MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH
+MSA_STATUS_SHAPE = 0x40
+MSA_STATUS_FATAL_MASK = (MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH
+                         | MSA_STATUS_SHAPE)
 
 MSA_KV_BF16 = 0
 MSA_KV_NVFP4 = 1
+MSA_KV_FP8 = 2
+
+MSA_PARTIAL_BF16 = 0
+MSA_PARTIAL_FP16 = 1
+MSA_PARTIAL_FP32 = 2
+
+
+class FwdOptions(ctypes.Structure):
+    """msa_fwd_options (include/msa.h)."""
+    _fields_ = [("partial_dtype", ctypes.c_int), ("lse_temperature_scale", ctypes.c_float),
+                ("lse_temperature", ctypes.c_void_p)]
 
 
 class MsaError(RuntimeError):
@@ -82,6 +95,21 @@ def lib():
     L.msa_sparse_attn_paged_fwd_workspace_size.restype = SZ
     L.msa_sparse_attn_paged_fwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P, P]
     L.msa_sparse_attn_paged_fwd.restype = I
+    L.msa_k2q_csr_varlen_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    L.msa_k2q_csr_varlen_workspace_size.restype = SZ
+    L.msa_plan_varlen_size.argtypes = [I, I, I, I, I, I]
+    L.msa_plan_varlen_size.restype = SZ
+    L.msa_build_k2q_csr_varlen.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P, SZ, P, P]
+    L.msa_build_k2q_csr_varlen.restype = I
+    L.msa_sparse_attn_fwd_varlen_workspace_size.argtypes = [I, I, I, I, P]
+    L.msa_sparse_attn_fwd_varlen_workspace_size.restype = SZ
+    L.msa_sparse_attn_fwd_varlen.argtypes = [P, P, P, I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P,
+                                             P, P, P, SZ, P, P]
+    L.msa_sparse_attn_fwd_varlen.restype = I
+    L.msa_paged_attn_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    L.msa_paged_attn_fwd_workspace_size.restype = SZ
+    L.msa_paged_attn_fwd.argtypes = [P, P, P, I, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P, P]
+    L.msa_paged_attn_fwd.restype = I
     L.msa_nvfp4_quantize.argtypes = [P, I64, I, P, P, P]
     L.msa_nvfp4_quantize.restype = I
     _lib = L

@@ -24,12 +24,14 @@
 namespace msa {
 
 // Split partials: topk slots per query head.
-FwdWorkspace fwd_workspace_layout(int B, int Sq, int Hq, int topk, int D) {
+FwdWorkspace fwd_workspace_layout(int64_t total_q, int Hq, int topk, int D, int part_dtype, bool temp) {
     FwdWorkspace w;
-    size_t rows = (size_t)B * Sq * topk * Hq;
+    const size_t rows = (size_t)total_q * topk * Hq;
+    const size_t elem = part_dtype == MSA_PARTIAL_FP32 ? 4 : 2;
     w.o_part = 0;
-    w.stat_part = align_up(rows * D * sizeof(__nv_bfloat16), 256);
-    w.bytes = align_up(w.stat_part + rows * sizeof(float2), 256);
+    w.stat_part = align_up(rows * D * elem, 256);
+    w.stat_temp = align_up(w.stat_part + rows * sizeof(float2), 256);
+    w.bytes = temp ? align_up(w.stat_temp + rows * sizeof(float2), 256) : w.stat_temp;
     return w;
 }
 
@@ -40,54 +42,50 @@ int num_sms() {
     return n;
 }
 
-namespace {
-template <int KV_FORMAT, int NKV, int NQ, bool WHOLE_ROW>
-int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
-                 cudaStream_t stream) {
-    const size_t smem = tck::Layout<NKV, NQ>::BYTES;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, WHOLE_ROW>, dim3(grid),
-                            dim3(tck::threads_for(WHOLE_ROW)), smem, stream, mk, mv, mq, t));
-    return MSA_OK;
-}
-}  // namespace
-
 // Builds the tensor maps (Q rows; K and V over kv_tokens token rows) and
 // launches the tile kernel for t, one CTA per SM, at most `capacity` CTAs
 // (the plan's unit capacity).
 int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void *k, const void *v, int64_t kv_tokens,
-                 int kv_format, cudaStream_t stream) {
+                 int kv_format, bool temp, cudaStream_t stream) {
     int grid = (int)std::min<int64_t>(capacity, (int64_t)num_sms());
     if (grid < 1) grid = 1;
     CUtensorMap mk, mv, mq;
     memset(&mk, 0, sizeof mk);
     memset(&mv, 0, sizeof mv);
-    const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, (int64_t)t.B * t.Sq * t.Hkv, t.qpk)
-                                 : make_q_map(&mq, q, (int64_t)t.B * t.Sq * t.Hq, 1);
+    const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, t.total_q * t.Hkv, t.qpk)
+                                 : make_q_map(&mq, q, t.total_q * t.Hq, 1);
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
         if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
         // prefill: two K/V stages and three Q stages; paged decode (a unit is
         // one chunk, its K/V block from HBM; a group's consecutive units share
         // one Q tile): three K/V stages and one Q
-        if (t.unit_page) return launch_tiles<MSA_KV_BF16, 3, 1, true>(mk, mv, mq, t, grid, stream);
-        return launch_tiles<MSA_KV_BF16, 2, 3, false>(mk, mv, mq, t, grid, stream);
+        if (t.unit_page) return launch_tiles_paged(mk, mv, mq, t, grid, stream);
+        return temp ? launch_tiles_bf16_temp(mk, mv, mq, t, grid, stream)
+                    : launch_tiles_bf16(mk, mv, mq, t, grid, stream);
     }
-    return launch_tiles<MSA_KV_NVFP4, 2, 3, false>(mk, mv, mq, t, grid, stream);
+    // NVFP4 / FP8: the dequantising warp reads K and V itself (no K/V maps)
+    if (kv_format == MSA_KV_FP8) {
+        if (t.unit_page) return launch_tiles_paged_fp8(mk, mv, mq, t, grid, stream);
+        return temp ? launch_tiles_fp8_temp(mk, mv, mq, t, grid, stream) : launch_tiles_fp8(mk, mv, mq, t, grid, stream);
+    }
+    return temp ? launch_tiles_nvfp4_temp(mk, mv, mq, t, grid, stream)
+                : launch_tiles_nvfp4(mk, mv, mq, t, grid, stream);
 }
 
 namespace {
 
 // Standalone LSE combine: one thread per output piece (group, 8-dim chunk c,
 // head j of the group), in the partials' own order, so for each split the
-// threads of a warp read contiguous 16-byte pieces.
-template <int MAXS>
-__global__ void __launch_bounds__(256, 2) combine_kernel(const uint4 *__restrict__ o_part,
+// threads of a warp read contiguous pieces.  The thread of chunk 0 also
+// writes the LSE and, with temperature statistics, the temperature LSE.
+template <int MAXS, int PD>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const void *__restrict__ o_part,
                                                          const float2 *__restrict__ stat_part,
+                                                         const float2 *__restrict__ stat_temp,
                                                          const int32_t *__restrict__ split_counts, int64_t groups,
                                                          int qpk, int topk, uint4 *__restrict__ o,
-                                                         float *__restrict__ lse) {
+                                                         float *__restrict__ lse, float *__restrict__ lse_temp) {
     grid_dependency_wait();  // the partials come from the previous kernel
     grid_dependents_launch();
     const int64_t item = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -100,27 +98,31 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4 *__restrict
     n = n < topk ? n : topk;
     uint4 out;
     float l;
-    combine_piece<MAXS>(o_part, stat_part, grp, n, topk, qpk, c, j, out, l);
+    combine_piece<MAXS, PD, PD == MSA_PARTIAL_FP32 ? 8 : 16>(o_part, stat_part, grp, n, topk, qpk, c, j, out, l);
     // o [B*Sq][Hq][D]: group grp = gq*Hkv + h holds query heads h*qpk .. h*qpk+qpk-1
     const int64_t orow = grp * qpk + j;  // == gq*Hq + h*qpk + j
     o[orow * 16 + c] = out;
     if (c == 0 && lse) lse[orow] = l;
+    if (c == 0 && lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, qpk, j);
 }
 
-// The combine for qhead_per_kv 16 (a group's pieces = 256 threads): one
-// persistent CTA per SM walks groups blockIdx.x, + gridDim.x, ...; thread 0
-// copies each group's split partials (n x 4 KB, contiguous) and statistics
-// (n x 128 B) into a ring of kRingBufs shared-memory buffers with bulk copies,
-// kRingBufs groups ahead, so that the bytes in flight do not live in
-// registers; the 256 threads merge from shared memory (same arithmetic as
+// The combine for qhead_per_kv 16 and 16-byte pieces (a group's pieces = 256
+// threads): one persistent CTA per SM walks groups blockIdx.x, + gridDim.x,
+// ...; thread 0 copies each group's split partials (n x 4 KB, contiguous) and
+// statistics (n x 128 B) into a ring of kRingBufs shared-memory buffers with
+// bulk copies, kRingBufs groups ahead, so that the bytes in flight do not live
+// in registers; the 256 threads merge from shared memory (same arithmetic as
 // combine_kernel) and release the buffer warp by warp.
 constexpr int kRingBufs = 3;
 __host__ __device__ constexpr uint32_t ring_buf_bytes(int topk) { return (uint32_t)topk * (4096u + 128u); }
+template <int PD>
 __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__restrict__ o_part,
                                                               const float2 *__restrict__ stat_part,
+                                                              const float2 *__restrict__ stat_temp,
                                                               const int32_t *__restrict__ split_counts,
                                                               int64_t groups, int topk, uint4 *__restrict__ o,
-                                                              float *__restrict__ lse, uint32_t *status) {
+                                                              float *__restrict__ lse, float *__restrict__ lse_temp,
+                                                              uint32_t *status) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t base = smem_u32(smem), bb = ring_buf_bytes(topk);
     const uint32_t bars = base + kRingBufs * bb;  // FULL[kRingBufs], EMPTY[kRingBufs]
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
     auto empty = [&](int b) { return bars + 8u * (kRingBufs + b); };
     __shared__ int abort_flag_s;
     volatile int *abort_flag = &abort_flag_s;
-    const int t = threadIdx.x, c = t >> 4, j = t & 15, warp = t >> 5, lane = t & 31;
+    const int t = threadIdx.x, c = t >> 4, j = t & 15, lane = t & 31;
     if (t == 0) {
         for (int b = 0; b < kRingBufs; ++b) {
             tc::mbar_init(full(b), 1);
@@ -172,14 +174,14 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
         n = n < topk ? n : topk;
         uint4 out;
         float l;
-        combine_piece<16, 16, true>(reinterpret_cast<const uint4 *>(smem + b * bb),
-                                    reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096), 0, n, topk, 16, c, j,
-                                    out, l);
+        combine_piece<16, PD, 16, true>(smem + b * bb, reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096),
+                                        0, n, topk, 16, c, j, out, l);
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty(b));
         const int64_t orow = grp * 16 + j;
         o[orow * 16 + c] = out;
         if (c == 0 && lse) lse[orow] = l;
+        if (c == 0 && lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, j);
         if (t == 0 && blockIdx.x + (k + kRingBufs) * G < groups && ok) {
             ok = issue(k + kRingBufs);
             if (ok) ++issued;
@@ -191,7 +193,86 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
         for (int64_t kk = k; kk < issued; ++kk)
             tc::mbar_wait(full((int)(kk % kRingBufs)), (uint32_t)((kk / kRingBufs) & 1), &dummy, status, 0);
     }
-    (void)warp;
+}
+
+template <int PD>
+int combine_generic(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
+                    int qpk, int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
+    const int64_t blocks = ceil_div(groups * 16 * qpk, 256);
+    if (topk <= 16)
+        MSA_CUDA_TRY(launch_pdl(combine_kernel<16, PD>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, tp,
+                                split_counts, groups, qpk, topk, ob, lse, lse_temp));
+    else
+        MSA_CUDA_TRY(launch_pdl(combine_kernel<32, PD>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, tp,
+                                split_counts, groups, qpk, topk, ob, lse, lse_temp));
+    return MSA_OK;
+}
+
+template <int PD>
+int combine_ring(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
+                 int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
+    const size_t smem = kRingBufs * ring_buf_bytes(topk) + 16u * kRingBufs;
+    MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel<PD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
+    MSA_CUDA_TRY(launch_pdl(combine_ring_kernel<PD>, dim3(grid), dim3(256), smem, stream,
+                            static_cast<const uint4 *>(op), sp, tp, split_counts, groups, topk, ob, lse, lse_temp,
+                            (uint32_t *)nullptr));
+    return MSA_OK;
+}
+
+}  // namespace
+
+int combine_launch(const int32_t *split_counts, int64_t groups, int qpk, int topk, void *o, float *lse,
+                   float *lse_temp, const char *ws, const FwdWorkspace &w, int part_dtype, cudaStream_t stream) {
+    const void *op = ws + w.o_part;
+    const float2 *sp = reinterpret_cast<const float2 *>(ws + w.stat_part);
+    const float2 *tp = lse_temp ? reinterpret_cast<const float2 *>(ws + w.stat_temp) : nullptr;
+    uint4 *ob = static_cast<uint4 *>(o);
+    // qhead_per_kv 16 with 16-byte pieces: staged through a shared-memory ring
+    if (qpk == 16 && topk <= 16 && part_dtype == MSA_PARTIAL_BF16)
+        return combine_ring<MSA_PARTIAL_BF16>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+    if (qpk == 16 && topk <= 16 && part_dtype == MSA_PARTIAL_FP16)
+        return combine_ring<MSA_PARTIAL_FP16>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+    if (part_dtype == MSA_PARTIAL_FP32)
+        return combine_generic<MSA_PARTIAL_FP32>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp,
+                                                 stream);
+    if (part_dtype == MSA_PARTIAL_FP16)
+        return combine_generic<MSA_PARTIAL_FP16>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp,
+                                                 stream);
+    return combine_generic<MSA_PARTIAL_BF16>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp, stream);
+}
+
+namespace {
+
+// TcParams of a prefill forward (uniform or ragged; the caller sets the
+// batch-specific fields).
+TcParams prefill_params(const void *k, const void *v, const void *k_scales, const void *v_scales,
+                        const int32_t *qsplit, const void *plan, char *ws, const FwdWorkspace &w, int Hq, int Hkv,
+                        int D, int topk, int causal, float softmax_scale, uint32_t *status_dev) {
+    TcParams t;
+    memset(&t, 0, sizeof t);
+    t.k_packed = static_cast<const uint8_t *>(k);
+    t.v_packed = static_cast<const uint8_t *>(v);
+    t.k_scales = static_cast<const uint8_t *>(k_scales);
+    t.v_scales = static_cast<const uint8_t *>(v_scales);
+    t.qsplit = qsplit;
+    t.plan = static_cast<const PlanHeader *>(plan);
+    t.units = reinterpret_cast<const PlanUnit *>(t.plan + 1);
+    t.o_part = ws + w.o_part;
+    t.stat_part = reinterpret_cast<float2 *>(ws + w.stat_part);
+    t.stat_temp = reinterpret_cast<float2 *>(ws + w.stat_temp);
+    t.part_dtype = MSA_PARTIAL_BF16;
+    t.inv_temp = 1.f;
+    t.seqused = nullptr;
+    t.unit_page = nullptr;
+    t.cu_q = t.cu_k = nullptr;
+    t.status = status_dev;
+    t.Hq = Hq; t.Hkv = Hkv; t.qpk = Hq / Hkv; t.topk = topk;
+    t.causal = causal ? 1 : 0;
+    t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+    t.scale_log2 = t.scale * 1.4426950408889634f;
+    t.p_bound = 64.f;
+    return t;
 }
 
 }  // namespace
@@ -201,7 +282,7 @@ using namespace msa;
 
 extern "C" size_t msa_sparse_attn_fwd_workspace_size(int B, int Sq, int Hq, int topk, int D) {
     if (B <= 0 || Sq <= 0 || Hq <= 0 || topk <= 0 || D != kD) return 0;
-    return fwd_workspace_layout(B, Sq, Hq, topk, D).bytes;
+    return fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D).bytes;
 }
 
 extern "C" int msa_sparse_attn_fwd_partial(const void *q, const void *k, const void *v, int kv_format,
@@ -212,37 +293,25 @@ extern "C" int msa_sparse_attn_fwd_partial(const void *q, const void *k, const v
                                            cudaStream_t stream) {
     if (!q || !k || !v || !q_indices || !qsplit || !plan || !workspace) return MSA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Skv <= 0 || Hq <= 0 || Hkv <= 0 || topk <= 0 || Hq % Hkv) return MSA_ERR_INVALID_ARG;
-    if (kv_format != MSA_KV_BF16 && kv_format != MSA_KV_NVFP4) return MSA_ERR_INVALID_ARG;
+    if (Hkv > kMaxHkv || ceil_div(Skv, kBlk) > kMaxNblk) return MSA_ERR_UNSUPPORTED;
+    if (kv_format != MSA_KV_BF16 && kv_format != MSA_KV_NVFP4 && kv_format != MSA_KV_FP8) return MSA_ERR_INVALID_ARG;
     if (kv_format == MSA_KV_NVFP4 && (!k_scales || !v_scales)) return MSA_ERR_INVALID_ARG;
     const int qpk = Hq / Hkv;
     if (D != kD || blk_kv != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
     if ((int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
-    FwdWorkspace w = fwd_workspace_layout(B, Sq, Hq, topk, D);
+    const FwdWorkspace w = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D);
     if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(plan, 16)) return MSA_ERR_INVALID_ARG;
 
-    char *ws = static_cast<char *>(workspace);
-    TcParams t;
-    t.k_packed = static_cast<const uint8_t *>(k);
-    t.v_packed = static_cast<const uint8_t *>(v);
-    t.k_scales = static_cast<const uint8_t *>(k_scales);
-    t.v_scales = static_cast<const uint8_t *>(v_scales);
-    t.qsplit = qsplit;
-    t.plan = static_cast<const PlanHeader *>(plan);
-    t.units = reinterpret_cast<const PlanUnit *>(t.plan + 1);
-    t.o_part = reinterpret_cast<__nv_bfloat16 *>(ws + w.o_part);
-    t.stat_part = reinterpret_cast<float2 *>(ws + w.stat_part);
-    t.seqused = nullptr;
-    t.unit_page = nullptr;
-    t.status = status_dev;
-    t.B = B; t.Sq = Sq; t.Skv = Skv; t.Hq = Hq; t.Hkv = Hkv; t.qpk = qpk; t.topk = topk;
+    TcParams t = prefill_params(k, v, k_scales, v_scales, qsplit, plan, static_cast<char *>(workspace), w, Hq, Hkv,
+                                D, topk, causal, softmax_scale, status_dev);
+    t.B = B; t.Sq = Sq; t.Skv = Skv;
     t.nblk = (int)ceil_div(Skv, kBlk);
-    t.causal = causal ? 1 : 0;
     t.cap = (int64_t)B * Sq * topk;
-    t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-    t.scale_log2 = t.scale * 1.4426950408889634f;
-
-    return tiles_launch(t, plan_capacity(B, Hkv, Sq, Skv, topk, qpk), q, k, v, (int64_t)B * Skv, kv_format, stream);
+    t.kv_rows = (int64_t)B * Skv;
+    t.total_q = (int64_t)B * Sq;
+    const int64_t cap = plan_capacity((int64_t)B * t.nblk, (int64_t)B * Sq, Hkv, topk, qpk);
+    return tiles_launch(t, cap, q, k, v, (int64_t)B * Skv, kv_format, false, stream);
 }
 
 extern "C" int msa_sparse_attn_combine(const int32_t *split_counts, int B, int Sq, int Hq, int Hkv, int D, int topk,
@@ -251,31 +320,11 @@ extern "C" int msa_sparse_attn_combine(const int32_t *split_counts, int B, int S
     if (!split_counts || !o || !workspace) return MSA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || topk <= 0 || Hq % Hkv) return MSA_ERR_INVALID_ARG;
     if (D != kD || !supported_topk(topk)) return MSA_ERR_UNSUPPORTED;
-    FwdWorkspace w = fwd_workspace_layout(B, Sq, Hq, topk, D);
+    const FwdWorkspace w = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D);
     if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
     if (!aligned(o, 16)) return MSA_ERR_INVALID_ARG;
-    const char *ws = static_cast<const char *>(workspace);
-    const int qpk = Hq / Hkv;
-    const int64_t groups = (int64_t)B * Sq * Hkv;
-    const int64_t blocks = ceil_div(groups * 16 * qpk, 256);
-    const uint4 *op = reinterpret_cast<const uint4 *>(ws + w.o_part);
-    const float2 *sp = reinterpret_cast<const float2 *>(ws + w.stat_part);
-    uint4 *ob = static_cast<uint4 *>(o);
-    if (qpk == 16 && topk <= 16) {
-        // staged through a shared-memory ring, one persistent CTA per SM
-        const size_t smem = kRingBufs * ring_buf_bytes(topk) + 16u * kRingBufs;
-        MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
-        MSA_CUDA_TRY(launch_pdl(combine_ring_kernel, dim3(grid), dim3(256), smem, stream, op, sp, split_counts, groups,
-                                topk, ob, lse, (uint32_t *)nullptr));
-    } else if (topk <= 16) {
-        MSA_CUDA_TRY(launch_pdl(combine_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, split_counts,
-                                groups, qpk, topk, ob, lse));
-    } else {
-        MSA_CUDA_TRY(launch_pdl(combine_kernel<32>, dim3((unsigned)blocks), dim3(256), 0, stream, op, sp, split_counts,
-                                groups, qpk, topk, ob, lse));
-    }
-    return MSA_OK;
+    return combine_launch(split_counts, (int64_t)B * Sq * Hkv, Hq / Hkv, topk, o, lse, nullptr,
+                          static_cast<const char *>(workspace), w, MSA_PARTIAL_BF16, stream);
 }
 
 extern "C" int msa_sparse_attn_fwd(const void *q, const void *k, const void *v, int kv_format, const void *k_scales,
@@ -291,4 +340,72 @@ extern "C" int msa_sparse_attn_fwd(const void *q, const void *k, const void *v, 
                                          status_dev, stream);
     if (rc != MSA_OK) return rc;
     return msa_sparse_attn_combine(split_counts, B, Sq, Hq, Hkv, D, topk, o, lse, workspace, ws_bytes, stream);
+}
+
+// Options of a ragged-batch forward: 0, or MSA_ERR_* for a value outside the supported set.
+static int check_options(const msa_fwd_options *opts) {
+    if (!opts) return MSA_OK;
+    if (opts->partial_dtype != MSA_PARTIAL_BF16 && opts->partial_dtype != MSA_PARTIAL_FP16 &&
+        opts->partial_dtype != MSA_PARTIAL_FP32)
+        return MSA_ERR_UNSUPPORTED;
+    if (opts->lse_temperature &&
+        !(opts->lse_temperature_scale > 0.f && opts->lse_temperature_scale < INFINITY))
+        return MSA_ERR_INVALID_ARG;
+    return MSA_OK;
+}
+
+extern "C" size_t msa_sparse_attn_fwd_varlen_workspace_size(int total_q, int Hq, int topk, int D,
+                                                          const msa_fwd_options *opts) {
+    if (total_q <= 0 || Hq <= 0 || topk <= 0 || D != kD || check_options(opts) != MSA_OK) return 0;
+    return fwd_workspace_layout(total_q, Hq, topk, D, opts ? opts->partial_dtype : MSA_PARTIAL_BF16,
+                                opts && opts->lse_temperature)
+        .bytes;
+}
+
+extern "C" int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int kv_format,
+                                          const void *k_scales, const void *v_scales, const int32_t *q_indices,
+                                          const int32_t *qsplit, const int32_t *split_counts, const void *plan,
+                                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B,
+                                          int total_q, int total_k, int Hq, int Hkv, int D, int blk_kv, int topk,
+                                          int causal, float softmax_scale, const msa_fwd_options *opts, void *o,
+                                          float *lse, void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                                          cudaStream_t stream) {
+    if (!q || !k || !v || !q_indices || !qsplit || !split_counts || !plan || !cu_seqlens_q || !cu_seqlens_k ||
+        !o || !workspace)
+        return MSA_ERR_INVALID_ARG;
+    if (B <= 0 || total_q <= 0 || total_k <= 0 || Hq <= 0 || Hkv <= 0 || topk <= 0 || Hq % Hkv)
+        return MSA_ERR_INVALID_ARG;
+    if (kv_format != MSA_KV_BF16 && kv_format != MSA_KV_NVFP4 && kv_format != MSA_KV_FP8) return MSA_ERR_INVALID_ARG;
+    if (kv_format == MSA_KV_NVFP4 && (!k_scales || !v_scales)) return MSA_ERR_INVALID_ARG;
+    const int qpk = Hq / Hkv;
+    if (D != kD || blk_kv != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
+    if (total_q >= (1 << 24) || Hkv > kMaxHkv) return MSA_ERR_UNSUPPORTED;
+    const int orc = check_options(opts);
+    if (orc != MSA_OK) return orc;
+    const int part_dtype = opts ? opts->partial_dtype : MSA_PARTIAL_BF16;
+    float *lse_temp = opts ? opts->lse_temperature : nullptr;
+    const FwdWorkspace w = fwd_workspace_layout(total_q, Hq, topk, D, part_dtype, lse_temp != nullptr);
+    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(plan, 16) || !aligned(o, 16))
+        return MSA_ERR_INVALID_ARG;
+
+    TcParams t = prefill_params(k, v, k_scales, v_scales, qsplit, plan, static_cast<char *>(workspace), w, Hq, Hkv,
+                                D, topk, causal, softmax_scale, status_dev);
+    t.cu_q = cu_seqlens_q;
+    t.cu_k = cu_seqlens_k;
+    // per-sequence sizes come from cu_seqlens; Sq / Skv / nblk are unused
+    t.B = B; t.Sq = 1; t.Skv = 1; t.nblk = 1;
+    t.cap = (int64_t)total_q * topk;
+    t.kv_rows = total_k;
+    t.total_q = total_q;
+    t.part_dtype = part_dtype;
+    // fp16 partials keep P <= 1 (the stored half-row P is rescaled whenever
+    // the row max grows), so that the unnormalised partial stays in range
+    t.p_bound = part_dtype == MSA_PARTIAL_FP16 ? 0.f : 64.f;
+    if (lse_temp) t.inv_temp = 1.f / opts->lse_temperature_scale;
+    int rc = tiles_launch(t, (int64_t)num_sms(), q, k, v, total_k, kv_format, lse_temp != nullptr, stream);
+    if (rc != MSA_OK) return rc;
+    // the combine's groups are (query, KV head) pairs over all sequences
+    return combine_launch(split_counts, (int64_t)total_q * Hkv, qpk, topk, o, lse, lse_temp,
+                          static_cast<const char *>(workspace), w, part_dtype, stream);
 }

@@ -275,4 +275,30 @@ __device__ __forceinline__ void nvfp4_piece_to_bf16(uint4 packed, uint32_t scale
     }
 }
 
+// Two e4m3 values (low 16 bits of x, first value in the low byte) -> f16x2,
+// exactly (every e4m3 value, subnormals included, is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+    uint32_t d;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(d) : "r"(x));
+    return d;
+}
+
+// 16 e4m3 values (16 bytes, first value in the lowest byte) -> 16 bf16 in two
+// 16-byte chunks, exactly (at most four significant bits each).
+__device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 (&out)[2]) {
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t f = e4m3x2_to_f16x2(words[i] >> (16 * h));
+            const float2 g = __half22float2(*reinterpret_cast<const __half2 *>(&f));
+            w[2 * i + h] = pack_bf16x2(g.x, g.y);
+        }
+    }
+    out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 }  // namespace msa

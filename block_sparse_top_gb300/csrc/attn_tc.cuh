@@ -48,15 +48,26 @@ struct TcParams {
     const int32_t *qsplit;
     const PlanHeader *plan;
     const PlanUnit *units;
-    __nv_bfloat16 *o_part;                // split partials, layout in combine.cuh
+    void *o_part;                         // split partials (part_dtype), layout in combine.cuh
     float2 *stat_part;                    // split statistics, layout in combine.cuh
+    float2 *stat_temp;                    // temperature statistics (instances with TEMP), same layout
+    int part_dtype;                       // MSA_PARTIAL_*: storage of the split partials
+    float inv_temp;                       // 1 / lse_temperature_scale (TEMP)
     // paged KV (decode): per-sequence used length and each unit's physical
     // page (-1: invalid entry, the unit's keys are skipped); null otherwise
     const int32_t *seqused;
     const int32_t *unit_page;
+    // ragged batches: cu_seqlens of the queries and keys [B+1]; null for a
+    // uniform batch (sequence b holds queries b*Sq.. and keys b*Skv..)
+    const int32_t *cu_q, *cu_k;
     uint32_t *status;
     int B, Sq, Skv, Hq, Hkv, qpk, topk, nblk, causal;
     int64_t cap;
+    int64_t kv_rows;  // token rows of the K/V arrays (bound of the dequant loads)
+    int64_t total_q;  // query rows of Q (all sequences)
+    // prefill softmax: largest log2 of a P value before the stored half-row P
+    // is rescaled to a new row max (bf16 / fp32 partials: 64; fp16: 0)
+    float p_bound;
     float scale, scale_log2;
 };
 
@@ -69,7 +80,8 @@ constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3, 
 // that stores each chunk's O; in paged decode the softmax warps store it.
 constexpr int threads_for(bool paged) { return paged ? kThreads : kThreads + 128; }
 // Chunk ring between the feed warp and the loader: per chunk its plan unit
-// (16 B), the unit's page, and up to 128 query ids (qsplit entries).
+// (16 B), the unit's page, its sequence's first key row (ragged batches), and
+// up to 128 query ids (qsplit entries).
 constexpr int kRing = 4;
 constexpr uint32_t kRingEntry = 32 + 128 * 4;
 
@@ -110,8 +122,8 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
     PlanUnit pu = p.units[u];
     Unit x;
     x.h = pu.head;
-    x.b = pu.row / p.nblk;
-    x.tok0 = (pu.row % p.nblk) * kBlk;
+    x.b = pu.seq;
+    x.tok0 = pu.blk * kBlk;
     x.start = pu.start;
     x.count = pu.count;
     int qc = 128 / p.qpk;
@@ -128,7 +140,9 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
 // one Q tile, and the softmax holds a whole S row in registers (one
 // tensor-memory load, 168 registers) instead of reading it in halves (133) --
 // the shorter chain suits decode, where one warp's rows gate each K/V stage.
-template <int KV_FORMAT, int NKV, int NQ, bool PAGED>
+// TEMP (prefill): each split also keeps the row sum of 2^(x / T), x = (S - m)
+// scale_log2, and its statistics (m scale / T, that sum), for the temperature LSE.
+template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool TEMP>
 __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
@@ -216,13 +230,14 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             if (!ok) break;
             const int *e = reinterpret_cast<const int *>(gbase + L::RING + slot * kRingEntry);
             Unit x;
-            x.h = e[0];
-            x.b = e[1] / p.nblk;
-            x.tok0 = (e[1] % p.nblk) * kBlk;
+            x.h = e[0] & 0xFFFF;
+            x.tok0 = (e[0] >> 16) * kBlk;
+            x.b = e[1];
             x.start = e[2];
             x.count = e[3];
             x.nch = (x.count + qc - 1) / qc;
             x.page = e[4];
+            const int seq_k0 = e[5];  // ragged: first key row of the sequence
             int ids[4];
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
@@ -238,8 +253,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                // token row: dense [B][Skv] layout, or the unit's page of the pool
-                const int row = p.unit_page ? x.page * kBlk : x.b * p.Skv + x.tok0;
+                // token row: the unit's page of the pool, the sequence's keys of
+                // a ragged batch, or dense [B][Skv]
+                const int row = p.unit_page ? x.page * kBlk : (p.cu_k ? seq_k0 : x.b * p.Skv) + x.tok0;
                 const bool copy = !p.unit_page || x.page >= 0;
                 if (lane == 0) {
                     if (copy)
@@ -350,6 +366,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 if (lane == 0) {
                     cp_async16(e, p.units + u);
                     if (p.unit_page) cp_async4(e + 16, p.unit_page + u);
+                    if (p.cu_k) cp_async4(e + 20, p.cu_k + x.b);
                 }
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4) {
@@ -362,8 +379,8 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         cp_async_wait<0>();
         __syncwarp();
     } else if (warp == kWarpDequant) {
-        // ------------------------------------------------------------------ NVFP4 K/V producer
-        if (KV_FORMAT == MSA_KV_NVFP4) {
+        // ------------------------------------------------------------------ NVFP4 / FP8 K/V producer
+        if (KV_FORMAT != MSA_KV_BF16) {
             int ui = 0;
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
@@ -374,23 +391,69 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                if constexpr (KV_FORMAT == MSA_KV_FP8) {
+                // 128 tokens x 8 pieces of 16 e4m3 values (16 bytes), for K and
+                // then for V.  Lane l converts piece l % 8 of tokens l / 8 + 4 i:
+                // lanes 8i..8i+7 read one token's 128 bytes.  Eight 16-byte
+                // loads are in flight before any is used.  Paged: the unit's
+                // page of the pool (an invalid page gives zeros; its keys are
+                // masked), all 128 rows.
+                const int pc = lane & 7, r0 = lane >> 3;
+                int64_t k0row, klen;
+                if (p.unit_page) {
+                    k0row = (int64_t)x.page * kBlk;
+                    klen = x.page >= 0 ? kBlk : 0;
+                } else {
+                    k0row = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b) : (int64_t)x.b * p.Skv) + x.tok0;
+                    klen = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - __ldg(p.cu_k + x.b) : (int64_t)p.Skv) - x.tok0;
+                }
+#pragma unroll 1
+                for (int k0 = 0; k0 < 64; k0 += 8) {
+                    const int isv = k0 >> 5, rb = r0 + 4 * (k0 & 31);
+                    const uint8_t *pbase = isv ? p.v_packed : p.k_packed;
+                    uint4 pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = rb + 4 * i;
+                        const bool in = r < klen && k0row + r < p.kv_rows;
+                        pk[i] = in ? __ldg(reinterpret_cast<const uint4 *>(pbase + ((k0row + r) * p.Hkv + x.h) * 128) + pc)
+                                   : make_uint4(0, 0, 0, 0);
+                    }
+                    // values 16 pc .. 16 pc + 15: column half pc / 4, chunks 2 (pc % 4), + 1
+                    const uint32_t tile = base + (isv ? L::V : L::K) + kb * 32768 + (pc >> 2) * 16384;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4 o4[2];
+                        e4m3x16_to_bf16(pk[i], o4);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                                             tile + tc::sw128_off(rb + 4 * i, (pc & 3) * 2 + c)),
+                                         "r"(o4[c].x), "r"(o4[c].y), "r"(o4[c].z), "r"(o4[c].w));
+                    }
+                }
+                } else {
                 // 128 tokens x 4 pieces of 32 values (16 packed bytes, two
                 // scales), for K and then for V.  Lane l converts piece l % 4
                 // of tokens l / 4 + 8 i: lanes 4i..4i+3 read one token's 64
                 // bytes.  Eight 16-byte loads are in flight before any is used.
                 const int pc = lane & 3, r0 = lane >> 2;
+                // the sequence's first key row and key count
+                const int64_t k0row = p.cu_k ? (int64_t)__ldg(p.cu_k + x.b) : (int64_t)x.b * p.Skv;
+                const int64_t klen = p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - k0row : (int64_t)p.Skv;
 #pragma unroll 1
                 for (int k0 = 0; k0 < 32; k0 += 8) {
                     const int isv = k0 >> 4, rb = r0 + 8 * (k0 & 15);
                     const uint8_t *pbase = isv ? p.v_packed : p.k_packed;
                     const uint8_t *sbase = isv ? p.v_scales : p.k_scales;
-                    const int64_t row0 = ((int64_t)x.b * p.Skv + x.tok0 + rb) * p.Hkv + x.h;
+                    const int64_t row0 = (k0row + x.tok0 + rb) * p.Hkv + x.h;
                     uint4 pk[8];
                     uint32_t sc2[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int64_t rr = row0 + (int64_t)(8 * i) * p.Hkv;
-                        const bool in = x.tok0 + rb + 8 * i < p.Skv;
+                        const int64_t t = x.tok0 + rb + 8 * i;
+                        const bool in = t < klen && k0row + t < p.kv_rows;
                         pk[i] = in ? __ldg(reinterpret_cast<const uint4 *>(pbase + rr * 64) + pc) : make_uint4(0, 0, 0, 0);
                         sc2[i] = in ? __ldg(reinterpret_cast<const uint16_t *>(sbase + rr * 8) + pc) : 0u;
                     }
@@ -406,6 +469,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                              tile + tc::sw128_off(rb + 8 * i, (pc & 1) * 4 + c)),
                                          "r"(o4[c].x), "r"(o4[c].y), "r"(o4[c].z), "r"(o4[c].w));
                     }
+                }
                 }
                 tc::fence_proxy_async();
                 tc::mbar_arrive(bar(L::KV_FULL + kb));
@@ -563,7 +627,10 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 // contiguous, so each store instruction writes whole runs
                 const int gq = packed & 0xFFFFFF, split = (packed >> 24) & 0xFF;
                 const int64_t grp = (int64_t)gq * p.Hkv + x.h;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
+                // piece (8 values) of chunk c at byte (index + c * qpk) * piece bytes
+                const int pb = part_piece_bytes(p.part_dtype);
+                char *dst = static_cast<char *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row) * pb;
+                const int64_t cstride = (int64_t)p.qpk * pb;
                 uint32_t r[64];
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
@@ -573,7 +640,28 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                         tc::fence_before_sync();
                         tc::mbar_arrive(bar(L::O_EMPTY + b));  // O is read: the next PV may start
                     }
-                    if (valid) {
+                    if (!valid) continue;
+                    // streaming stores: evict first from L2
+                    if (p.part_dtype == MSA_PARTIAL_FP32) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            float4 *d = reinterpret_cast<float4 *>(dst + (8 * hf + v4) * cstride);
+                            __stcs(d, make_float4(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]),
+                                                  __uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])));
+                            __stcs(d + 1, make_float4(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]),
+                                                      __uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+                        }
+                    } else if (p.part_dtype == MSA_PARTIAL_FP16) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4) {
+                            uint4 o4;
+                            o4.x = pack_f16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
+                            o4.y = pack_f16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
+                            o4.z = pack_f16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
+                            o4.w = pack_f16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
+                            __stcs(reinterpret_cast<uint4 *>(dst + (8 * hf + v4) * cstride), o4);
+                        }
+                    } else {
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4) {
                             uint4 o4;
@@ -581,7 +669,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                             o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
                             o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
                             o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                            __stcs(dst + (int64_t)(8 * hf + v4) * p.qpk, o4);  // streaming: evict first from L2
+                            __stcs(reinterpret_cast<uint4 *>(dst + (8 * hf + v4) * cstride), o4);
                         }
                     }
                 }
@@ -597,20 +685,29 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         const int j_of_row = R % p.qpk;  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
-        // the unit and its sequence's key count (paged: seqused[b]), loaded one unit ahead
-        auto kv_len_of = [&](const Unit &y) -> int { return PAGED ? __ldg(p.seqused + y.b) : p.Skv; };
+        // the unit and its sequence's key count (paged: seqused[b]), first
+        // global query and query count, loaded one unit ahead
+        auto seq_of = [&](const Unit &y) -> int3 {
+            if (PAGED) return make_int3(__ldg(p.seqused + y.b), y.b * p.Sq, p.Sq);
+            if (p.cu_q) {
+                const int q0 = __ldg(p.cu_q + y.b);
+                return make_int3(__ldg(p.cu_k + y.b + 1) - __ldg(p.cu_k + y.b), q0, __ldg(p.cu_q + y.b + 1) - q0);
+            }
+            return make_int3(p.Skv, y.b * p.Sq, p.Sq);
+        };
         Unit xnext{};
-        int kvnext = p.Skv;
+        int3 seqnext = make_int3(p.Skv, 0, p.Sq);
         if (u_begin < u_end) {
             xnext = load_unit(p, u_begin);
-            kvnext = kv_len_of(xnext);
+            seqnext = seq_of(xnext);
         }
         for (int u = u_begin; u < u_end && ok; u += u_step) {
             const Unit x = xnext;
-            const int64_t kv_len = kvnext;
+            const int64_t kv_len = seqnext.x;
+            const int seq_q0 = seqnext.y, seq_nq = seqnext.z;
             if (u + u_step < u_end) {
                 xnext = load_unit(p, u + u_step);
-                kvnext = kv_len_of(xnext);
+                seqnext = seq_of(xnext);
             }
             for (int c = 0; c < x.nch && ok; ++c, ++ci) {
                 if ((ci & 1) != wg) continue;
@@ -651,9 +748,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     if (valid && (!p.unit_page || x.page >= 0)) {
                         // keys visible to query sq of a sequence of kv_len keys
                         // (bottom-right causal: up to key sq + kv_len - Sq)
-                        const int sq = gq % p.Sq;
+                        const int sq = gq - seq_q0;
                         int64_t limit = kv_len - 1;
-                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
+                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - seq_nq);
                         const int64_t nv = limit - x.tok0 + 1;
                         nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                     }
@@ -723,8 +820,14 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     }
                 } else {
                     tc::fence_after_sync();
-                    // The S row is read 64 keys at a time: one pass for the max, one
-                    // for P (a whole row in registers leaves the compiler no room).
+                    // The S row is read 64 keys at a time (a whole row in registers
+                    // leaves the compiler no room), once: the first half's max is the
+                    // reference m for the whole row.  P = exp2((S - m) * scale_log2)
+                    // is exact softmax arithmetic for any reference, and the split
+                    // statistics carry m, so the second half may exceed it; only when
+                    // it exceeds it by more than p_bound (log2 units: P up to
+                    // 2^p_bound) is the first half's P rescaled to the new max (a
+                    // warp-uniform slow path).
                     uint32_t r[64];
                     tc::tmem_ld64(s_addr, r);
                     // row info while the load is in flight
@@ -734,9 +837,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     if (valid && (!p.unit_page || x.page >= 0)) {
                         // keys visible to query sq of a sequence of kv_len keys
                         // (bottom-right causal: up to key sq + kv_len - Sq)
-                        const int sq = gq % p.Sq;
+                        const int sq = gq - seq_q0;
                         int64_t limit = kv_len - 1;
-                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - p.Sq);
+                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - seq_nq);
                         const int64_t nv = limit - x.tok0 + 1;
                         nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
                     }
@@ -749,46 +852,80 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                 if (j >= lim) r[j] = 0xff800000u;
                         }
                     };
-                    // row max: three-input max, four independent chains
-                    float mm[4];
+                    // max of the half in registers: three-input max, four chains
+                    auto half_max = [&]() -> float {
+                        float mm[4];
 #pragma unroll
-                    for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
-                        tc::tmem_ld_wait();
-                        mask_half(hf);
+                        for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
 #pragma unroll
                         for (int j = 0; j < 64; j += 8) {
 #pragma unroll
                             for (int a = 0; a < 4; ++a)
                                 mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                         }
-                    }
-                    const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                    // P = exp2(S * scale_log2 - m * scale_log2): each half is read
-                    // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
-                    // the half) and stored over columns the half has already read;
-                    // row sum in packed f32x2 adds
-                    const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
+                        return fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                    };
                     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                    const float2 nm2 = make_float2(-mc, -mc);
                     float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 lt = make_float2(0.f, 0.f);  // TEMP: row sum of 2^(x / T)
+                    float m = -INFINITY;  // reference max
+                    float f = 1.f;        // rescale factor of the first half's P
+                    bool grow = false;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
-                        tc::tmem_ld64(s_addr + 64 * hf, r);
+                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
                         tc::tmem_ld_wait();
                         mask_half(hf);
+                        const float mh = half_max();
+                        if (hf == 0) {
+                            m = mh;
+                        } else {
+                            // the second half's max exceeds the reference by more
+                            // than the bound: it becomes the reference, the first
+                            // half's sum now and its stored P below scale by
+                            // f = 2^((m - mh) scale_log2) (0 when m was -inf)
+                            grow = mh > m && (m == -INFINITY || (mh - m) * p.scale_log2 > p.p_bound);
+                            if (grow) {
+                                f = (m == -INFINITY) ? 0.f : ex2_approx((m - mh) * p.scale_log2);
+                                if constexpr (TEMP) {
+                                    const float ft = (m == -INFINITY) ? 0.f : ex2_approx((m - mh) * p.scale_log2 * p.inv_temp);
+                                    lt.x *= ft;
+                                    lt.y *= ft;
+                                }
+                                m = mh;
+                                ll[0].x *= f; ll[0].y *= f; ll[1].x *= f; ll[1].y *= f;
+                            }
+                        }
+                        // P of this half against the reference, packed to bf16
+                        // pairs in place (r[j] <- keys 2j, 2j+1 of the half) and
+                        // stored over columns already read; row sum in packed
+                        // f32x2 adds
+                        const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
+                        const float2 nm2 = make_float2(-mc, -mc);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             float2 e =
                                 __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
+                            if constexpr (TEMP) {
+                                const float2 t = __fmul2_rn(e, make_float2(p.inv_temp, p.inv_temp));
+                                lt = __fadd2_rn(lt, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                            }
                             e.x = ex2_approx(e.x);
                             e.y = ex2_approx(e.y);
                             ll[j & 1] = __fadd2_rn(ll[j & 1], e);
                             r[j] = pack_bf16x2(e.x, e.y);
                         }
                         tc::tmem_st32(s_addr + 32 * hf, r);
+                    }
+                    if (__any_sync(0xffffffffu, grow)) {
+                        // rare: rescale the stored first-half P (columns 0-31) of
+                        // the rows whose reference moved (f = 1 leaves the others)
+                        tc::tmem_st_wait();
+                        tc::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = pack_bf16x2(bf16_lo(r[j]) * f, bf16_hi(r[j]) * f);
+                        tc::tmem_st32(s_addr, r);
                     }
                     const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
                     tc::tmem_st_wait();
@@ -798,8 +935,13 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     // stores the unnormalised O once PV has run
                     if (valid) {
                         const int64_t grp = (int64_t)gq * p.Hkv + x.h;
+                        const int64_t si = part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
                         const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
-                        __stcs(p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row), st);
+                        __stcs(p.stat_part + si, st);
+                        if constexpr (TEMP) {
+                            const float ltt = lt.x + lt.y;
+                            __stcs(p.stat_temp + si, make_float2(ltt > 0.f ? m * p.scale * p.inv_temp : -INFINITY, ltt));
+                        }
                     }
                 }
             }

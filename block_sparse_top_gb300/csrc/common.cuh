@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -67,8 +68,9 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
 // ---------------------------------------------------------------------------
 // Work plan shared by the CSR builder (writer) and the prefill kernel (reader)
 // ---------------------------------------------------------------------------
-// A unit is (KV head, CSR row, first q_indices position, query count); its
-// queries are processed in chunks of 128/qhead_per_kv queries, 128 rows each.
+// A unit is (KV head, KV block blk of sequence seq, first q_indices position,
+// query count); its queries are processed in chunks of 128/qhead_per_kv
+// queries, 128 rows each.
 struct PlanHeader {
     int32_t work_count;  // units written (device side, no host readback)
     int32_t capacity;    // units the buffer holds
@@ -81,11 +83,14 @@ struct PlanHeader {
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
 struct PlanUnit {
-    int32_t head;   // KV head h
-    int32_t row;    // global CSR row r = b*nblk + j
+    int16_t head;   // KV head h
+    int16_t blk;    // KV block j within the sequence (tokens 128 j ..)
+    int32_t seq;    // sequence b
     int32_t start;  // first position in q_indices[h]
     int32_t count;  // queries in this unit
 };
+static_assert(sizeof(PlanUnit) == 16, "plan unit is 16 bytes");
+constexpr int kMaxHkv = 32767;  // KV heads a plan unit can name
 
 inline int q_per_chunk(int qpk) { return 128 / qpk; }
 // Queries per unit: 8 chunks (K/V block loaded once per unit).
@@ -98,25 +103,23 @@ inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
 // -- W * qhead_per_kv * topk rows of D bf16 plus two floats -- at about 512
 // MiB: on the 32K causal workload the tiles + combine took 4.86 ms at 32 MiB,
 // 4.63 at 128, 4.49 at 512, and 4.47 with one wave per head.
-inline int64_t wave_queries(int B, int Sq, int qpk, int topk) {
+inline int64_t wave_queries(int64_t total_q, int qpk, int topk) {
     const int64_t per_q = (int64_t)qpk * topk * (kD * 2 + 8);
     int64_t w = ((((int64_t)512 << 20) / per_q) + 64) / 128 * 128;  // nearest multiple of 128
     if (w < 128) w = 128;
-    const int64_t total = (int64_t)B * Sq;
-    return w > total ? total : w;
+    return w > total_q ? total_q : w;
 }
-inline int64_t num_waves(int B, int Sq, int qpk, int topk) {
-    return ceil_div((int64_t)B * Sq, wave_queries(B, Sq, qpk, topk));
+inline int64_t num_waves(int64_t total_q, int qpk, int topk) {
+    return ceil_div(total_q, wave_queries(total_q, qpk, topk));
 }
 
-// Units: every (head, row, wave) segment adds at most one partial unit.
-inline int64_t plan_capacity(int B, int Hkv, int Sq, int Skv, int topk, int qpk) {
-    int64_t nblk = ceil_div(Skv, kBlk);
-    int64_t rows = (int64_t)B * nblk;
-    int64_t nnz = (int64_t)B * Sq * topk;
-    int64_t segs = rows * num_waves(B, Sq, qpk, topk);
+// Units of a plan over `rows` CSR rows per KV head and total_q queries: every
+// (head, row, wave) segment adds at most one partial unit.
+inline int64_t plan_capacity(int64_t rows, int64_t total_q, int Hkv, int topk, int qpk) {
+    const int64_t nnz = total_q * topk;
+    int64_t segs = rows * num_waves(total_q, qpk, topk);
     if (segs > nnz) segs = nnz;
-    int64_t per_head = segs + ceil_div(nnz, q_per_unit(qpk));
+    const int64_t per_head = segs + ceil_div(nnz, q_per_unit(qpk));
     return per_head * Hkv;
 }
 
@@ -125,6 +128,11 @@ inline int64_t plan_capacity(int B, int Hkv, int Sq, int Skv, int topk, int qpk)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 

@@ -19,6 +19,15 @@
 // The plan then cuts every row into units of at most 8 chunks of 128 rows,
 // ordered by KV head, then by wave: wave w holds the queries [w*W, (w+1)*W)
 // (W: wave_queries in common.cuh).
+//
+// Uniform batches (B sequences of Sq queries and Skv keys, q2k
+// [B][Hkv][Sq][topk]) and ragged ones (interface.py sparse_atten_func:
+// cu_seqlens_q / cu_seqlens_k, q2k [Hkv][total_q][topk] with block ids local
+// to each sequence) run the same kernels; for a ragged batch a first kernel
+// turns the cu_seqlens into a per-sequence table {first query, queries, keys,
+// first CSR row} (sequence b owns rows row0_b .. row0_b + ceil(keys/128) - 1),
+// dropping with MSA_STATUS_SHAPE any sequence whose ranges are inconsistent
+// or do not fit the sizes the caller declared.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,9 +38,41 @@ namespace {
 constexpr int kTileQ = 128;  // queries per CSR tile (4 x 32-bit mask words)
 
 struct CsrShape {
-    int B, Hkv, Sq, Skv, topk, nblk, ntiles;
-    int64_t rows, cap;
+    int B, Hkv, Sq, Skv, topk, nblk, ntiles;  // ragged: Sq, Skv, nblk, ntiles are per-sequence maxima
+    int64_t rows, cap, total_q;
+    const int4 *seqs;  // ragged: per sequence {first query, queries, keys, first row}; uniform: null
 };
+
+// One sequence's queries, keys, block count and first CSR row.
+struct Seq {
+    int64_t q0, row0;
+    int sq, kv, nblk;
+};
+
+__device__ __forceinline__ Seq seq_info(const CsrShape &s, int b) {
+    Seq x;
+    if (s.seqs) {
+        const int4 e = s.seqs[b];
+        x.q0 = e.x;
+        x.sq = e.y;
+        x.kv = e.z;
+        x.row0 = e.w;
+    } else {
+        x.q0 = (int64_t)b * s.Sq;
+        x.sq = s.Sq;
+        x.kv = s.Skv;
+        x.row0 = (int64_t)b * s.nblk;
+    }
+    x.nblk = (int)ceil_div(x.kv, kBlk);
+    return x;
+}
+
+// The top-k list of query sl (local) of sequence b, KV head h.
+__device__ __forceinline__ const int32_t *sel_of(const int32_t *q2k, const CsrShape &s, const Seq &x, int b, int h,
+                                                 int sl) {
+    return s.seqs ? q2k + ((int64_t)h * s.total_q + x.q0 + sl) * s.topk
+                  : q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sl) * s.topk;
+}
 
 // Validity of one slot: 0 <= j < nvalid and not named by an earlier slot.
 __device__ __forceinline__ bool slot_valid(const int32_t *sel, int t, int nvalid, uint32_t *status) {
@@ -49,31 +90,101 @@ __device__ __forceinline__ bool slot_valid(const int32_t *sel, int t, int nvalid
     return true;
 }
 
-__device__ __forceinline__ int seq_nvalid(const int32_t *seqused, int b, int Skv, int nblk) {
-    int64_t kv = seqused ? (int64_t)seqused[b] : (int64_t)Skv;
+// Blocks of sequence b a query may name: those below the used KV length.
+__device__ __forceinline__ int seq_nvalid(const int32_t *seqused, int b, const Seq &x) {
+    int64_t kv = seqused ? (int64_t)seqused[b] : (int64_t)x.kv;
     int64_t n = ceil_div(kv, kBlk);
-    if (n > nblk) n = nblk;
+    if (n > x.nblk) n = x.nblk;
     if (n < 0) n = 0;
     return (int)n;
 }
 
+// Ragged batches: the per-sequence table and row offsets row_off [B+1] from
+// cu_seqlens_q / cu_seqlens_k.  One CTA; sequences are scanned in passes of
+// blockDim.x.  A sequence with a decreasing range, a start below 0, queries
+// past total_q, more queries or keys than the declared maxima, or rows past
+// total_rows is dropped (no queries, no keys) and raises MSA_STATUS_SHAPE.
+__global__ void __launch_bounds__(1024) csr_seq_kernel(const int32_t *__restrict__ cu_q,
+                                                       const int32_t *__restrict__ cu_k, int B, int64_t total_q,
+                                                       int64_t total_rows, int max_sq, int max_kv, int4 *seqs,
+                                                       int32_t *row_off, uint32_t *status) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry_s;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < B; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        int q0 = 0, sq = 0, kv = 0, nb = 0;
+        if (b < B) {
+            q0 = cu_q[b];
+            const int q1 = cu_q[b + 1], k0 = cu_k[b], k1 = cu_k[b + 1];
+            sq = q1 - q0;
+            kv = k1 - k0;
+            const bool ok = q0 >= 0 && sq >= 0 && (int64_t)q1 <= total_q && sq <= max_sq && k0 >= 0 && kv >= 0 &&
+                            kv <= max_kv;
+            if (!ok) {
+                set_status(status, MSA_STATUS_SHAPE);
+                sq = kv = 0;
+            }
+            nb = (int)ceil_div(kv, kBlk);
+        }
+        int32_t x = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int32_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry_s;
+        int32_t row0 = incl - nb;
+        if (b < B) {
+            if ((int64_t)incl > total_rows) {  // rows past the declared capacity: drop the sequence
+                set_status(status, MSA_STATUS_SHAPE);
+                sq = kv = 0;
+                row0 = (int32_t)total_rows;
+            }
+            seqs[b] = make_int4(q0, sq, kv, row0);
+            row_off[b] = row0;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry_s = incl;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        row_off[B] = carry_s > total_rows ? (int32_t)total_rows : carry_s;
+        if ((int64_t)cu_q[B] != total_q) set_status(status, MSA_STATUS_SHAPE);  // queries outside every sequence
+    }
+}
+
 // Builds the per-block query masks of one tile in shared memory.
 __device__ void build_masks(uint32_t *masks, const int32_t *q2k, const int32_t *seqused, const CsrShape &s,
-                            int tile, int b, int h, uint32_t *status, int32_t *split_counts) {
-    for (int i = threadIdx.x; i < s.nblk * 4; i += blockDim.x) masks[i] = 0u;
+                            const Seq &x, int tile, int b, int h, uint32_t *status, int32_t *split_counts) {
+    for (int i = threadIdx.x; i < x.nblk * 4; i += blockDim.x) masks[i] = 0u;
     __syncthreads();
     int i = threadIdx.x;
     int sq = tile * kTileQ + i;
-    if (sq < s.Sq) {
-        int nvalid = seq_nvalid(seqused, b, s.Skv, s.nblk);
-        const int32_t *sel = q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sq) * s.topk;
+    if (sq < x.sq) {
+        int nvalid = seq_nvalid(seqused, b, x);
+        const int32_t *sel = sel_of(q2k, s, x, b, h, sq);
         int cnt = 0;
         for (int t = 0; t < s.topk; ++t) {
             if (!slot_valid(sel, t, nvalid, status)) continue;
             atomicOr(&masks[sel[t] * 4 + (i >> 5)], 1u << (i & 31));
             ++cnt;
         }
-        if (split_counts) split_counts[((int64_t)b * s.Sq + sq) * s.Hkv + h] = cnt;
+        if (split_counts) split_counts[(x.q0 + sq) * s.Hkv + h] = cnt;
     }
     __syncthreads();
 }
@@ -83,9 +194,11 @@ __global__ void csr_hist_kernel(const int32_t *__restrict__ q2k, const int32_t *
                                 uint32_t *status) {
     extern __shared__ uint32_t masks[];
     int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
-    build_masks(masks, q2k, seqused, s, tile, b, h, status, split_counts);
+    const Seq x = seq_info(s, b);
+    if (tile * kTileQ >= x.sq) return;  // past this sequence's queries (whole CTA)
+    build_masks(masks, q2k, seqused, s, x, tile, b, h, status, split_counts);
     int32_t *out = tile_counts + (((int64_t)h * s.B + b) * s.ntiles + tile) * s.nblk;
-    for (int j = threadIdx.x; j < s.nblk; j += blockDim.x) {
+    for (int j = threadIdx.x; j < x.nblk; j += blockDim.x) {
         const uint32_t *m = masks + j * 4;
         out[j] = __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
     }
@@ -101,12 +214,15 @@ __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *_
     const int ty = blockDim.y;
     int j = blockIdx.x * 32 + threadIdx.x;
     int b = blockIdx.y, h = blockIdx.z;
-    int per = (s.ntiles + ty - 1) / ty;
+    const Seq x = seq_info(s, b);
+    if (blockIdx.x * 32 >= x.nblk) return;  // past this sequence's blocks (whole CTA)
+    const int ntiles = (int)ceil_div(x.sq, kTileQ);
+    int per = (ntiles + ty - 1) / ty;
     int t0 = threadIdx.y * per;
-    int t1 = min(t0 + per, s.ntiles);
+    int t1 = min(t0 + per, ntiles);
     int32_t *base = tile_counts + ((int64_t)h * s.B + b) * s.ntiles * (int64_t)s.nblk;
     int32_t sum = 0;
-    if (j < s.nblk)
+    if (j < x.nblk)
         for (int t = t0; t < t1; ++t) sum += base[(int64_t)t * s.nblk + j];
     part[threadIdx.y][threadIdx.x] = sum;
     __syncthreads();
@@ -117,10 +233,10 @@ __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *_
             part[y][threadIdx.x] = run;
             run += v;
         }
-        if (j < s.nblk) row_ptr[(int64_t)h * (s.rows + 1) + (int64_t)b * s.nblk + j + 1] = run;
+        if (j < x.nblk) row_ptr[(int64_t)h * (s.rows + 1) + x.row0 + j + 1] = run;
     }
     __syncthreads();
-    if (j < s.nblk) {
+    if (j < x.nblk) {
         int32_t run = part[threadIdx.y][threadIdx.x];
         for (int t = t0; t < t1; ++t) {
             int32_t v = base[(int64_t)t * s.nblk + j];
@@ -203,17 +319,19 @@ __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_
                                    int32_t *__restrict__ q_indices, int32_t *__restrict__ qsplit) {
     extern __shared__ uint32_t masks[];
     int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
-    build_masks(masks, q2k, seqused, s, tile, b, h, nullptr, nullptr);
+    const Seq x = seq_info(s, b);
+    if (tile * kTileQ >= x.sq) return;  // past this sequence's queries (whole CTA)
+    build_masks(masks, q2k, seqused, s, x, tile, b, h, nullptr, nullptr);
     int i = threadIdx.x;
     int sq = tile * kTileQ + i;
-    if (sq >= s.Sq) return;
-    int nvalid = seq_nvalid(seqused, b, s.Skv, s.nblk);
-    const int32_t *sel = q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sq) * s.topk;
+    if (sq >= x.sq) return;
+    int nvalid = seq_nvalid(seqused, b, x);
+    const int32_t *sel = sel_of(q2k, s, x, b, h, sq);
     const int32_t *off = tile_off + (((int64_t)h * s.B + b) * s.ntiles + tile) * s.nblk;
-    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1) + (int64_t)b * s.nblk;
+    const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1) + x.row0;
     int32_t *qi = q_indices + (int64_t)h * s.cap;
     int32_t *qs = qsplit + (int64_t)h * s.cap;
-    int32_t gq = (int32_t)((int64_t)b * s.Sq + sq);
+    int32_t gq = (int32_t)(x.q0 + sq);
     int w = i >> 5;
     uint32_t below = (1u << (i & 31)) - 1u;
     int rank = 0;
@@ -222,7 +340,7 @@ __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_
         int j = sel[t];
         const uint32_t *m = masks + j * 4;
         int r = __popc(m[w] & below);
-        for (int x = 0; x < w; ++x) r += __popc(m[x]);
+        for (int y = 0; y < w; ++y) r += __popc(m[y]);
         int64_t pos = (int64_t)rp[j] + off[j] + r;
         qi[pos] = gq;
         qs[pos] = gq | (rank << 24);
@@ -258,7 +376,25 @@ __device__ __forceinline__ int32_t lower_bound(const int32_t *a, int32_t lo, int
 struct PlanShape {
     int64_t W, nwaves;
     int qpu;
+    const int32_t *row_off;  // ragged: first row of each sequence [B+1]; uniform: null
 };
+
+// Sequence and block of global row r.
+__device__ __forceinline__ void row_owner(const CsrShape &s, const PlanShape &ps, int64_t r, int &seq, int &blk) {
+    if (!ps.row_off) {
+        seq = (int)(r / s.nblk);
+        blk = (int)(r % s.nblk);
+        return;
+    }
+    int lo = 0, hi = s.B;  // last b with row_off[b] <= r (sequences without rows are skipped)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ps.row_off[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    seq = lo;
+    blk = (int)(r - ps.row_off[lo]);
+}
 
 __device__ __forceinline__ void segment_range(const int32_t *row_ptr, const int32_t *q_indices, const CsrShape &s,
                                               const PlanShape &ps, int64_t idx, int &h, int64_t &r, int32_t &lo,
@@ -311,12 +447,16 @@ __global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, const int
     int32_t lo, hi;
     segment_range(row_ptr, q_indices, s, ps, idx, h, r, lo, hi);
     const int32_t c = hi - lo;
+    if (c == 0) return;
     const int32_t u0 = unit_off[idx];
+    int seq, blk;
+    row_owner(s, ps, r, seq, blk);
     for (int32_t u = 0; u * ps.qpu < c; ++u) {
         if (u0 + u >= capacity) break;
         PlanUnit pu;
-        pu.head = h;
-        pu.row = (int32_t)r;
+        pu.head = (int16_t)h;
+        pu.blk = (int16_t)blk;
+        pu.seq = seq;
         pu.start = lo + u * ps.qpu;
         pu.count = min(ps.qpu, c - u * ps.qpu);
         units[u0 + u] = pu;
@@ -329,29 +469,41 @@ CsrShape make_shape(int B, int Hkv, int Sq, int Skv, int topk) {
     s.nblk = (int)ceil_div(Skv, kBlk);
     s.ntiles = (int)ceil_div(Sq, kTileQ);
     s.rows = (int64_t)B * s.nblk;
-    s.cap = (int64_t)B * Sq * topk;
+    s.total_q = (int64_t)B * Sq;
+    s.cap = s.total_q * topk;
+    s.seqs = nullptr;
+    return s;
+}
+
+// Ragged batch: Sq / Skv are the per-sequence maxima, rows the declared row capacity.
+CsrShape make_varlen_shape(int B, int Hkv, int64_t total_q, int max_sq, int max_kv, int64_t total_rows, int topk) {
+    CsrShape s = make_shape(B, Hkv, max_sq, max_kv, topk);
+    s.rows = total_rows;
+    s.total_q = total_q;
+    s.cap = total_q * topk;
     return s;
 }
 
 struct CsrWorkspace {
-    size_t tile_counts, units_per_row, total, bytes;
+    size_t tile_counts, units_per_row, total, seqs, row_off, bytes;
 };
 
 PlanShape make_plan_shape(const CsrShape &s, int qpk) {
     PlanShape ps;
-    ps.W = wave_queries(s.B, s.Sq, qpk, s.topk);
-    ps.nwaves = num_waves(s.B, s.Sq, qpk, s.topk);
+    ps.W = wave_queries(s.total_q, qpk, s.topk);
+    ps.nwaves = num_waves(s.total_q, qpk, s.topk);
     ps.qpu = q_per_unit(qpk);
+    ps.row_off = nullptr;
     return ps;
 }
 
 // Segments (head, wave, row) of the plan; qpk 16 gives the smallest waves,
 // hence the most of them.
 int64_t max_segments(const CsrShape &s) {
-    return num_waves(s.B, s.Sq, 16, s.topk) * s.Hkv * s.rows;
+    return num_waves(s.total_q, 16, s.topk) * s.Hkv * s.rows;
 }
 
-CsrWorkspace csr_workspace_layout(const CsrShape &s) {
+CsrWorkspace csr_workspace_layout(const CsrShape &s, bool ragged) {
     CsrWorkspace w;
     size_t off = 0;
     w.tile_counts = off;
@@ -360,43 +512,29 @@ CsrWorkspace csr_workspace_layout(const CsrShape &s) {
     off = align_up(off + sizeof(int32_t) * (size_t)max_segments(s), 256);
     w.total = off;
     off = align_up(off + 256, 256);
+    w.seqs = off;
+    if (ragged) off = align_up(off + sizeof(int4) * (size_t)s.B, 256);
+    w.row_off = off;
+    if (ragged) off = align_up(off + sizeof(int32_t) * ((size_t)s.B + 1), 256);
     w.bytes = off;
     return w;
 }
 
-}  // namespace
-}  // namespace msa
-
-using namespace msa;
-
-extern "C" size_t msa_k2q_csr_workspace_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv) {
-    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk) return 0;
-    return csr_workspace_layout(make_shape(B, Hkv, Sq, Skv, topk)).bytes;
+// Common argument checks of both builders (shape s already made).
+int check_csr_args(const CsrShape &s, int topk, int blk_kv, int qpk) {
+    if (blk_kv != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
+    if (s.total_q >= (1 << 24) || s.nblk > kMaxNblk || s.Hkv > kMaxHkv || s.B > 65535) return MSA_ERR_UNSUPPORTED;
+    if (s.rows >= ((int64_t)1 << 31) || s.cap >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
+    if ((int64_t)s.ntiles > 65535 * 1024) return MSA_ERR_UNSUPPORTED;
+    return MSA_OK;
 }
 
-extern "C" size_t msa_plan_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv, int qhead_per_kv) {
-    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk || !supported_qpk(qhead_per_kv))
-        return 0;
-    return sizeof(PlanHeader) + sizeof(PlanUnit) * (size_t)plan_capacity(B, Hkv, Sq, Skv, topk, qhead_per_kv);
-}
-
-extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, int topk, int blk_kv,
-                                 int qhead_per_kv, const int32_t *seqused, int32_t *row_ptr, int32_t *q_indices,
-                                 int32_t *qsplit, int32_t *split_counts, void *plan, size_t plan_bytes,
-                                 void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
-    if (!q2k || !row_ptr || !q_indices || !qsplit || !split_counts || !workspace) return MSA_ERR_INVALID_ARG;
-    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0) return MSA_ERR_INVALID_ARG;
-    if (blk_kv != kBlk || !supported_topk(topk) || !supported_qpk(qhead_per_kv)) return MSA_ERR_UNSUPPORTED;
-    if ((int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
-    CsrShape s = make_shape(B, Hkv, Sq, Skv, topk);
-    if (s.nblk > kMaxNblk) return MSA_ERR_UNSUPPORTED;
-    CsrWorkspace w = csr_workspace_layout(s);
-    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
-    if (plan && (plan_bytes < msa_plan_size(B, Hkv, Sq, Skv, topk, blk_kv, qhead_per_kv) || !aligned(plan, 16)))
-        return MSA_ERR_WORKSPACE;
-    char *ws = static_cast<char *>(workspace);
+// The CSR passes and the plan, once the shape (and, ragged, its sequence
+// table in the workspace) is set.
+int csr_launch(const CsrShape &s, const int32_t *q2k, int qhead_per_kv, const int32_t *seqused, int32_t *row_ptr,
+               int32_t *q_indices, int32_t *qsplit, int32_t *split_counts, void *plan, char *ws,
+               const CsrWorkspace &w, const int32_t *row_off, uint32_t *status_dev, cudaStream_t stream) {
     int32_t *tile_counts = reinterpret_cast<int32_t *>(ws + w.tile_counts);
-
     size_t mask_smem = sizeof(uint32_t) * 4 * (size_t)s.nblk;
     static bool smem_set = false;
     if (!smem_set) {
@@ -406,28 +544,35 @@ extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int
                                           sizeof(uint32_t) * 4 * kMaxNblk));
         smem_set = true;
     }
-    dim3 tgrid(s.ntiles, B, Hkv);
+    dim3 tgrid(s.ntiles, s.B, s.Hkv);
     csr_hist_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, split_counts, status_dev);
     MSA_LAUNCH_CHECK();
-    dim3 cgrid((unsigned)ceil_div(s.nblk, 32), B, Hkv);
+    if (s.seqs) {
+        // rows past the sequences' blocks (capacity above need) count 0
+        MSA_CUDA_TRY(cudaMemsetAsync(row_ptr, 0, sizeof(int32_t) * (size_t)(s.rows + 1) * s.Hkv, stream));
+    } else {
+        // row_ptr[h][0] = 0; the column scan writes every other entry
+        MSA_CUDA_TRY(cudaMemset2DAsync(row_ptr, sizeof(int32_t) * (s.rows + 1), 0, sizeof(int32_t), s.Hkv, stream));
+    }
+    dim3 cgrid((unsigned)ceil_div(s.nblk, 32), s.B, s.Hkv);
     csr_colscan_kernel<<<cgrid, dim3(32, (unsigned)std::min(32, s.ntiles)), 0, stream>>>(tile_counts, row_ptr, s);
     MSA_LAUNCH_CHECK();
-    // row_ptr[h][0] = 0, then inclusive scan of the row totals in [1, rows]
-    MSA_CUDA_TRY(cudaMemset2DAsync(row_ptr, sizeof(int32_t) * (s.rows + 1), 0, sizeof(int32_t), Hkv, stream));
-    segment_scan_kernel<<<Hkv, 1024, 0, stream>>>(row_ptr + 1, s.rows, s.rows + 1, 0, nullptr);
+    // inclusive scan of the row totals in [1, rows]
+    segment_scan_kernel<<<s.Hkv, 1024, 0, stream>>>(row_ptr + 1, s.rows, s.rows + 1, 0, nullptr);
     MSA_LAUNCH_CHECK();
     csr_scatter_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, row_ptr, q_indices,
                                                              qsplit);
     MSA_LAUNCH_CHECK();
     int tail_blocks = (int)std::min<int64_t>(ceil_div(s.cap, 256), 1024);
-    csr_tail_kernel<<<dim3(tail_blocks, Hkv), 256, 0, stream>>>(row_ptr, s, q_indices, qsplit);
+    csr_tail_kernel<<<dim3(tail_blocks, s.Hkv), 256, 0, stream>>>(row_ptr, s, q_indices, qsplit);
     MSA_LAUNCH_CHECK();
 
     if (plan) {
         PlanShape ps = make_plan_shape(s, qhead_per_kv);
+        ps.row_off = row_off;
         int32_t *ups = reinterpret_cast<int32_t *>(ws + w.units_per_row);
         int32_t *total = reinterpret_cast<int32_t *>(ws + w.total);
-        int64_t n = ps.nwaves * Hkv * s.rows;
+        int64_t n = ps.nwaves * s.Hkv * s.rows;
         int blocks = (int)ceil_div(n, 256);
         plan_count_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups);
         MSA_LAUNCH_CHECK();
@@ -435,10 +580,94 @@ extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int
         MSA_LAUNCH_CHECK();
         PlanHeader *ph = static_cast<PlanHeader *>(plan);
         PlanUnit *units = reinterpret_cast<PlanUnit *>(ph + 1);
-        int capacity = (int)plan_capacity(B, Hkv, Sq, Skv, topk, qhead_per_kv);
+        int capacity = (int)plan_capacity(s.rows, s.total_q, s.Hkv, s.topk, qhead_per_kv);
         plan_write_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups, total, ph, units, capacity,
                                                       qhead_per_kv, status_dev);
         MSA_LAUNCH_CHECK();
     }
     return MSA_OK;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" size_t msa_k2q_csr_workspace_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv) {
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk) return 0;
+    return csr_workspace_layout(make_shape(B, Hkv, Sq, Skv, topk), false).bytes;
+}
+
+extern "C" size_t msa_plan_size(int B, int Hkv, int Sq, int Skv, int topk, int blk_kv, int qhead_per_kv) {
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0 || blk_kv != kBlk || !supported_qpk(qhead_per_kv))
+        return 0;
+    const CsrShape s = make_shape(B, Hkv, Sq, Skv, topk);
+    return sizeof(PlanHeader) + sizeof(PlanUnit) * (size_t)plan_capacity(s.rows, s.total_q, Hkv, topk, qhead_per_kv);
+}
+
+extern "C" int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, int topk, int blk_kv,
+                                 int qhead_per_kv, const int32_t *seqused, int32_t *row_ptr, int32_t *q_indices,
+                                 int32_t *qsplit, int32_t *split_counts, void *plan, size_t plan_bytes,
+                                 void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
+    if (!q2k || !row_ptr || !q_indices || !qsplit || !split_counts || !workspace) return MSA_ERR_INVALID_ARG;
+    if (B <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0 || topk <= 0) return MSA_ERR_INVALID_ARG;
+    const CsrShape s = make_shape(B, Hkv, Sq, Skv, topk);
+    const int rc = check_csr_args(s, topk, blk_kv, qhead_per_kv);
+    if (rc != MSA_OK) return rc;
+    const CsrWorkspace w = csr_workspace_layout(s, false);
+    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
+    if (plan && (plan_bytes < msa_plan_size(B, Hkv, Sq, Skv, topk, blk_kv, qhead_per_kv) || !aligned(plan, 16)))
+        return MSA_ERR_WORKSPACE;
+    return csr_launch(s, q2k, qhead_per_kv, seqused, row_ptr, q_indices, qsplit, split_counts, plan,
+                      static_cast<char *>(workspace), w, nullptr, status_dev, stream);
+}
+
+extern "C" size_t msa_k2q_csr_varlen_workspace_size(int B, int Hkv, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                                    int total_rows, int topk, int blk_kv) {
+    if (B <= 0 || Hkv <= 0 || total_q <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || total_rows <= 0 ||
+        topk <= 0 || blk_kv != kBlk)
+        return 0;
+    return csr_workspace_layout(make_varlen_shape(B, Hkv, total_q, max_seqlen_q, max_seqlen_k, total_rows, topk),
+                                true)
+        .bytes;
+}
+
+extern "C" size_t msa_plan_varlen_size(int Hkv, int total_q, int total_rows, int topk, int blk_kv,
+                                       int qhead_per_kv) {
+    if (Hkv <= 0 || total_q <= 0 || total_rows <= 0 || topk <= 0 || blk_kv != kBlk || !supported_qpk(qhead_per_kv))
+        return 0;
+    return sizeof(PlanHeader) + sizeof(PlanUnit) * (size_t)plan_capacity(total_rows, total_q, Hkv, topk, qhead_per_kv);
+}
+
+extern "C" int msa_build_k2q_csr_varlen(const int32_t *q2k, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                        int B, int Hkv, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                        int total_rows, int topk, int blk_kv, int qhead_per_kv,
+                                        const int32_t *seqused, int32_t *row_ptr, int32_t *q_indices,
+                                        int32_t *qsplit, int32_t *split_counts, void *plan, size_t plan_bytes,
+                                        void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                                        cudaStream_t stream) {
+    if (!q2k || !cu_seqlens_q || !cu_seqlens_k || !row_ptr || !q_indices || !qsplit || !split_counts || !workspace)
+        return MSA_ERR_INVALID_ARG;
+    if (B <= 0 || Hkv <= 0 || total_q <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || total_rows <= 0 ||
+        topk <= 0)
+        return MSA_ERR_INVALID_ARG;
+    CsrShape s = make_varlen_shape(B, Hkv, total_q, max_seqlen_q, max_seqlen_k, total_rows, topk);
+    const int rc = check_csr_args(s, topk, blk_kv, qhead_per_kv);
+    if (rc != MSA_OK) return rc;
+    const CsrWorkspace w = csr_workspace_layout(s, true);
+    if (ws_bytes < w.bytes || !aligned(workspace, 256)) return MSA_ERR_WORKSPACE;
+    if (plan && (plan_bytes < msa_plan_varlen_size(Hkv, total_q, total_rows, topk, blk_kv, qhead_per_kv) ||
+                 !aligned(plan, 16)))
+        return MSA_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    // a query outside every kept sequence keeps 0 splits (O = 0, LSE = -inf)
+    MSA_CUDA_TRY(cudaMemsetAsync(split_counts, 0, sizeof(int32_t) * (size_t)total_q * Hkv, stream));
+    int4 *seqs = reinterpret_cast<int4 *>(ws + w.seqs);
+    int32_t *row_off = reinterpret_cast<int32_t *>(ws + w.row_off);
+    csr_seq_kernel<<<1, 1024, 0, stream>>>(cu_seqlens_q, cu_seqlens_k, B, total_q, total_rows, max_seqlen_q,
+                                           max_seqlen_k, seqs, row_off, status_dev);
+    MSA_LAUNCH_CHECK();
+    s.seqs = seqs;
+    return csr_launch(s, q2k, qhead_per_kv, seqused, row_ptr, q_indices, qsplit, split_counts, plan, ws, w, row_off,
+                      status_dev, stream);
 }

@@ -94,7 +94,9 @@ __global__ void __launch_bounds__(256) decode_union_kernel(DecParams p) {
     for (int i = tid; i < nwords; i += blockDim.x) bitmap[i] = 0u;
     for (int i = tid; i < p.maxu * p.wq; i += blockDim.x) mk[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < gi.nq * p.topk; i += blockDim.x) {
+    // dense mode (no q2k): every block below the used length, every query
+    for (int j = tid; !p.q2k && j < nvalid; j += blockDim.x) atomicOr(&bitmap[j >> 5], 1u << (j & 31));
+    for (int i = tid; p.q2k && i < gi.nq * p.topk; i += blockDim.x) {
         const int qi = i / p.topk, t = i % p.topk;
         const int32_t *sel = p.q2k + (((int64_t)gi.b * p.Hkv + gi.h) * p.Sq + gi.q0 + qi) * p.topk;
         int j = sel[t];
@@ -140,8 +142,13 @@ __global__ void __launch_bounds__(256) decode_union_kernel(DecParams p) {
     }
     __syncthreads();
     const int nu = s_nu;
-    // selection masks: position of each selected block by binary search
-    for (int i = tid; i < gi.nq * p.topk; i += blockDim.x) {
+    // selection masks: every query of the group (dense), or the position of
+    // each selected block by binary search
+    for (int i = tid; !p.q2k && i < nu * p.wq; i += blockDim.x) {
+        const int w = i % p.wq, n = min(32, gi.nq - 32 * w);
+        mk[i] = n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
+    }
+    for (int i = tid; p.q2k && i < gi.nq * p.topk; i += blockDim.x) {
         const int qi = i / p.topk;
         const int32_t *sel = p.q2k + (((int64_t)gi.b * p.Hkv + gi.h) * p.Sq + gi.q0 + qi) * p.topk;
         const int j = sel[i % p.topk];
@@ -605,11 +612,14 @@ int union_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int n
                     int max_pages, const int32_t *seqused_k, const int32_t *q2k, int B, int Sq, int Hq, int Hkv,
                     int D, int page_size, int topk, int causal, float softmax_scale, void *o, float *lse,
                     void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
-    if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !q2k || !o || !workspace) return MSA_ERR_INVALID_ARG;
+    // q2k == NULL: dense mode, every block of the sequence (topk is then unused)
+    if (!q2k) topk = max_pages;
+    if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !o || !workspace) return MSA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages <= 0 || topk <= 0 || Hq % Hkv)
         return MSA_ERR_INVALID_ARG;
     const int qpk = Hq / Hkv;
-    if (D != kD || page_size != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
+    if (D != kD || page_size != kBlk || (q2k && !supported_topk(topk)) || !supported_qpk(qpk))
+        return MSA_ERR_UNSUPPORTED;
     if (max_pages > kMaxPagesDecode || (int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
     if ((int64_t)num_pages * kBlk >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
@@ -647,8 +657,9 @@ int union_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int n
     MSA_CUDA_TRY(cudaMemsetAsync(p.counters, 0, sizeof(int32_t) * (size_t)d.groups, stream));
     const size_t usmem = sizeof(uint32_t) * (kMaxPagesDecode / 32) + sizeof(int32_t) * (size_t)d.maxu +
                          sizeof(uint32_t) * (size_t)d.maxu * d.wq;
+    if (usmem > 227 * 1024) return MSA_ERR_UNSUPPORTED;
     MSA_CUDA_TRY(cudaFuncSetAttribute(decode_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)(sizeof(uint32_t) * (kMaxPagesDecode / 32 + 128 * 32 * 5))));
+                                      (int)std::max<size_t>(usmem, sizeof(uint32_t) * (kMaxPagesDecode / 32 + 128 * 32 * 5))));
     MSA_CUDA_TRY(cudaFuncSetAttribute(decode_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kDecSmAlloc));
     decode_union_kernel<<<d.groups, 256, usmem, stream>>>(p);

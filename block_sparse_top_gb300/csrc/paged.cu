@@ -26,6 +26,7 @@
 // _decode_paged_kv_chunk (logical block j of sequence b is page
 // page_table[b][j]).
 #include <algorithm>
+#include <cstring>
 
 #include "tiles.h"
 
@@ -246,8 +247,9 @@ __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
         const int64_t u = off + e;
         const int start = (int)(u * a.qg);
         PlanUnit pu;
-        pu.head = x.h;
-        pu.row = x.b * a.max_pages + j;
+        pu.head = (int16_t)x.h;
+        pu.blk = (int16_t)j;
+        pu.seq = x.b;
         pu.start = start;
         pu.count = x.nq;
         a.units[u] = pu;
@@ -290,7 +292,7 @@ PagedWorkspace paged_workspace_layout(const PagedShape &d, int B, int Sq, int Hq
     w.unit_page = o;
     o = align_up(o + sizeof(int32_t) * (size_t)d.groups * d.maxu, 256);
     w.fwd = o;
-    w.fwd_bytes = fwd_workspace_layout(B, Sq, Hq, topk, kD).bytes;
+    w.fwd_bytes = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, kD).bytes;
     o = align_up(o + w.fwd_bytes, 256);
     w.bytes = o;
     return w;
@@ -311,18 +313,19 @@ extern "C" size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq
     return paged_workspace_layout(d, B, Sq, Hq, Hkv, topk).bytes;
 }
 
-extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
-                                         const int32_t *page_table, int max_pages, const int32_t *seqused_k,
-                                         const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
-                                         int topk, int causal, float softmax_scale, void *o, float *lse,
-                                         void *workspace, size_t ws_bytes, uint32_t *status_dev,
-                                         cudaStream_t stream) {
+namespace msa {
+// Paged decode over the tile pipeline for K/V pools of kv_format (bf16, or
+// e4m3 staged to bf16 on load).
+int paged_tiles_fwd(const void *q, const void *k_pool, const void *v_pool, int kv_format, int num_pages,
+                    const int32_t *page_table, int max_pages, const int32_t *seqused_k, const int32_t *q2k, int B,
+                    int Sq, int Hq, int Hkv, int D, int page_size, int topk, int causal, float softmax_scale, void *o,
+                    float *lse, void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
     if (!q || !k_pool || !v_pool || !page_table || !seqused_k || !q2k || !o || !workspace) return MSA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages <= 0 || topk <= 0 || Hq % Hkv)
         return MSA_ERR_INVALID_ARG;
     const int qpk = Hq / Hkv;
     if (D != kD || page_size != kBlk || !supported_topk(topk) || !supported_qpk(qpk)) return MSA_ERR_UNSUPPORTED;
-    if (max_pages > kMaxNblk || (int64_t)B * Sq >= (1 << 24)) return MSA_ERR_UNSUPPORTED;
+    if (max_pages > kMaxNblk || (int64_t)B * Sq >= (1 << 24) || Hkv > kMaxHkv) return MSA_ERR_UNSUPPORTED;
     if ((int64_t)num_pages * kBlk >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
         return MSA_ERR_INVALID_ARG;
@@ -355,9 +358,10 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     MSA_CUDA_TRY(launch_pdl(paged_scan_kernel, dim3(1), dim3(1024), 0, stream, a));
     MSA_CUDA_TRY(launch_pdl(paged_write_kernel, dim3(d.groups), dim3(128), 0, stream, a));
 
-    const FwdWorkspace fw = fwd_workspace_layout(B, Sq, Hq, topk, D);
+    const FwdWorkspace fw = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D);
     char *fws = ws + w.fwd;
     TcParams t;
+    memset(&t, 0, sizeof t);
     t.k_packed = static_cast<const uint8_t *>(k_pool);
     t.v_packed = static_cast<const uint8_t *>(v_pool);
     t.k_scales = nullptr;
@@ -365,10 +369,15 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     t.qsplit = a.qlist;
     t.plan = a.plan;
     t.units = a.units;
-    t.o_part = reinterpret_cast<__nv_bfloat16 *>(fws + fw.o_part);
+    t.o_part = fws + fw.o_part;
     t.stat_part = reinterpret_cast<float2 *>(fws + fw.stat_part);
+    t.part_dtype = MSA_PARTIAL_BF16;
+    t.inv_temp = 1.f;
     t.seqused = seqused_k;
     t.unit_page = a.unit_page;
+    t.cu_q = t.cu_k = nullptr;
+    t.kv_rows = (int64_t)num_pages * kBlk;
+    t.total_q = (int64_t)B * Sq;
     t.status = status_dev;
     t.B = B; t.Sq = Sq; t.Skv = max_pages * kBlk; t.Hq = Hq; t.Hkv = Hkv; t.qpk = qpk; t.topk = topk;
     t.nblk = max_pages;
@@ -376,8 +385,54 @@ extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, cons
     t.cap = 0;  // unit starts index qlist directly
     t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
     t.scale_log2 = t.scale * 1.4426950408889634f;
+    t.p_bound = 64.f;
     const int rc = tiles_launch(t, (int64_t)d.groups * d.maxu, q, k_pool, v_pool, (int64_t)num_pages * kBlk,
-                                MSA_KV_BF16, stream);
+                                kv_format, false, stream);
     if (rc != MSA_OK) return rc;
-    return msa_sparse_attn_combine(a.split_counts, B, Sq, Hq, Hkv, D, topk, o, lse, fws, w.fwd_bytes, stream);
+    return combine_launch(a.split_counts, (int64_t)B * Sq * Hkv, qpk, topk, o, lse, nullptr, fws, fw,
+                          MSA_PARTIAL_BF16, stream);
+}
+
+// The per-group union decode of decode.cu (dense mode when q2k is NULL) and its scratch.
+int union_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages, const int32_t *page_table,
+                    int max_pages, const int32_t *seqused_k, const int32_t *q2k, int B, int Sq, int Hq, int Hkv,
+                    int D, int page_size, int topk, int causal, float softmax_scale, void *o, float *lse,
+                    void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream);
+size_t union_paged_fwd_scratch(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
+}  // namespace msa
+
+extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
+                                         const int32_t *page_table, int max_pages, const int32_t *seqused_k,
+                                         const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                                         int topk, int causal, float softmax_scale, void *o, float *lse,
+                                         void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                                         cudaStream_t stream) {
+    if (!q2k) return MSA_ERR_INVALID_ARG;
+    return paged_tiles_fwd(q, k_pool, v_pool, MSA_KV_BF16, num_pages, page_table, max_pages, seqused_k, q2k, B, Sq,
+                           Hq, Hkv, D, page_size, topk, causal, softmax_scale, o, lse, workspace, ws_bytes,
+                           status_dev, stream);
+}
+
+extern "C" size_t msa_paged_attn_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages) {
+    if (topk == 0) return union_paged_fwd_scratch(B, Sq, Hq, Hkv, D, max_pages, max_pages);
+    return msa_sparse_attn_paged_fwd_workspace_size(B, Sq, Hq, Hkv, D, topk, max_pages);
+}
+
+extern "C" int msa_paged_attn_fwd(const void *q, const void *k_pool, const void *v_pool, int kv_format,
+                                  int num_pages, const int32_t *page_table, int max_pages, const int32_t *seqused_k,
+                                  const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size, int topk,
+                                  int causal, float softmax_scale, void *o, float *lse, void *workspace,
+                                  size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream) {
+    if (kv_format != MSA_KV_BF16 && kv_format != MSA_KV_FP8) return MSA_ERR_INVALID_ARG;
+    if (!q2k) {
+        // dense: every block of each sequence, by the per-group union decode (bf16 pools)
+        if (kv_format != MSA_KV_BF16) return MSA_ERR_UNSUPPORTED;
+        if ((int64_t)B * Sq >= (1 << 24) || Hkv > kMaxHkv) return MSA_ERR_UNSUPPORTED;
+        return union_paged_fwd(q, k_pool, v_pool, num_pages, page_table, max_pages, seqused_k, nullptr, B, Sq, Hq,
+                               Hkv, D, page_size, max_pages, causal, softmax_scale, o, lse, workspace, ws_bytes,
+                               status_dev, stream);
+    }
+    return paged_tiles_fwd(q, k_pool, v_pool, kv_format, num_pages, page_table, max_pages, seqused_k, q2k, B, Sq, Hq,
+                           Hkv, D, page_size, topk, causal, softmax_scale, o, lse, workspace, ws_bytes, status_dev,
+                           stream);
 }

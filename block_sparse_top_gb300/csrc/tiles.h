@@ -5,18 +5,55 @@
 
 namespace msa {
 
-// Split partials of a forward: topk slots per query head (layout in combine.cuh).
+// Split partials of a forward: topk slots per query head (layout in
+// combine.cuh), of the partial type; with `temp` also the temperature
+// statistics.
 struct FwdWorkspace {
-    size_t o_part, stat_part, bytes;
+    size_t o_part, stat_part, stat_temp, bytes;
 };
-FwdWorkspace fwd_workspace_layout(int B, int Sq, int Hq, int topk, int D);
+FwdWorkspace fwd_workspace_layout(int64_t total_q, int Hq, int topk, int D, int part_dtype = MSA_PARTIAL_BF16,
+                                  bool temp = false);
 
 // Multiprocessor count of the current device.
 int num_sms();
 
 // Launches the tile kernel for the plan in t (grid: at most one CTA per SM and
-// at most `capacity` CTAs); K and V are viewed as kv_tokens token rows.
+// at most `capacity` CTAs); K and V are viewed as kv_tokens token rows; temp
+// selects the instance that keeps the temperature statistics.
 int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void *k, const void *v, int64_t kv_tokens,
-                 int kv_format, cudaStream_t stream);
+                 int kv_format, bool temp, cudaStream_t stream);
+
+// LSE combine of a forward's split partials (workspace ws laid out as w) over
+// `groups` (query, KV head) pairs into o, lse (may be null) and, when the
+// workspace holds temperature statistics, lse_temp.
+int combine_launch(const int32_t *split_counts, int64_t groups, int qpk, int topk, void *o, float *lse,
+                   float *lse_temp, const char *ws, const FwdWorkspace &w, int part_dtype, cudaStream_t stream);
+
+// One launch function per tile-kernel instance, each compiled in a
+// translation unit of its own (tiles_*.cu) so that the build runs them in
+// parallel.
+#define MSA_TILE_INSTANCE(NAME)                                                                                   \
+    int NAME(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid, \
+             cudaStream_t stream)
+MSA_TILE_INSTANCE(launch_tiles_bf16);
+MSA_TILE_INSTANCE(launch_tiles_bf16_temp);
+MSA_TILE_INSTANCE(launch_tiles_nvfp4);
+MSA_TILE_INSTANCE(launch_tiles_nvfp4_temp);
+MSA_TILE_INSTANCE(launch_tiles_fp8);
+MSA_TILE_INSTANCE(launch_tiles_fp8_temp);
+MSA_TILE_INSTANCE(launch_tiles_paged);
+MSA_TILE_INSTANCE(launch_tiles_paged_fp8);
+
+// The launch of instance <KV_FORMAT, NKV, NQ, PAGED, TEMP> (used by tiles_*.cu).
+template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool TEMP>
+int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
+                 cudaStream_t stream) {
+    const size_t smem = tck::Layout<NKV, NQ>::BYTES;
+    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, TEMP>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, TEMP>, dim3(grid),
+                            dim3(tck::threads_for(PAGED)), smem, stream, mk, mv, mq, t));
+    return MSA_OK;
+}
 
 }  // namespace msa

@@ -60,11 +60,35 @@ extern "C" {
 #define MSA_STATUS_PLAN_OVERFLOW 0x8u /* the plan buffer could not hold the schedule (fatal) */
 #define MSA_STATUS_TIMEOUT 0x10u      /* a bounded wait inside a kernel gave up; output invalid (fatal) */
 #define MSA_STATUS_LAUNCH 0x20u       /* a kernel found its shared memory misaligned; nothing written (fatal) */
-#define MSA_STATUS_FATAL_MASK (MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH)
+#define MSA_STATUS_SHAPE 0x40u        /* cu_seqlens disagree with the declared sizes; sequence dropped (fatal) */
+#define MSA_STATUS_FATAL_MASK \
+    (MSA_STATUS_PAGE_RANGE | MSA_STATUS_PLAN_OVERFLOW | MSA_STATUS_TIMEOUT | MSA_STATUS_LAUNCH | MSA_STATUS_SHAPE)
 
-/* K/V storage formats of msa_sparse_attn_fwd */
+/* K/V storage formats of msa_sparse_attn_fwd (and, bf16 / fp8, of the paged decode pools) */
 #define MSA_KV_BF16 0
 #define MSA_KV_NVFP4 1
+#define MSA_KV_FP8 2 /* e4m3 bytes [..][Hkv][D], staged to bf16 on load (exact) for both MMAs */
+
+/* Storage type of the split partials (msa_fwd_options.partial_dtype) */
+#define MSA_PARTIAL_BF16 0
+#define MSA_PARTIAL_FP16 1
+#define MSA_PARTIAL_FP32 2
+
+/*
+ * Options of msa_sparse_attn_fwd_varlen; NULL selects the defaults (bf16
+ * partials, no temperature LSE).  Source: interface.py sparse_atten_func
+ * (partial_dtype, lse_temperature_scale, return_temperature_lse).
+ *   partial_dtype          MSA_PARTIAL_*: storage of each split's partial output.
+ *   lse_temperature_scale  T > 0, finite: used when lse_temperature != NULL.
+ *   lse_temperature        [total_q][Hq] fp32 device output or NULL: the LSE of
+ *                          the visible scores divided by T, log sum_t
+ *                          exp(scale q.k_t / T) (-inf for a row with no key).
+ */
+typedef struct msa_fwd_options {
+    int partial_dtype;
+    float lse_temperature_scale;
+    float *lse_temperature;
+} msa_fwd_options;
 
 /* Human-readable name of an MSA_* status code (static string). */
 const char *msa_status_string(int status);
@@ -125,6 +149,39 @@ int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, int t
                       void *workspace, size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream);
 
 /* =========================================================================
+ * Ragged batches: k->q CSR and work plan
+ * =========================================================================
+ * Source: interface.py sparse_atten_func and _validate_csr_varlen_inputs
+ * (cu_seqlens_q / cu_seqlens_k [B+1] int32 prefix sums, q2k
+ * [Hkv][total_q][topK], k2q_row_ptr [Hkv][total_rows+1]).
+ *
+ *   q2k          [Hkv][total_q][topk] int32, device; ids are blocks of the
+ *                query's own sequence (0 .. ceil(keys_b/blk_kv)-1), < 0 padding.
+ *   cu_seqlens_q, cu_seqlens_k  [B+1] int32, device: sequence b holds queries
+ *                cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and keys
+ *                cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.
+ *   total_q      rows of q2k (cu_seqlens_q[B] must equal it).
+ *   max_seqlen_q, max_seqlen_k  per-sequence maxima (size the builder's tiles).
+ *   total_rows   row capacity of row_ptr: >= sum_b ceil(keys_b / blk_kv).
+ *   seqused      [B] or NULL: used key count per sequence (<= keys_b).
+ * Outputs as msa_build_k2q_csr with rows r = row0_b + j, row0_b = sum over
+ * earlier sequences of ceil(keys/blk_kv); rows past the last sequence's are
+ * empty; query ids are global (cu_seqlens_q[b] + local index).  A sequence
+ * whose ranges decrease, start below 0, exceed total_q / total_rows or the
+ * maxima is dropped (its queries see nothing) and MSA_STATUS_SHAPE is set.
+ * Limits: total_q < 2^24, ceil(max_seqlen_k/blk_kv) <= 8192, B <= 65535.
+ */
+size_t msa_k2q_csr_varlen_workspace_size(int B, int Hkv, int total_q, int max_seqlen_q, int max_seqlen_k,
+                                         int total_rows, int topk, int blk_kv);
+size_t msa_plan_varlen_size(int Hkv, int total_q, int total_rows, int topk, int blk_kv, int qhead_per_kv);
+int msa_build_k2q_csr_varlen(const int32_t *q2k, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B,
+                             int Hkv, int total_q, int max_seqlen_q, int max_seqlen_k, int total_rows, int topk,
+                             int blk_kv, int qhead_per_kv, const int32_t *seqused, int32_t *row_ptr,
+                             int32_t *q_indices, int32_t *qsplit, int32_t *split_counts, void *plan,
+                             size_t plan_bytes, void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                             cudaStream_t stream);
+
+/* =========================================================================
  * (a3, a4, a6) block-sparse prefill forward, dense KV
  * =========================================================================
  * Source: interface.py sparse_atten_func / sparse_atten_nvfp4_kv_func and
@@ -135,6 +192,7 @@ int msa_build_k2q_csr(const int32_t *q2k, int B, int Hkv, int Sq, int Skv, int t
  *
  *   q       [B][Sq][Hq][D] bf16, device.
  *   k, v    kv_format MSA_KV_BF16: [B][Skv][Hkv][D] bf16.
+ *           kv_format MSA_KV_FP8: [B][Skv][Hkv][D] e4m3 bytes, staged to bf16 on load.
  *           kv_format MSA_KV_NVFP4: [B][Skv][Hkv][D/2] uint8, e2m1 codes, element
  *           2i in the low nibble; k_scales / v_scales [B][Skv][Hkv][D/16] e4m3
  *           bytes, one per 16 elements along D; value = e2m1 * e4m3 (no global scale).
@@ -170,6 +228,29 @@ int msa_sparse_attn_fwd_partial(const void *q, const void *k, const void *v, int
                                 uint32_t *status_dev, cudaStream_t stream);
 int msa_sparse_attn_combine(const int32_t *split_counts, int B, int Sq, int Hq, int Hkv, int D, int topk, void *o,
                             float *lse, const void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Ragged-batch forward: msa_sparse_attn_fwd over sequences of different
+ * lengths (the tiles and then the LSE combine, one call).
+ *   q       [total_q][Hq][D] bf16.
+ *   k, v    [total_k][Hkv][D] bf16 (MSA_KV_NVFP4: [total_k][Hkv][D/2] codes and
+ *           [total_k][Hkv][D/16] scales).
+ *   q_indices, qsplit, split_counts, plan: from msa_build_k2q_csr_varlen with
+ *           the same q2k, cu_seqlens and qhead_per_kv = Hq / Hkv.
+ *   cu_seqlens_q, cu_seqlens_k [B+1] device, as given to the builder; causal
+ *           masking is bottom-right per sequence (key t <= s + keys_b - queries_b).
+ *   opts    NULL or msa_fwd_options (partial dtype, temperature LSE).
+ *   o       [total_q][Hq][D] bf16; lse [total_q][Hq] fp32 or NULL.
+ *   workspace  msa_sparse_attn_fwd_varlen_workspace_size() bytes.
+ */
+size_t msa_sparse_attn_fwd_varlen_workspace_size(int total_q, int Hq, int topk, int D, const msa_fwd_options *opts);
+int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int kv_format, const void *k_scales,
+                               const void *v_scales, const int32_t *q_indices, const int32_t *qsplit,
+                               const int32_t *split_counts, const void *plan, const int32_t *cu_seqlens_q,
+                               const int32_t *cu_seqlens_k, int B, int total_q, int total_k, int Hq, int Hkv, int D,
+                               int blk_kv, int topk, int causal, float softmax_scale, const msa_fwd_options *opts,
+                               void *o, float *lse, void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                               cudaStream_t stream);
 
 /* =========================================================================
  * (a5) block-sparse paged decode
@@ -207,6 +288,24 @@ int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_p
                               const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,
                               int topk, int causal, float softmax_scale, void *o, float *lse, void *workspace,
                               size_t ws_bytes, uint32_t *status_dev, cudaStream_t stream);
+
+/*
+ * General paged decode: as msa_sparse_attn_paged_fwd, plus
+ *   kv_format  MSA_KV_BF16, or MSA_KV_FP8 (pools of e4m3 bytes, staged to bf16
+ *              on load, exact; sparse mode only);
+ *   q2k        NULL selects the dense mode (interface.py sparse_decode_atten_func
+ *              with q2k_indices = None): every block of each sequence, i.e.
+ *              causal attention over all seqused_k[b] keys; topk is then ignored.
+ * The dense mode runs the per-group union decode (an online softmax over each
+ * group's blocks, partials only where a group is split between CTAs), with the
+ * workspace msa_paged_attn_fwd_workspace_size(..., topk = 0, ...).
+ */
+size_t msa_paged_attn_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
+int msa_paged_attn_fwd(const void *q, const void *k_pool, const void *v_pool, int kv_format, int num_pages,
+                       const int32_t *page_table, int max_pages, const int32_t *seqused_k, const int32_t *q2k, int B,
+                       int Sq, int Hq, int Hkv, int D, int page_size, int topk, int causal, float softmax_scale,
+                       void *o, float *lse, void *workspace, size_t ws_bytes, uint32_t *status_dev,
+                       cudaStream_t stream);
 
 /*
  * msa_sparse_attn_paged_fwd without a workspace argument: the same paged

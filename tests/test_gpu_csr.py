@@ -28,11 +28,27 @@ def _check_equal(csr, ref):
     assert np.array_equal(csr.split_counts.cpu().numpy(), ref["split_counts"])
 
 
-def _check_plan(csr):
-    plan = csr.plan.cpu().view(torch.int32).numpy()
+def plan_units(plan: torch.Tensor, row_off):
+    """Decodes a plan buffer: header ints and units as (head, row, start, count),
+    row = row_off[seq] + block (units are {int16 head, int16 block, int32 seq,
+    int32 start, int32 count})."""
+    words = plan.cpu().view(torch.int32).numpy()
+    work = int(words[0])
+    raw = words[16:16 + 4 * work].reshape(-1, 4)
+    head = (raw[:, 0] & 0xFFFF).astype(np.int64)
+    blk = (raw[:, 0] >> 16).astype(np.int64)
+    seq = raw[:, 1].astype(np.int64)
+    rows = np.asarray(row_off, dtype=np.int64)[seq] + blk
+    return words, [(int(h), int(r), int(st), int(c)) for h, r, st, c in zip(head, rows, raw[:, 2], raw[:, 3])]
+
+
+def _check_plan(csr, row_off=None):
+    if row_off is None:  # uniform batch: sequence b owns rows b*nblk ..
+        nblk = -(-csr.Skv // 128)
+        row_off = [b * nblk for b in range(csr.B)]
+    plan, units = plan_units(csr.plan, row_off)
     work, cap, qpk, qpu = plan[:4]
     assert work <= cap and qpk == csr.qhead_per_kv
-    units = plan[16:16 + 4 * work].reshape(-1, 4)
     rp = csr.row_ptr.cpu().numpy()
     rows = rp.shape[1] - 1
     covered = np.zeros((csr.Hkv, rows), dtype=np.int64)
