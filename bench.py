@@ -213,7 +213,7 @@ def workload_config(spec: synth.PrefillSpec) -> dict:
     part_gb = spec.B * spec.Sq * spec.topk * spec.Hq * (spec.D * 2 + 8) / 1e9
     return {"workload": spec.name, "B": spec.B, "Sq": spec.Sq, "Skv": spec.Skv, "Hkv": spec.Hkv,
             "qhead_per_kv": spec.qpk, "topk": spec.topk, "D": spec.D, "blk_kv": 128, "causal": spec.causal,
-            "pattern": spec.pattern, "per_rank_problem": "independent (seed + rank)",
+            "pattern": spec.pattern, "kv_format": spec.kv_format, "per_rank_problem": "independent (seed + rank)",
             "l2": f"inputs larger than L2 (Q {q_mib:.0f} MiB; split partials {part_gb:.1f} GB per step); "
                   "no flush"}
 
@@ -301,6 +301,9 @@ WORKLOADS = {
     # smaller case of the same kernel for ncu captures (partials ~1.1 GB on the device)
     "causal_sink_16k_1kv": synth.PrefillSpec("causal_sink_16k_1kv", B=1, Sq=16384, Skv=16384, Hkv=1, qpk=16,
                                              topk=16, causal=True, pattern="sink"),
+    # smaller case of the NVFP4 instance (qhead_per_kv 2, as the 384K NVFP4 workload) for ncu captures
+    "causal_sink_64k_qpk2_nvfp4": synth.PrefillSpec("causal_sink_64k_qpk2_nvfp4", B=1, Sq=65536, Skv=65536, Hkv=1,
+                                                    qpk=2, topk=16, causal=True, pattern="sink", kv_format="nvfp4"),
 }
 
 
@@ -312,6 +315,13 @@ def run_ours(args, world, rank):
     spec_r = synth.PrefillSpec(**{**spec.__dict__, "seed": spec.seed + rank})
     x = synth.make_prefill_inputs(spec_r, device=dev)
     flops = prefill_flops(spec_r, x["q2k"])
+    kvkw = {}
+    kv_bf16 = {"k": x["k"], "v": x["v"]}  # the oracle's timing sample runs on bf16 K/V
+    if spec.kv_format == "nvfp4":
+        # NVFP4 workloads: K/V (and their scales) stored as the library's encoder writes them
+        x["k"], x["k_scales"] = msa.nvfp4_quantize(x["k"])
+        x["v"], x["v_scales"] = msa.nvfp4_quantize(x["v"])
+        kvkw = {"kv_format": "nvfp4"}
     nominal = 4.0 * spec.D * spec.Hq * spec.Sq * spec.B * spec.topk * 128
     csr, csr_ws = msa.csr_buffers(spec.B, spec.Hkv, spec.Sq, spec.Skv, spec.topk, spec.qpk, dev)
     fwd_ws = msa.fwd_workspace(spec.B, spec.Sq, spec.Hq, spec.topk, dev)
@@ -325,7 +335,8 @@ def run_ours(args, world, rank):
         msa.build_k2q_csr(x["q2k"], spec.Skv, spec.qpk, out=csr, workspace=csr_ws)
         if ev is not None:
             ev[1].record(stream)
-        msa.sparse_attn_fwd_partial(x["q"], x["k"], x["v"], csr, causal=True, workspace=fwd_ws)
+        msa.sparse_attn_fwd_partial(x["q"], x["k"], x["v"], csr, causal=True, workspace=fwd_ws,
+                                    k_scales=x.get("k_scales"), v_scales=x.get("v_scales"), **kvkw)
         if ev is not None:
             ev[2].record(stream)
         msa.sparse_attn_combine(csr, spec.Hq, out, lse, fwd_ws)
@@ -389,7 +400,8 @@ def run_ours(args, world, rank):
         with torch.cuda.stream(comp):
             msa.build_k2q_csr(dev_in[s]["q2k"], spec.Skv, spec.qpk, out=csr, workspace=csr_ws)
             msa.sparse_attn_fwd(dev_in[s]["q"], dev_in[s]["k"], dev_in[s]["v"], csr, causal=True, out=dev_out[s][0],
-                                lse=dev_out[s][1], workspace=fwd_ws)
+                                lse=dev_out[s][1], workspace=fwd_ws, k_scales=dev_in[s].get("k_scales"),
+                                v_scales=dev_in[s].get("v_scales"), **kvkw)
             ev_comp[s].record(comp)
         down.wait_event(ev_comp[s])
         with torch.cuda.stream(down):
@@ -439,7 +451,7 @@ def run_ours(args, world, rank):
                      "peak_source": f"{peak_src} bf16 {'sustained' if long_region else 'burst'}",
                      "kernel_source_hash": khash},
     }
-    x_cpu = {k_: v_.cpu() for k_, v_ in x.items()}
+    x_cpu = {k_: v_.cpu() for k_, v_ in {**x, **kv_bf16}.items() if k_ in ("q", "k", "v", "q2k")}
     del x, csr, csr_ws, fwd_ws, out, lse, host, out_h, lse_h, dev_in, dev_out
     torch.cuda.empty_cache()
     if not args.no_configs:
@@ -620,6 +632,8 @@ def main():
     ap.add_argument("--decode-L", type=int, nargs="*", default=list(synth.DECODE_SWEEP_L))
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the paged-decode sweep (for profiling its kernels); prints its JSON")
     ap.add_argument("--config-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
@@ -632,6 +646,12 @@ def main():
             return
         res = run_reference(args, world, rank)
         print(json.dumps(res), flush=True)
+        return
+    if args.decode_only:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        peaks, peak_src = load_peaks()
+        if rank == 0:
+            print(json.dumps({"decode": decode_sweep(args, dev, peaks, peak_src)}), flush=True)
         return
     res = run_ours(args, world, rank)
     if rank == 0:

@@ -174,11 +174,13 @@ def build_k2q_csr_varlen(q2k: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqle
     return out
 
 
-def _opts(partial_dtype: int, lse_temperature_scale: float, lse_temperature: Optional[torch.Tensor]):
+def _opts(partial_dtype: int, lse_temperature_scale: float, lse_temperature: Optional[torch.Tensor],
+          qk_fp8: bool = False):
     o = FwdOptions()
     o.partial_dtype = int(partial_dtype)
     o.lse_temperature_scale = float(lse_temperature_scale)
     o.lse_temperature = None if lse_temperature is None else lse_temperature.data_ptr()
+    o.qk_fp8 = int(bool(qk_fp8))
     return o
 
 
@@ -189,8 +191,15 @@ def sparse_attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cs
                            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                            stream=None):
-    """msa_sparse_attn_fwd_varlen: q [total_q,Hq,D], k/v [total_k,Hkv,D] -> (O, LSE[, temperature LSE])."""
-    _need(q, torch.bfloat16, "q")
+    """msa_sparse_attn_fwd_varlen: q [total_q,Hq,D], k/v [total_k,Hkv,D] -> (O, LSE[, temperature LSE]).
+
+    q of e4m3 bytes (float8_e4m3fn or uint8) with kv_format "fp8" runs S = Q K^T as an fp8 MMA."""
+    qk_fp8 = q.dtype in (torch.uint8, _FP8)
+    if qk_fp8:
+        if not (q.is_cuda and q.is_contiguous()) or kv_format != "fp8":
+            raise ValueError("e4m3 q needs a contiguous CUDA tensor and kv_format 'fp8'")
+    else:
+        _need(q, torch.bfloat16, "q")
     total_q, Hq, D = q.shape
     fmt = _kv_format(kv_format, k, v, k_scales, v_scales)
     total_k, Hkv = k.shape[0], k.shape[1]
@@ -201,7 +210,7 @@ def sparse_attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cs
     lse_t = None
     if lse_temperature_scale is not None:
         lse_t = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
-    opts = _opts(partial_dtype, 1.0 if lse_temperature_scale is None else lse_temperature_scale, lse_t)
+    opts = _opts(partial_dtype, 1.0 if lse_temperature_scale is None else lse_temperature_scale, lse_t, qk_fp8)
     L = lib()
     if workspace is None:
         n = L.msa_sparse_attn_fwd_varlen_workspace_size(total_q, Hq, csr.topk, D, ctypes.byref(opts))

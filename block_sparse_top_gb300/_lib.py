@@ -41,7 +41,7 @@ MSA_PARTIAL_FP32 = 2
 class FwdOptions(ctypes.Structure):
     """msa_fwd_options (include/msa.h)."""
     _fields_ = [("partial_dtype", ctypes.c_int), ("lse_temperature_scale", ctypes.c_float),
-                ("lse_temperature", ctypes.c_void_p)]
+                ("lse_temperature", ctypes.c_void_p), ("qk_fp8", ctypes.c_int)]
 
 
 class MsaError(RuntimeError):
@@ -67,7 +67,13 @@ def lib():
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m block_sparse_top_gb300.build` "
                            "(or __graft_entry__.build()); there is no CPU fallback")
-    L = ctypes.CDLL(LIB_PATH)
+    _lib = load(LIB_PATH)
+    return _lib
+
+
+def load(path: str):
+    """Opens a build of the library at `path` with the C signatures of include/msa.h."""
+    L = ctypes.CDLL(path)
     P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     L.msa_status_string.argtypes = [I]
     L.msa_status_string.restype = ctypes.c_char_p
@@ -112,7 +118,6 @@ def lib():
     L.msa_paged_attn_fwd.restype = I
     L.msa_nvfp4_quantize.argtypes = [P, I64, I, P, P, P]
     L.msa_nvfp4_quantize.restype = I
-    _lib = L
     return L
 
 

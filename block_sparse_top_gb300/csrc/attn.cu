@@ -46,12 +46,18 @@ int num_sms() {
 // launches the tile kernel for t, one CTA per SM, at most `capacity` CTAs
 // (the plan's unit capacity).
 int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void *k, const void *v, int64_t kv_tokens,
-                 int kv_format, bool temp, cudaStream_t stream) {
+                 int kv_format, bool opts, cudaStream_t stream, bool qk_fp8) {
     int grid = (int)std::min<int64_t>(capacity, (int64_t)num_sms());
     if (grid < 1) grid = 1;
     CUtensorMap mk, mv, mq;
     memset(&mk, 0, sizeof mk);
     memset(&mv, 0, sizeof mv);
+    if (qk_fp8) {
+        // e4m3 Q and K by TMA, e4m3 V staged by the dequantising warp
+        if (!make_q8_map(&mq, q, t.total_q * t.Hq, t.qpk) || !make_k8_map(&mk, k, t.Hkv, kv_tokens))
+            return MSA_ERR_CUDA;
+        return opts ? launch_tiles_qk8_opts(mk, mv, mq, t, grid, stream) : launch_tiles_qk8(mk, mv, mq, t, grid, stream);
+    }
     const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, t.total_q * t.Hkv, t.qpk)
                                  : make_q_map(&mq, q, t.total_q * t.Hq, 1);
     if (!q_ok) return MSA_ERR_CUDA;
@@ -61,15 +67,15 @@ int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void 
         // one chunk, its K/V block from HBM; a group's consecutive units share
         // one Q tile): three K/V stages and one Q
         if (t.unit_page) return launch_tiles_paged(mk, mv, mq, t, grid, stream);
-        return temp ? launch_tiles_bf16_temp(mk, mv, mq, t, grid, stream)
+        return opts ? launch_tiles_bf16_opts(mk, mv, mq, t, grid, stream)
                     : launch_tiles_bf16(mk, mv, mq, t, grid, stream);
     }
     // NVFP4 / FP8: the dequantising warp reads K and V itself (no K/V maps)
     if (kv_format == MSA_KV_FP8) {
         if (t.unit_page) return launch_tiles_paged_fp8(mk, mv, mq, t, grid, stream);
-        return temp ? launch_tiles_fp8_temp(mk, mv, mq, t, grid, stream) : launch_tiles_fp8(mk, mv, mq, t, grid, stream);
+        return opts ? launch_tiles_fp8_opts(mk, mv, mq, t, grid, stream) : launch_tiles_fp8(mk, mv, mq, t, grid, stream);
     }
-    return temp ? launch_tiles_nvfp4_temp(mk, mv, mq, t, grid, stream)
+    return opts ? launch_tiles_nvfp4_opts(mk, mv, mq, t, grid, stream)
                 : launch_tiles_nvfp4(mk, mv, mq, t, grid, stream);
 }
 
@@ -111,8 +117,15 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const void *__restrict_
 // ...; thread 0 copies each group's split partials (n x 4 KB, contiguous) and
 // statistics (n x 128 B) into a ring of kRingBufs shared-memory buffers with
 // bulk copies, kRingBufs groups ahead, so that the bytes in flight do not live
-// in registers; the 256 threads merge from shared memory (same arithmetic as
-// combine_kernel) and release the buffer warp by warp.
+// in registers.  Each group is then merged in two phases:
+//   1. thread (head j, split s): its split's weight w = exp(a_s - A_j), with
+//      A_j the max over the group's splits of head j and den_j = sum w l_s
+//      (16-lane shuffles), into a shared weight table; lane s = 0 writes the
+//      LSE A_j + ln den_j;
+//   2. thread (8-dim chunk c, head j): O = sum_s w_s U_s / den_j over its
+//      pieces, in packed f32x2 FMAs,
+// so each weight is computed once, not once per piece.  The table is double
+// buffered, so one CTA barrier per group separates the phases.
 constexpr int kRingBufs = 3;
 __host__ __device__ constexpr uint32_t ring_buf_bytes(int topk) { return (uint32_t)topk * (4096u + 128u); }
 template <int PD>
@@ -129,8 +142,11 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
     auto full = [&](int b) { return bars + 8u * b; };
     auto empty = [&](int b) { return bars + 8u * (kRingBufs + b); };
     __shared__ int abort_flag_s;
+    __shared__ float wts[2][16][17];  // [parity][head][split] weights
+    __shared__ float inv_den[2][16];
     volatile int *abort_flag = &abort_flag_s;
     const int t = threadIdx.x, c = t >> 4, j = t & 15, lane = t & 31;
+    const int jw = t >> 4, sw = t & 15;  // phase 1: head, split
     if (t == 0) {
         for (int b = 0; b < kRingBufs; ++b) {
             tc::mbar_init(full(b), 1);
@@ -167,21 +183,64 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
         for (; issued < kRingBufs && blockIdx.x + issued * G < groups && ok; ++issued) ok = issue(issued);
     for (; blockIdx.x + k * G < groups; ++k) {
         const int64_t grp = blockIdx.x + k * G;
-        const int b = (int)(k % kRingBufs);
+        const int b = (int)(k % kRingBufs), par = (int)(k & 1);
         ok = tc::mbar_wait(full(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status, MSA_STATUS_TIMEOUT);
-        if (!__all_sync(0xffffffffu, ok)) break;
+        // the whole CTA leaves together (the phases below meet at a barrier):
+        // on a timed-out wait here or in thread 0's copy issue
+        if (!__syncthreads_and(ok && *abort_flag == 0)) break;
         int n = split_counts[grp];
         n = n < topk ? n : topk;
-        uint4 out;
-        float l;
-        combine_piece<16, PD, 16, true>(smem + b * bb, reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096),
-                                        0, n, topk, 16, c, j, out, l);
+        const uint4 *up = reinterpret_cast<const uint4 *>(smem + b * bb);
+        const float2 *stp = reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096);
+        // phase 1: weights of (head jw, split sw), max and sum over the 16 splits
+        {
+            const float2 st = sw < n ? stp[sw * 16 + jw] : make_float2(-INFINITY, 0.f);
+            const float a = isfinite(st.x) ? st.x : -INFINITY;
+            float A = a;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, o));
+            const float w = (a == -INFINITY) ? 0.f : __expf(a - A);
+            float den = w * st.y;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            wts[par][jw][sw] = w;
+            if (sw == 0) {
+                inv_den[par][jw] = den > 0.f ? 1.f / den : 0.f;
+                const int64_t orow = grp * 16 + jw;
+                if (lse) lse[orow] = den > 0.f ? A + logf(den) : -INFINITY;
+                if (lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, jw);
+            }
+        }
+        __syncthreads();
+        // phase 2: the piece (chunk c, head j)
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int sp = 0; sp < 16; ++sp) {
+            if (sp >= n) break;
+            const uint4 u = up[(sp * 16 + c) * 16 + j];
+            const float w = wts[par][j][sp];
+            const float2 w2 = make_float2(w, w);
+            const uint32_t words[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 v;
+                if (PD == MSA_PARTIAL_FP16) {
+                    v = __half22float2(*reinterpret_cast<const __half2 *>(&words[i]));
+                } else {
+                    v = make_float2(bf16_lo(words[i]), bf16_hi(words[i]));
+                }
+                acc[i] = __ffma2_rn(v, w2, acc[i]);
+            }
+        }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(empty(b));
-        const int64_t orow = grp * 16 + j;
-        o[orow * 16 + c] = out;
-        if (c == 0 && lse) lse[orow] = l;
-        if (c == 0 && lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, j);
+        if (lane == 0) tc::mbar_arrive(empty(b));  // this warp is done with the buffer
+        const float inv = inv_den[par][j];
+        uint4 out;
+        out.x = pack_bf16x2(acc[0].x * inv, acc[0].y * inv);
+        out.y = pack_bf16x2(acc[1].x * inv, acc[1].y * inv);
+        out.z = pack_bf16x2(acc[2].x * inv, acc[2].y * inv);
+        out.w = pack_bf16x2(acc[3].x * inv, acc[3].y * inv);
+        o[(grp * 16 + j) * 16 + c] = out;
         if (t == 0 && blockIdx.x + (k + kRingBufs) * G < groups && ok) {
             ok = issue(k + kRingBufs);
             if (ok) ++issued;
@@ -382,6 +441,8 @@ extern "C" int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const vo
     if (total_q >= (1 << 24) || Hkv > kMaxHkv) return MSA_ERR_UNSUPPORTED;
     const int orc = check_options(opts);
     if (orc != MSA_OK) return orc;
+    const bool qk_fp8 = opts && opts->qk_fp8;
+    if (qk_fp8 && kv_format != MSA_KV_FP8) return MSA_ERR_INVALID_ARG;
     const int part_dtype = opts ? opts->partial_dtype : MSA_PARTIAL_BF16;
     float *lse_temp = opts ? opts->lse_temperature : nullptr;
     const FwdWorkspace w = fwd_workspace_layout(total_q, Hq, topk, D, part_dtype, lse_temp != nullptr);
@@ -399,11 +460,12 @@ extern "C" int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const vo
     t.kv_rows = total_k;
     t.total_q = total_q;
     t.part_dtype = part_dtype;
-    // fp16 partials keep P <= 1 (the stored half-row P is rescaled whenever
-    // the row max grows), so that the unnormalised partial stays in range
-    t.p_bound = part_dtype == MSA_PARTIAL_FP16 ? 0.f : 64.f;
-    if (lse_temp) t.inv_temp = 1.f / opts->lse_temperature_scale;
-    int rc = tiles_launch(t, (int64_t)num_sms(), q, k, v, total_k, kv_format, lse_temp != nullptr, stream);
+    if (lse_temp) {
+        t.temp_on = 1;
+        t.inv_temp = 1.f / opts->lse_temperature_scale;
+    }
+    const bool use_opts = lse_temp != nullptr || part_dtype != MSA_PARTIAL_BF16;
+    int rc = tiles_launch(t, (int64_t)num_sms(), q, k, v, total_k, kv_format, use_opts, stream, qk_fp8);
     if (rc != MSA_OK) return rc;
     // the combine's groups are (query, KV head) pairs over all sequences
     return combine_launch(split_counts, (int64_t)total_q * Hkv, qpk, topk, o, lse, lse_temp,

@@ -50,9 +50,10 @@ struct TcParams {
     const PlanUnit *units;
     void *o_part;                         // split partials (part_dtype), layout in combine.cuh
     float2 *stat_part;                    // split statistics, layout in combine.cuh
-    float2 *stat_temp;                    // temperature statistics (instances with TEMP), same layout
-    int part_dtype;                       // MSA_PARTIAL_*: storage of the split partials
-    float inv_temp;                       // 1 / lse_temperature_scale (TEMP)
+    float2 *stat_temp;                    // temperature statistics (OPTS instances, temp_on), same layout
+    int part_dtype;                       // MSA_PARTIAL_*: storage of the split partials (OPTS instances)
+    int temp_on;                          // 1: keep the temperature statistics (OPTS instances)
+    float inv_temp;                       // 1 / lse_temperature_scale
     // paged KV (decode): per-sequence used length and each unit's physical
     // page (-1: invalid entry, the unit's keys are skipped); null otherwise
     const int32_t *seqused;
@@ -65,8 +66,8 @@ struct TcParams {
     int64_t cap;
     int64_t kv_rows;  // token rows of the K/V arrays (bound of the dequant loads)
     int64_t total_q;  // query rows of Q (all sequences)
-    // prefill softmax: largest log2 of a P value before the stored half-row P
-    // is rescaled to a new row max (bf16 / fp32 partials: 64; fp16: 0)
+    // paged decode: largest log2 of a P value against a row's reference max
+    // before the row's accumulated O is rescaled to a new reference
     float p_bound;
     float scale, scale_log2;
 };
@@ -85,11 +86,12 @@ constexpr int threads_for(bool paged) { return paged ? kThreads : kThreads + 128
 constexpr int kRing = 4;
 constexpr uint32_t kRingEntry = 32 + 128 * 4;
 
-// Shared memory of a kernel with NKV K/V stages and NQ Q stages (32 KB tiles):
+// Shared memory of a kernel with NKV K/V stages and NQ Q stages of KS / QS
+// bytes (bf16 K and Q tiles 32 KB, e4m3 ones 16 KB; V tiles are bf16, 32 KB):
 // K [NKV] | V [NKV] | Q [NQ] | mbarriers | TMEM slot | abort flag | chunk ring.
-template <int NKV, int NQ>
+template <int NKV, int NQ, uint32_t KS = 32768u, uint32_t QS = 32768u>
 struct Layout {
-    static constexpr uint32_t K = 0, V = NKV * 32768u, Q = 2u * NKV * 32768u, BAR = Q + NQ * 32768u;
+    static constexpr uint32_t K = 0, V = NKV * KS, Q = V + NKV * 32768u, BAR = Q + NQ * QS;
     enum : int {
         KV_FULL = 0,
         KV_EMPTY = NKV,
@@ -112,6 +114,11 @@ struct Layout {
 };
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescS8 = tc::idesc_e4m3_f32(128, 128);
+
+// K/V format of the instance that keeps Q and K in e4m3 (S = Q K^T as an fp8
+// MMA) and stages V to bf16 (not a value of the public kv_format argument)
+constexpr int kKvQk8 = 3;
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, 0, 1);
 
 struct Unit {
@@ -140,14 +147,20 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
 // one Q tile, and the softmax holds a whole S row in registers (one
 // tensor-memory load, 168 registers) instead of reading it in halves (133) --
 // the shorter chain suits decode, where one warp's rows gate each K/V stage.
-// TEMP (prefill): each split also keeps the row sum of 2^(x / T), x = (S - m)
-// scale_log2, and its statistics (m scale / T, that sum), for the temperature LSE.
-template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool TEMP>
+// OPTS (prefill): the instance that serves the forward's options at run
+// time -- the partials' storage type (bf16, fp16 or fp32) and, with temp_on,
+// the row sum of 2^(x / T), x = (S - m) scale_log2, with its statistics (m
+// scale / T, that sum) for the temperature LSE.  Without OPTS the epilogue
+// stores bf16 and nothing else: the run-time type switch alone cost the
+// 32K causal workload's tiles a tenth of their time.
+template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool OPTS>
 __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
     using namespace tck;
-    using L = Layout<NKV, NQ>;
+    constexpr bool QK8 = KV_FORMAT == kKvQk8;
+    constexpr uint32_t KS = QK8 ? 16384u : 32768u, QS = QK8 ? 16384u : 32768u;  // K and Q stage bytes
+    using L = Layout<NKV, NQ, KS, QS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t *const gbase = smem_raw;
@@ -162,7 +175,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
 
     if (tid == 0) {
         for (int i = 0; i < NKV; ++i) {
-            tc::mbar_init(bar(L::KV_FULL + i), KV_FORMAT == MSA_KV_BF16 ? 1 : 32);
+            // arrivals: the loader's copy (bf16 K and V; e4m3 K), the
+            // dequantising warp's 32 lanes (NVFP4 / FP8 K and V; e4m3 V)
+            tc::mbar_init(bar(L::KV_FULL + i), KV_FORMAT == MSA_KV_BF16 ? 1 : (QK8 ? 33 : 32));
             tc::mbar_init(bar(L::KV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -193,6 +208,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             tc::tma_prefetch_desc(&tm_k);
             tc::tma_prefetch_desc(&tm_v);
         }
+        if (QK8) tc::tma_prefetch_desc(&tm_k);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -219,8 +235,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         // chunk and the chunk's Q rows.
         int ci = 0, ui = 0, c = 0;
         int qn = 0, q_key = -1;  // Q tiles loaded; resident group (paged): first query * Hkv + head
-        int kv_armed[NKV];
+        int kv_armed[NKV], q_armed[NQ];  // phase parity of each stage's last copy, -1: none
         for (int i = 0; i < NKV; ++i) kv_armed[i] = -1;
+        for (int i = 0; i < NQ; ++i) q_armed[i] = -1;
         bool ok = true;
         const uint64_t keep = tc::l2_policy_evict_last();  // gather4 Q rows
         for (int u = u_begin; u < u_end && ok;) {
@@ -247,7 +264,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(L::RING_EMPTY + slot));
             const int kb = ui % NKV;
-            if (c == 0 && KV_FORMAT == MSA_KV_BF16) {
+            if (c == 0 && (KV_FORMAT == MSA_KV_BF16 || QK8)) {
                 if (lane == 0 && ui >= NKV)
                     ok = tc::mbar_wait(bar(L::KV_EMPTY + kb), ((ui / NKV) - 1) & 1, abort_flag, p.status,
                                        MSA_STATUS_TIMEOUT);
@@ -257,18 +274,31 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 // a ragged batch, or dense [B][Skv]
                 const int row = p.unit_page ? x.page * kBlk : (p.cu_k ? seq_k0 : x.b * p.Skv) + x.tok0;
                 const bool copy = !p.unit_page || x.page >= 0;
-                if (lane == 0) {
+#ifdef MSA_TEST_DROP_KV_ARRIVAL
+                // test build only: CTA 0 never signals its first unit's K/V, so
+                // the MMA warp's bounded wait runs out and the CTA aborts
+                const bool drop = blockIdx.x == 0 && ui == 0;
+#else
+                constexpr bool drop = false;
+#endif
+                if (lane == 0 && !drop) {
                     if (copy)
-                        tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), 65536);
+                        tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), QK8 ? 16384u : 65536u);
                     else
                         tc::mbar_arrive(bar(L::KV_FULL + kb));  // invalid page: no copy, keys masked
                     kv_armed[kb] = (ui / NKV) & 1;
                 }
                 __syncwarp();
-                // lane 0 copies K, lane 1 V, in one instruction
-                if (copy && lane < 2)
-                    tc::tma_load_4d(base + (lane ? L::V : L::K) + kb * 32768, lane ? &tm_v : &tm_k,
-                                    bar(L::KV_FULL + kb), 0, row, 0, x.h);
+                if constexpr (QK8) {
+                    // e4m3 K by TMA (V is staged to bf16 by the dequantising warp)
+                    if (copy && lane == 0 && !drop)
+                        tc::tma_load_3d(base + L::K + kb * KS, &tm_k, bar(L::KV_FULL + kb), 0, row, x.h);
+                } else {
+                    // lane 0 copies K, lane 1 V, in one instruction
+                    if (copy && lane < 2 && !drop)
+                        tc::tma_load_4d(base + (lane ? L::V : L::K) + kb * 32768, lane ? &tm_v : &tm_k,
+                                        bar(L::KV_FULL + kb), 0, row, 0, x.h);
+                }
             }
             // Paged decode: a unit is one chunk holding all queries of its group
             // (rows of queries that did not select the block are masked), so
@@ -285,6 +315,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
+                q_armed[qs] = (qn / NQ) & 1;
                 ++qn;
             }
             // The chunk's 128 Q rows (row R = query R / qpk of the chunk, head
@@ -295,11 +326,35 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             // qpk >= 8 loads only the chunk's real queries (padding rows keep
             // stale data; their keys are all masked, so they give P = 0);
             // gather4 rows of padding repeat the chunk's first query.
-            const uint32_t qt = base + L::Q + qs * 32768;
+            const uint32_t qt = base + L::Q + qs * QS;
             const int nq = min(qc, x.count - c * qc);
             if (load_q && lane == 0)
-                tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs), p.qpk >= 8 ? (uint32_t)(nq * p.qpk * 256) : 32768u);
+                tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs),
+                                          p.qpk >= 8 ? (uint32_t)(nq * p.qpk * (QK8 ? 128 : 256)) : QS);
             if (!load_q) {
+            } else if (QK8) {
+                // e4m3 rows of 128 bytes: one 4D box per query (qpk >= 8: its
+                // row octets 1024 bytes apart), or four rows per gather4
+                if (p.qpk >= 8) {
+                    if (lane < nq)
+                        tc::tma_load_4d(qt + (uint32_t)(lane * p.qpk * 128), &tm_q, bar(L::Q_FULL + qs), 0, 0, 0,
+                                        ids[0] * p.Hkv + x.h);
+                } else {
+                    int r[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int R = 4 * lane + t, qi = R / p.qpk;
+                        const int g0 = __shfl_sync(0xffffffffu, ids[0], qi & 31);
+                        const int g1 = __shfl_sync(0xffffffffu, ids[1], qi & 31);
+                        const int g2 = __shfl_sync(0xffffffffu, ids[2], qi & 31);
+                        const int g3 = __shfl_sync(0xffffffffu, ids[3], qi & 31);
+                        const int sl = qi >> 5;
+                        int gq = sl == 0 ? g0 : sl == 1 ? g1 : sl == 2 ? g2 : g3;
+                        if (gq < 0) gq = first;
+                        r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
+                    }
+                    tc::tma_gather4_hint(qt + lane * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
+                }
             } else if (p.qpk >= 8) {
                 // lane l issues query slot l's box: one instruction issues them all
                 if (lane < nq)
@@ -331,11 +386,14 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 u += u_step;
             }
         }
-        // drain outstanding copies before the CTA can exit
+        // drain outstanding copies (K/V and Q) before the CTA can exit: after
+        // an abort, copies may still be landing in shared memory
         if (lane == 0) {
             volatile int dummy = 0;
             for (int i = 0; i < NKV; ++i)
                 if (kv_armed[i] >= 0) tc::mbar_wait(bar(L::KV_FULL + i), (uint32_t)kv_armed[i], &dummy, p.status, 0);
+            for (int i = 0; i < NQ; ++i)
+                if (q_armed[i] >= 0) tc::mbar_wait(bar(L::Q_FULL + i), (uint32_t)q_armed[i], &dummy, p.status, 0);
         }
         __syncwarp();
     } else if (warp == kWarpFeed) {
@@ -380,7 +438,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         __syncwarp();
     } else if (warp == kWarpDequant) {
         // ------------------------------------------------------------------ NVFP4 / FP8 K/V producer
-        if (KV_FORMAT != MSA_KV_BF16) {
+        if (KV_FORMAT != MSA_KV_BF16) {  // NVFP4 / FP8: K and V; QK8: V
             int ui = 0;
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
@@ -391,7 +449,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if constexpr (KV_FORMAT == MSA_KV_FP8) {
+                if constexpr (KV_FORMAT == MSA_KV_FP8 || QK8) {
                 // 128 tokens x 8 pieces of 16 e4m3 values (16 bytes), for K and
                 // then for V.  Lane l converts piece l % 8 of tokens l / 8 + 4 i:
                 // lanes 8i..8i+7 read one token's 128 bytes.  Eight 16-byte
@@ -408,7 +466,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     klen = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - __ldg(p.cu_k + x.b) : (int64_t)p.Skv) - x.tok0;
                 }
 #pragma unroll 1
-                for (int k0 = 0; k0 < 64; k0 += 8) {
+                for (int k0 = QK8 ? 32 : 0; k0 < 64; k0 += 8) {
                     const int isv = k0 >> 5, rb = r0 + 4 * (k0 & 31);
                     const uint8_t *pbase = isv ? p.v_packed : p.k_packed;
                     uint4 pk[8];
@@ -420,7 +478,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                    : make_uint4(0, 0, 0, 0);
                     }
                     // values 16 pc .. 16 pc + 15: column half pc / 4, chunks 2 (pc % 4), + 1
-                    const uint32_t tile = base + (isv ? L::V : L::K) + kb * 32768 + (pc >> 2) * 16384;
+                    const uint32_t tile = base + (isv ? L::V + kb * 32768 : L::K + kb * KS) + (pc >> 2) * 16384;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         uint4 o4[2];
@@ -485,8 +543,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             int ci = 0, ui = 0;
             bool ok = true;
             int pv_ci = -1, pv_kb = 0, pv_last = 0;
+            bool pv_cont = false;  // paged: PV accumulates onto the warpgroup's O
             // Q tile geometry (see the loader): octet stride and half offset
-            const uint32_t q_sbo = p.qpk >= 8 ? 2048u : 1024u, q_half = p.qpk >= 8 ? 1024u : 16384u;
+            const uint32_t q_sbo = (p.qpk >= 8 && !QK8) ? 2048u : 1024u, q_half = p.qpk >= 8 ? 1024u : 16384u;
             auto pv_ready = [&](int cj) -> bool {
                 const int b = cj & 1;
                 return tc::mbar_test(bar(L::P_FULL + b), (cj >> 1) & 1) &&
@@ -499,7 +558,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
-                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, kk > 0);
+                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, (kk > 0 || pv_cont) ? 1u : 0u);
                 tc::mma_commit(bar(L::O_FULL + b));
                 if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
@@ -508,13 +567,21 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             auto issue_s = [&](int cj, int kbj, int qn, bool release_q) {
                 const int b = cj & 1, qs = qn % NQ;
                 tc::fence_after_sync();
-                const uint32_t qt = base + L::Q + qs * 32768, ks = base + L::K + kbj * 32768;
+                const uint32_t qt = base + L::Q + qs * QS, ks = base + L::K + kbj * KS;
+                if constexpr (QK8) {
+                    // e4m3: a 128-byte row holds all 128 dims, 32 per MMA
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint32_t qoff = (kk >> 2) * q_half + (kk & 3) * 32;
-                    tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + qoff, 16, q_sbo),
-                               tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ss_f8(tmem + b * 128, tc::sdesc_sw128(qt + kk * 32, 16, 1024),
+                                      tc::sdesc_sw128(ks + kk * 32, 16, 1024), kIdescS8, kk > 0);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t qoff = (kk >> 2) * q_half + (kk & 3) * 32;
+                        tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + qoff, 16, q_sbo),
+                                   tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
+                    }
                 }
                 tc::mma_commit(bar(L::S_FULL + b));
                 if (release_q) tc::mma_commit(bar(L::Q_EMPTY + qs));
@@ -551,19 +618,20 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             // Q tiles as the loader issues them: one per chunk, or (paged
             // decode) one per run of consecutive units of one group, told apart
             // by first query * Hkv + head (read one unit ahead)
-            auto first_query = [&](const Unit &y) -> int {
-                return PAGED ? (__ldg(p.qsplit + (int64_t)y.h * p.cap + y.start) & 0xFFFFFF) * p.Hkv + y.h : 0;
+            auto first_query = [&](const Unit &y) -> int64_t {
+                return PAGED ? (int64_t)(__ldg(p.qsplit + (int64_t)y.h * p.cap + y.start) & 0xFFFFFF) * p.Hkv + y.h : 0;
             };
-            int qn = -1, q_first = -1;
+            int qn = -1;
+            int64_t q_first = -1, key_m1 = -1, key_m2 = -1;  // paged: group keys of units ci-1, ci-2
             Unit xnext{};
-            int fnext = -1;
+            int64_t fnext = -1;
             if (u_begin < u_end) {
                 xnext = load_unit(p, u_begin);
                 fnext = first_query(xnext);
             }
             for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
                 const Unit x = xnext;
-                const int fx = fnext;
+                const int64_t fx = fnext;
                 const bool has_next = u + u_step < u_end;
                 if (has_next) {
                     xnext = load_unit(p, u + u_step);
@@ -583,6 +651,13 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
+                    if constexpr (PAGED) {
+                        // a warpgroup's consecutive units of one group (ci - 2,
+                        // ci) accumulate into its O buffer
+                        pv_cont = ci >= 2 && fx == key_m2;
+                        key_m2 = key_m1;
+                        key_m1 = fx;
+                    }
                 }
             }
             if (ok && pv_ci >= 0) drive(-1, 0, false, 0, 0, false);
@@ -642,7 +717,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     }
                     if (!valid) continue;
                     // streaming stores: evict first from L2
-                    if (p.part_dtype == MSA_PARTIAL_FP32) {
+                    if (OPTS && p.part_dtype == MSA_PARTIAL_FP32) {
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4) {
                             float4 *d = reinterpret_cast<float4 *>(dst + (8 * hf + v4) * cstride);
@@ -651,7 +726,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                             __stcs(d + 1, make_float4(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]),
                                                       __uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
                         }
-                    } else if (p.part_dtype == MSA_PARTIAL_FP16) {
+                    } else if (OPTS && p.part_dtype == MSA_PARTIAL_FP16) {
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4) {
                             uint4 o4;
@@ -685,26 +760,86 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         const int j_of_row = R % p.qpk;  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
-        // the unit and its sequence's key count (paged: seqused[b]), first
-        // global query and query count, loaded one unit ahead
-        auto seq_of = [&](const Unit &y) -> int3 {
-            if (PAGED) return make_int3(__ldg(p.seqused + y.b), y.b * p.Sq, p.Sq);
-            if (p.cu_q) {
-                const int q0 = __ldg(p.cu_q + y.b);
-                return make_int3(__ldg(p.cu_k + y.b + 1) - __ldg(p.cu_k + y.b), q0, __ldg(p.cu_q + y.b + 1) - q0);
+        // the unit and, loaded one unit ahead, its sequence's key count kv
+        // (paged: seqused[b]; ragged: from cu_seqlens_k) and cb = kv - (first
+        // query + query count) of the sequence: global query gq sees keys up to
+        // min(kv - 1, gq + cb) (bottom-right causal: local query s sees keys up
+        // to s + kv - Sq)
+        auto seq_of = [&](const Unit &y) -> int2 {
+            if (PAGED) {
+                const int kv = __ldg(p.seqused + y.b);
+                return make_int2(kv, kv - (y.b + 1) * p.Sq);
             }
-            return make_int3(p.Skv, y.b * p.Sq, p.Sq);
+            if (p.cu_k) {
+                const int kv = __ldg(p.cu_k + y.b + 1) - __ldg(p.cu_k + y.b);
+                return make_int2(kv, kv - __ldg(p.cu_q + y.b + 1));
+            }
+            return make_int2(p.Skv, p.Skv - (y.b + 1) * p.Sq);
         };
         Unit xnext{};
-        int3 seqnext = make_int3(p.Skv, 0, p.Sq);
+        int2 seqnext = make_int2(p.Skv, 0);
         if (u_begin < u_end) {
             xnext = load_unit(p, u_begin);
             seqnext = seq_of(xnext);
         }
+        // paged decode: this warpgroup accumulates O over its consecutive units
+        // of one group (a piece); per row: the reference max, the sum of P, the
+        // row's piece (partial slot, -1 while it selected nothing) and its
+        // (query, KV head) group
+        float m_acc = -INFINITY, l_acc = 0.f, lr_acc = 0.f;  // reference, sum of P, sum of the rounded P
+        int piece_acc = -1, gq_acc = 0, h_acc = 0;
+        // group key of a unit: first query | (KV head mod 128) << 24 (query
+        // ids are below 2^24; the units compared, this warpgroup's consecutive
+        // ones, are at most two groups apart, so their heads differ mod 128)
+        int key_prev = -1;
+        int ci_prev = -1;  // this warpgroup's previous unit
+        // writes the rows' pieces and starts a new piece; the O buffer holds
+        // every PV of the piece (its last one has completed).  A piece is the
+        // fp32 partial U * (l / lr) with statistics (m scale, l): U sums the
+        // rounded P, so dividing by their sum lr makes each P's weight
+        // consistent, while l, the sum of the unrounded P, keeps the LSE exact
+        auto finalize = [&]() {
+            if constexpr (PAGED) {
+                if (__any_sync(0xffffffffu, piece_acc >= 0)) {
+                    const int64_t grp_acc = (int64_t)gq_acc * p.Hkv + h_acc;
+                    // piece of chunk c at float4 index 2 (index + c qpk) (32-byte pieces)
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part) +
+                                  2 * part_o_index(grp_acc, p.topk, p.qpk, piece_acc < 0 ? 0 : piece_acc, 0, j_of_row);
+                    const float fac = lr_acc > 0.f ? l_acc / lr_acc : 0.f;
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t po[64];
+                        tc::tmem_ld64(o_addr + 64 * hf, po);
+                        tc::tmem_ld_wait();
+                        if (piece_acc >= 0) {
+#pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4) {
+                                float4 *d = dst + (int64_t)2 * (8 * hf + v4) * p.qpk;
+                                __stcs(d, make_float4(__uint_as_float(po[8 * v4 + 0]) * fac,
+                                                      __uint_as_float(po[8 * v4 + 1]) * fac,
+                                                      __uint_as_float(po[8 * v4 + 2]) * fac,
+                                                      __uint_as_float(po[8 * v4 + 3]) * fac));
+                                __stcs(d + 1, make_float4(__uint_as_float(po[8 * v4 + 4]) * fac,
+                                                          __uint_as_float(po[8 * v4 + 5]) * fac,
+                                                          __uint_as_float(po[8 * v4 + 6]) * fac,
+                                                          __uint_as_float(po[8 * v4 + 7]) * fac));
+                            }
+                        }
+                    }
+                    if (piece_acc >= 0) {
+                        const float2 st = make_float2(l_acc > 0.f ? m_acc * p.scale : -INFINITY, l_acc);
+                        __stcs(p.stat_part + part_stat_index(grp_acc, p.topk, p.qpk, piece_acc, j_of_row), st);
+                    }
+                }
+                m_acc = -INFINITY;
+                l_acc = 0.f;
+                lr_acc = 0.f;
+                piece_acc = -1;
+            }
+        };
         for (int u = u_begin; u < u_end && ok; u += u_step) {
             const Unit x = xnext;
-            const int64_t kv_len = seqnext.x;
-            const int seq_q0 = seqnext.y, seq_nq = seqnext.z;
+            const int kv_len = seqnext.x, seq_cb = seqnext.y;
             if (u + u_step < u_end) {
                 xnext = load_unit(p, u + u_step);
                 seqnext = seq_of(xnext);
@@ -717,6 +852,129 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 const int packed = in_chunk ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
                 // split 255: a query of a paged unit's group that did not select the block
                 const bool valid = in_chunk && (!PAGED || ((uint32_t)packed >> 24) != 0xFFu);
+                if constexpr (PAGED) {
+                    // -------- paged decode: pieces accumulate in the O buffer
+                    const int key = (__ldg(p.qsplit + x.start) & 0xFFFFFF) | ((x.h & 127) << 24);
+                    ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    if (ci_prev >= 0) {
+                        // the PV of this warpgroup's previous unit has completed
+                        ok = tc::mbar_wait(bar(L::O_FULL + wg), (ci_prev >> 1) & 1, abort_flag, p.status,
+                                           MSA_STATUS_TIMEOUT);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        if (key != key_prev) finalize();  // a new group: its PV overwrites O
+                    }
+                    // the S row (rows of queries that did not select the block
+                    // and padding rows: P = 0)
+                    const bool any_sel = __any_sync(0xffffffffu, valid);
+                    const int gq = packed & 0xFFFFFF;
+                    int nvis = 0;
+                    if (valid && x.page >= 0) {
+                        // keys of the block visible to query gq
+                        int limit = kv_len - 1;
+                        if (p.causal) limit = min(limit, gq + seq_cb);
+                        const int nv = limit - x.tok0 + 1;
+                        nvis = nv < 0 ? 0 : (nv > 128 ? 128 : nv);
+                    }
+                    uint32_t pr[128];
+                    float l = 0.f, lround = 0.f;
+                    if (any_sel) {
+#define MSA_LOAD_S_ROW()                                                 \
+    do {                                                                 \
+        tc::tmem_ld128(s_addr, pr);                                      \
+        tc::tmem_ld_wait();                                              \
+        if (nvis < 128) {                                                \
+            _Pragma("unroll") for (int j = 0; j < 128; ++j) if (j >= nvis) pr[j] = 0xff800000u; \
+        }                                                                \
+    } while (0)
+                        MSA_LOAD_S_ROW();
+                        float mm[4];
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 128; j += 8) {
+#pragma unroll
+                            for (int a = 0; a < 4; ++a)
+                                mm[a] = fmax3(mm[a], __uint_as_float(pr[j + 2 * a]), __uint_as_float(pr[j + 2 * a + 1]));
+                        }
+                        const float mh = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                        // a row whose max exceeds its reference by more than the
+                        // bound (rare): its O row and sum are rescaled to the new
+                        // max (O is stable: the previous PV has completed, the
+                        // next waits for O_EMPTY below)
+                        const bool grow = valid && m_acc != -INFINITY && (mh - m_acc) * p.scale_log2 > p.p_bound;
+                        if (__any_sync(0xffffffffu, grow)) {
+                            const float f = grow ? ex2_approx((m_acc - mh) * p.scale_log2) : 1.f;
+                            if (grow) {
+                                l_acc *= f;
+                                lr_acc *= f;
+                                m_acc = mh;
+                            }
+#pragma unroll 1
+                            for (int hf = 0; hf < 2; ++hf) {
+                                uint32_t po[64];
+                                tc::tmem_ld64(o_addr + 64 * hf, po);
+                                tc::tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 64; ++j) po[j] = __float_as_uint(__uint_as_float(po[j]) * f);
+                                tc::tmem_st64h(o_addr + 64 * hf, po);
+                            }
+                            tc::tmem_st_wait();
+                            MSA_LOAD_S_ROW();
+                        }
+#undef MSA_LOAD_S_ROW
+                        if (valid && m_acc == -INFINITY) m_acc = mh;  // the piece's first visible keys of the row
+                        if (ci_prev >= 0) {
+                            tc::fence_before_sync();
+                            tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: this unit's PV may start
+                        }
+                        // P = exp2((S - m) scale_log2) packed to bf16 in place
+                        // (pr[j] <- keys 2j, 2j+1); the sums of P and of the
+                        // rounded P that PV uses (against a reference below the
+                        // row max the largest P is not 1)
+                        const float mc = (m_acc == -INFINITY) ? 0.f : m_acc * p.scale_log2;
+                        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                        const float2 nm2 = make_float2(-mc, -mc);
+                        float2 ll = make_float2(0.f, 0.f), lr = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) {
+                            float2 e = __ffma2_rn(make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])),
+                                                  sc2, nm2);
+                            e.x = ex2_approx(e.x);
+                            e.y = ex2_approx(e.y);
+                            ll = __fadd2_rn(ll, e);
+                            pr[j] = pack_bf16x2(e.x, e.y);
+                            lr = __fadd2_rn(lr, make_float2(bf16_lo(pr[j]), bf16_hi(pr[j])));
+                        }
+                        l = ll.x + ll.y;
+                        lround = lr.x + lr.y;
+                    } else {
+                        if (ci_prev >= 0) {
+                            tc::fence_before_sync();
+                            tc::mbar_arrive(bar(L::O_EMPTY + wg));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) pr[j] = 0u;  // no row selects the block: P = 0
+                    }
+                    tc::tmem_st64(s_addr, pr);
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(bar(L::P_FULL + wg));
+                    if (valid) {
+                        l_acc += l;
+                        lr_acc += lround;
+                        piece_acc = (packed >> 24) & 0xFF;
+                        gq_acc = gq;
+                        h_acc = x.h;
+                    }
+                    key_prev = key;
+                    ci_prev = ci;
+                    continue;
+                }
                 ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -727,107 +985,12 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     tc::fence_after_sync();
                     tc::fence_before_sync();
                     tc::mbar_arrive(bar(L::P_FULL + wg));
-                    if constexpr (PAGED) {
-                        ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        tc::fence_after_sync();
-                        tc::fence_before_sync();
-                        tc::mbar_arrive(bar(L::O_EMPTY + wg));
-                    }
                     continue;
                 }
-                if constexpr (PAGED) {
+                {
                     tc::fence_after_sync();
-                    uint32_t r[128];
-                    tc::tmem_ld128(s_addr, r);
-                    // row info while the load is in flight
-                    const int gq = packed & 0xFFFFFF;
-                    const int split = (packed >> 24) & 0xFF;
-                    int nvis = 0;
-                    if (valid && (!p.unit_page || x.page >= 0)) {
-                        // keys visible to query sq of a sequence of kv_len keys
-                        // (bottom-right causal: up to key sq + kv_len - Sq)
-                        const int sq = gq - seq_q0;
-                        int64_t limit = kv_len - 1;
-                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - seq_nq);
-                        const int64_t nv = limit - x.tok0 + 1;
-                        nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
-                    }
-                    tc::tmem_ld_wait();
-                    // keys past the causal limit (diagonal block rows) become -inf
-                    if (nvis < 128) {
-#pragma unroll
-                        for (int j = 0; j < 128; ++j)
-                            if (j >= nvis) r[j] = 0xff800000u;
-                    }
-                    // row max: three-input max, four independent chains
-                    float mm[4];
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-#pragma unroll
-                    for (int j = 0; j < 128; j += 8) {
-#pragma unroll
-                        for (int a = 0; a < 4; ++a)
-                            mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
-                    }
-                    const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                    // P = exp2(S * scale_log2 - m * scale_log2) packed to bf16 in place
-                    // (r[j] <- keys 2j, 2j+1); row sum in packed f32x2 adds
-                    const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
-                    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                    const float2 nm2 = make_float2(-mc, -mc);
-                    float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        float2 e = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
-                        e.x = ex2_approx(e.x);
-                        e.y = ex2_approx(e.y);
-                        ll[j & 1] = __fadd2_rn(ll[j & 1], e);
-                        r[j] = pack_bf16x2(e.x, e.y);
-                    }
-                    const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
-                    tc::tmem_st64(s_addr, r);
-                    tc::tmem_st_wait();
-                    tc::fence_before_sync();
-                    tc::mbar_arrive(bar(L::P_FULL + wg));
-                    // epilogue: unnormalised O -> bf16 partial, (m * scale, l)
-                    ok = tc::mbar_wait(bar(L::O_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    tc::tmem_ld128(o_addr, r);
-                    tc::tmem_ld_wait();
-                    tc::fence_before_sync();
-                    tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is in registers: the next PV may start
-                    if (valid) {
-                        // grouped layout: for a fixed (split, c) the heads of one group are
-                        // contiguous, so each store instruction writes whole runs
-                        const int64_t grp = (int64_t)gq * p.Hkv + x.h;
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row);
-#pragma unroll
-                        for (int v4 = 0; v4 < 16; ++v4) {
-                            uint4 o4;
-                            o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
-                            o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
-                            o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
-                            o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                            __stcs(dst + (int64_t)v4 * p.qpk, o4);  // streaming: evict first from L2
-                        }
-                        const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
-                        float2 *sdst = p.stat_part + part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
-                        __stcs(sdst, st);
-                    }
-                } else {
-                    tc::fence_after_sync();
-                    // The S row is read 64 keys at a time (a whole row in registers
-                    // leaves the compiler no room), once: the first half's max is the
-                    // reference m for the whole row.  P = exp2((S - m) * scale_log2)
-                    // is exact softmax arithmetic for any reference, and the split
-                    // statistics carry m, so the second half may exceed it; only when
-                    // it exceeds it by more than p_bound (log2 units: P up to
-                    // 2^p_bound) is the first half's P rescaled to the new max (a
-                    // warp-uniform slow path).
+                    // The S row is read 64 keys at a time: one pass for the max, one
+                    // for P (a whole row in registers leaves the compiler no room).
                     uint32_t r[64];
                     tc::tmem_ld64(s_addr, r);
                     // row info while the load is in flight
@@ -835,13 +998,11 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     const int split = (packed >> 24) & 0xFF;
                     int nvis = 0;
                     if (valid && (!p.unit_page || x.page >= 0)) {
-                        // keys visible to query sq of a sequence of kv_len keys
-                        // (bottom-right causal: up to key sq + kv_len - Sq)
-                        const int sq = gq - seq_q0;
-                        int64_t limit = kv_len - 1;
-                        if (p.causal) limit = min(limit, (int64_t)sq + kv_len - seq_nq);
-                        const int64_t nv = limit - x.tok0 + 1;
-                        nvis = (int)(nv < 0 ? 0 : (nv > 128 ? 128 : nv));
+                        // keys of the block visible to query gq
+                        int limit = kv_len - 1;
+                        if (p.causal) limit = min(limit, gq + seq_cb);
+                        const int nv = limit - x.tok0 + 1;
+                        nvis = nv < 0 ? 0 : (nv > 128 ? 128 : nv);
                     }
                     // keys past the causal limit (diagonal block rows) become -inf
                     auto mask_half = [&](int hf) {
@@ -852,61 +1013,42 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                 if (j >= lim) r[j] = 0xff800000u;
                         }
                     };
-                    // max of the half in registers: three-input max, four chains
-                    auto half_max = [&]() -> float {
-                        float mm[4];
+                    // row max: three-input max, four independent chains
+                    float mm[4];
 #pragma unroll
-                        for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+                    for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
+                        tc::tmem_ld_wait();
+                        mask_half(hf);
 #pragma unroll
                         for (int j = 0; j < 64; j += 8) {
 #pragma unroll
                             for (int a = 0; a < 4; ++a)
                                 mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                         }
-                        return fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                    };
+                    }
+                    const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                    // P = exp2(S * scale_log2 - m * scale_log2): each half is read
+                    // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
+                    // the half) and stored over columns the half has already read;
+                    // row sum in packed f32x2 adds (TEMP: also of 2^(x / T))
+                    const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
                     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nm2 = make_float2(-mc, -mc);
                     float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                    float2 lt = make_float2(0.f, 0.f);  // TEMP: row sum of 2^(x / T)
-                    float m = -INFINITY;  // reference max
-                    float f = 1.f;        // rescale factor of the first half's P
-                    bool grow = false;
+                    float2 lt = make_float2(0.f, 0.f);
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
-                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
+                        tc::tmem_ld64(s_addr + 64 * hf, r);
                         tc::tmem_ld_wait();
                         mask_half(hf);
-                        const float mh = half_max();
-                        if (hf == 0) {
-                            m = mh;
-                        } else {
-                            // the second half's max exceeds the reference by more
-                            // than the bound: it becomes the reference, the first
-                            // half's sum now and its stored P below scale by
-                            // f = 2^((m - mh) scale_log2) (0 when m was -inf)
-                            grow = mh > m && (m == -INFINITY || (mh - m) * p.scale_log2 > p.p_bound);
-                            if (grow) {
-                                f = (m == -INFINITY) ? 0.f : ex2_approx((m - mh) * p.scale_log2);
-                                if constexpr (TEMP) {
-                                    const float ft = (m == -INFINITY) ? 0.f : ex2_approx((m - mh) * p.scale_log2 * p.inv_temp);
-                                    lt.x *= ft;
-                                    lt.y *= ft;
-                                }
-                                m = mh;
-                                ll[0].x *= f; ll[0].y *= f; ll[1].x *= f; ll[1].y *= f;
-                            }
-                        }
-                        // P of this half against the reference, packed to bf16
-                        // pairs in place (r[j] <- keys 2j, 2j+1 of the half) and
-                        // stored over columns already read; row sum in packed
-                        // f32x2 adds
-                        const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
-                        const float2 nm2 = make_float2(-mc, -mc);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             float2 e =
                                 __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
-                            if constexpr (TEMP) {
+                            if (OPTS && p.temp_on) {
                                 const float2 t = __fmul2_rn(e, make_float2(p.inv_temp, p.inv_temp));
                                 lt = __fadd2_rn(lt, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                             }
@@ -916,16 +1058,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                             r[j] = pack_bf16x2(e.x, e.y);
                         }
                         tc::tmem_st32(s_addr + 32 * hf, r);
-                    }
-                    if (__any_sync(0xffffffffu, grow)) {
-                        // rare: rescale the stored first-half P (columns 0-31) of
-                        // the rows whose reference moved (f = 1 leaves the others)
-                        tc::tmem_st_wait();
-                        tc::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = pack_bf16x2(bf16_lo(r[j]) * f, bf16_hi(r[j]) * f);
-                        tc::tmem_st32(s_addr, r);
                     }
                     const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
                     tc::tmem_st_wait();
@@ -938,11 +1070,22 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                         const int64_t si = part_stat_index(grp, p.topk, p.qpk, split, j_of_row);
                         const float2 st = make_float2(l > 0.f ? m * p.scale : -INFINITY, l);
                         __stcs(p.stat_part + si, st);
-                        if constexpr (TEMP) {
+                        if (OPTS && p.temp_on) {
                             const float ltt = lt.x + lt.y;
                             __stcs(p.stat_temp + si, make_float2(ltt > 0.f ? m * p.scale * p.inv_temp : -INFINITY, ltt));
                         }
                     }
+                }
+            }
+        }
+        if constexpr (PAGED) {
+            // the warpgroup's last piece, once its last PV has completed
+            if (ok && ci_prev >= 0) {
+                ok = tc::mbar_wait(bar(L::O_FULL + wg), (ci_prev >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    tc::fence_after_sync();
+                    finalize();
                 }
             }
         }

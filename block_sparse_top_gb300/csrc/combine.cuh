@@ -56,8 +56,8 @@ struct PartPiece {
 
 // Merges the first n of topk splits of piece (group grp, 8-dim chunk c, head j
 // of the group) into out (8 bf16) and lse_out.  Every load of a batch of BATCH
-// splits is issued before any is used (all topk slots are read, those at or
-// past n are ignored); batches merge online with a running max.  SMEM: the
+// splits is issued before any is used (only the first n slots are read);
+// batches merge online with a running max.  SMEM: the
 // group's partials and statistics were staged in shared memory (o_part and
 // stat_part point at the copy, grp 0).  PD: the partials' storage type.
 template <int MAXS, int PD, int BATCH = 16, bool SMEM = false>
@@ -71,19 +71,16 @@ __device__ __forceinline__ void combine_piece(const void *__restrict__ o_part, c
     float mx = -INFINITY, den = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-    for (int s0 = 0; s0 < (MAXS < topk ? MAXS : topk); s0 += BATCH) {
+    for (int s0 = 0; s0 < (MAXS < n ? MAXS : n); s0 += BATCH) {
         PartPiece<PD> v[BATCH];
         float2 sv[BATCH];
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)
-            if (s0 + t < topk) v[t].load(src + (s0 + t) * o_stride, SMEM);
+            if (s0 + t < n) v[t].load(src + (s0 + t) * o_stride, SMEM);
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)
-            sv[t] = (s0 + t < topk) ? (SMEM ? st[(s0 + t) * qpk] : __ldg(st + (int64_t)(s0 + t) * qpk))
-                                    : make_float2(-INFINITY, 0.f);
-#pragma unroll
-        for (int t = 0; t < BATCH; ++t)
-            if (s0 + t >= n) sv[t].x = -INFINITY;
+            sv[t] = (s0 + t < n) ? (SMEM ? st[(s0 + t) * qpk] : __ldg(st + (int64_t)(s0 + t) * qpk))
+                                 : make_float2(-INFINITY, 0.f);
         float bm = mx;
 #pragma unroll
         for (int t = 0; t < BATCH; ++t)

@@ -59,6 +59,7 @@ struct PlanArgs {
     int32_t *unit_page;
     uint32_t *status;
     int B, Sq, Hkv, qpk, topk, num_pages, max_pages, qg, qgroups, groups, maxu;
+    int grid;  // CTAs of the tile kernel (its partition of the unit list)
 };
 
 struct Group {
@@ -259,10 +260,49 @@ __global__ void __launch_bounds__(128) paged_write_kernel(PlanArgs a) {
             pg = -1;  // the tile kernel skips the block
         }
         a.unit_page[u] = pg;
-        for (int qi = 0; qi < x.nq; ++qi) {
-            const int split = us[qi];
-            a.qlist[start + qi] = (x.b * a.Sq + x.q0 + qi) | (split << 24);
+    }
+    // Query tables.  The tile kernel's CTA c runs units [work c / G, work (c+1) / G)
+    // and, inside its run, alternates them between its two softmax warpgroups;
+    // a warpgroup accumulates O over consecutive units of one group, so a
+    // query's partials are its pieces: the distinct (CTA, warpgroup) pairs
+    // that hold a unit it selected, numbered in order of first appearance
+    // (at most one per selected block, so at most topk).  The table holds the
+    // query's piece for each unit it selected, 255 for the others, and the
+    // piece count becomes the query's split count.  One warp per query: lane
+    // l takes units l, l + 32, ...; the order of first appearance runs over
+    // the selected units only (a ballot per 32 units), so the serial steps are
+    // at most topk.
+    const int64_t work = a.ucount[a.groups].x, G = a.grid;
+    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int qi = threadIdx.x >> 5; qi < x.nq; qi += nwarps) {
+        const int gq = x.b * a.Sq + x.q0 + qi;
+        int cur_c = -1, pw0 = -1, pw1 = -1, pieces = 0;
+        for (int e0 = 0; e0 < nu; e0 += 32) {
+            const int e = e0 + lane;
+            const int64_t u = off + e;
+            const bool sel = e < nu && a.usplit[((int64_t)g * a.maxu + e) * a.qg + qi] != 255;
+            int c = 0, w = 0;
+            if (sel) {
+                c = (int)(((u + 1) * G - 1) / work);  // CTA holding unit u
+                w = (int)((u - work * c / G) & 1);     // its warpgroup there
+            }
+            int mine = 255;
+            uint32_t m = __ballot_sync(0xffffffffu, sel);
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int cl = __shfl_sync(0xffffffffu, c, l), wl = __shfl_sync(0xffffffffu, w, l);
+                if (cl != cur_c) {
+                    cur_c = cl;
+                    pw0 = pw1 = -1;
+                }
+                int &pw = wl ? pw1 : pw0;
+                if (pw < 0) pw = pieces++;
+                if (lane == l) mine = pw;
+            }
+            if (e < nu) a.qlist[u * a.qg + qi] = gq | (mine << 24);
         }
+        if (lane == 0) a.split_counts[(int64_t)gq * a.Hkv + x.h] = pieces;
     }
 }
 
@@ -292,7 +332,7 @@ PagedWorkspace paged_workspace_layout(const PagedShape &d, int B, int Sq, int Hq
     w.unit_page = o;
     o = align_up(o + sizeof(int32_t) * (size_t)d.groups * d.maxu, 256);
     w.fwd = o;
-    w.fwd_bytes = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, kD).bytes;
+    w.fwd_bytes = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, kD, MSA_PARTIAL_FP32).bytes;
     o = align_up(o + w.fwd_bytes, 256);
     w.bytes = o;
     return w;
@@ -350,6 +390,7 @@ int paged_tiles_fwd(const void *q, const void *k_pool, const void *v_pool, int k
     a.status = status_dev;
     a.B = B; a.Sq = Sq; a.Hkv = Hkv; a.qpk = qpk; a.topk = topk; a.num_pages = num_pages;
     a.max_pages = max_pages; a.qg = d.qg; a.qgroups = d.qgroups; a.groups = d.groups; a.maxu = d.maxu;
+    a.grid = (int)std::min<int64_t>((int64_t)d.groups * d.maxu, (int64_t)num_sms());  // as tiles_launch
 
     const size_t usmem = sizeof(uint32_t) * (((size_t)max_pages + 31) / 32) + sizeof(int32_t) * (size_t)d.maxu +
                          sizeof(int32_t) * (size_t)d.qg * topk;
@@ -358,7 +399,9 @@ int paged_tiles_fwd(const void *q, const void *k_pool, const void *v_pool, int k
     MSA_CUDA_TRY(launch_pdl(paged_scan_kernel, dim3(1), dim3(1024), 0, stream, a));
     MSA_CUDA_TRY(launch_pdl(paged_write_kernel, dim3(d.groups), dim3(128), 0, stream, a));
 
-    const FwdWorkspace fw = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D);
+    // fp32 pieces: an accumulated piece is a sum over many keys, kept exact
+    // until the combine's single rounding to bf16
+    const FwdWorkspace fw = fwd_workspace_layout((int64_t)B * Sq, Hq, topk, D, MSA_PARTIAL_FP32);
     char *fws = ws + w.fwd;
     TcParams t;
     memset(&t, 0, sizeof t);
@@ -371,7 +414,7 @@ int paged_tiles_fwd(const void *q, const void *k_pool, const void *v_pool, int k
     t.units = a.units;
     t.o_part = fws + fw.o_part;
     t.stat_part = reinterpret_cast<float2 *>(fws + fw.stat_part);
-    t.part_dtype = MSA_PARTIAL_BF16;
+    t.part_dtype = MSA_PARTIAL_FP32;
     t.inv_temp = 1.f;
     t.seqused = seqused_k;
     t.unit_page = a.unit_page;
@@ -390,7 +433,7 @@ int paged_tiles_fwd(const void *q, const void *k_pool, const void *v_pool, int k
                                 kv_format, false, stream);
     if (rc != MSA_OK) return rc;
     return combine_launch(a.split_counts, (int64_t)B * Sq * Hkv, qpk, topk, o, lse, nullptr, fws, fw,
-                          MSA_PARTIAL_BF16, stream);
+                          MSA_PARTIAL_FP32, stream);
 }
 
 // The per-group union decode of decode.cu (dense mode when q2k is NULL) and its scratch.

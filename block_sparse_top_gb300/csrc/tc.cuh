@@ -51,8 +51,13 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
     return ok != 0;
 }
 // Waits are bounded in time: a wait that has not completed within
-// kWaitLimitNs of the device's global nanosecond timer gives up.
+// kWaitLimitNs of the device's global nanosecond timer gives up.  (A test
+// build of the library sets a short limit to check the abort path.)
+#ifdef MSA_TEST_WAIT_LIMIT_NS
+constexpr uint64_t kWaitLimitNs = MSA_TEST_WAIT_LIMIT_NS;
+#else
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+#endif
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
@@ -232,6 +237,23 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0),
+// fp32 accumulate, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                       // D format: f32
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], e4m3 operands (K = 32 per instruction)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // D[tmem] (+)= A[tmem] * B[smem desc]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -288,6 +310,22 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[12
         : "memory");
 #undef MSA_W8
 }
+// Stores r[0..127] into 128 consecutive columns (a whole O row per thread).
+__device__ __forceinline__ void tmem_st128(uint32_t taddr, const uint32_t (&r)[128]) {
+#define MSA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                  "r"(r[i + 6]), "r"(r[i + 7])
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x128.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,"
+        "%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,"
+        "%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,"
+        "%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,"
+        "%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127,%128};\n" ::"r"(taddr),
+        MSA_W8(0), MSA_W8(8), MSA_W8(16), MSA_W8(24), MSA_W8(32), MSA_W8(40), MSA_W8(48), MSA_W8(56), MSA_W8(64),
+        MSA_W8(72), MSA_W8(80), MSA_W8(88), MSA_W8(96), MSA_W8(104), MSA_W8(112), MSA_W8(120)
+        : "memory");
+#undef MSA_W8
+}
 // 64 consecutive columns of the warp's 32 lanes (half an S or O row per
 // thread), as two 32-column loads.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
@@ -302,6 +340,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[64
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
         "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
         MSA_W8(0), MSA_W8(8), MSA_W8(16), MSA_W8(24)
+        : "memory");
+#undef MSA_W8
+}
+// Stores r[0..63] into 64 consecutive columns (from a 64-register array).
+__device__ __forceinline__ void tmem_st64h(uint32_t taddr, const uint32_t (&r)[64]) {
+#define MSA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                  "r"(r[i + 6]), "r"(r[i + 7])
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,"
+        "%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n" ::"r"(taddr),
+        MSA_W8(0), MSA_W8(8), MSA_W8(16), MSA_W8(24), MSA_W8(32), MSA_W8(40), MSA_W8(48), MSA_W8(56)
         : "memory");
 #undef MSA_W8
 }
@@ -351,6 +401,51 @@ inline bool make_kv_map(CUtensorMap *map, const void *base, int heads, int64_t t
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3D e4m3 view of a K cache [tokens][heads][128 bytes]: dims {128, tokens,
+// heads} with byte strides {heads*128, 128} and box {128, 128, 1}: one copy
+// brings a 128-token block of one head as [128 tokens][128 B], 128-byte swizzled.
+inline bool make_k8_map(CUtensorMap *map, const void *base, int heads, int64_t tokens) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)tokens, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)heads * 128, 128};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// e4m3 query rows [rows][128 bytes]: qpk >= 8, one box per (query, KV head)
+// group as 4D {128, 8 rows, qpk/8 octets, groups} (strides {128, 1024,
+// qpk*128}, box {128, 8, qpk/8, 1}: [octet][8 rows][128 B], octets 1024 bytes
+// apart); qpk < 8, 2D rows {128, rows} with a one-row box for tile::gather4.
+inline bool make_q8_map(CUtensorMap *map, const void *base, int64_t rows, int qpk) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    CUresult r;
+    if (qpk >= 8) {
+        const int64_t groups = rows / qpk;
+        cuuint64_t dims[4] = {128, 8, (cuuint64_t)(qpk / 8), (cuuint64_t)groups};
+        cuuint64_t strides[3] = {128, 1024, (cuuint64_t)qpk * 128};
+        cuuint32_t box[4] = {128, 8, (cuuint32_t)(qpk / 8), 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {128};
+        cuuint32_t box[2] = {128, 1};
+        cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 

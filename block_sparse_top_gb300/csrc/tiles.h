@@ -18,10 +18,10 @@ FwdWorkspace fwd_workspace_layout(int64_t total_q, int Hq, int topk, int D, int 
 int num_sms();
 
 // Launches the tile kernel for the plan in t (grid: at most one CTA per SM and
-// at most `capacity` CTAs); K and V are viewed as kv_tokens token rows; temp
-// selects the instance that keeps the temperature statistics.
+// at most `capacity` CTAs); K and V are viewed as kv_tokens token rows; opts
+// selects the instance that serves t's options (partial type, temperature).
 int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void *k, const void *v, int64_t kv_tokens,
-                 int kv_format, bool temp, cudaStream_t stream);
+                 int kv_format, bool opts, cudaStream_t stream, bool qk_fp8 = false);
 
 // LSE combine of a forward's split partials (workspace ws laid out as w) over
 // `groups` (query, KV head) pairs into o, lse (may be null) and, when the
@@ -36,22 +36,25 @@ int combine_launch(const int32_t *split_counts, int64_t groups, int qpk, int top
     int NAME(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid, \
              cudaStream_t stream)
 MSA_TILE_INSTANCE(launch_tiles_bf16);
-MSA_TILE_INSTANCE(launch_tiles_bf16_temp);
+MSA_TILE_INSTANCE(launch_tiles_bf16_opts);
 MSA_TILE_INSTANCE(launch_tiles_nvfp4);
-MSA_TILE_INSTANCE(launch_tiles_nvfp4_temp);
+MSA_TILE_INSTANCE(launch_tiles_nvfp4_opts);
 MSA_TILE_INSTANCE(launch_tiles_fp8);
-MSA_TILE_INSTANCE(launch_tiles_fp8_temp);
+MSA_TILE_INSTANCE(launch_tiles_fp8_opts);
+MSA_TILE_INSTANCE(launch_tiles_qk8);
+MSA_TILE_INSTANCE(launch_tiles_qk8_opts);
 MSA_TILE_INSTANCE(launch_tiles_paged);
 MSA_TILE_INSTANCE(launch_tiles_paged_fp8);
 
-// The launch of instance <KV_FORMAT, NKV, NQ, PAGED, TEMP> (used by tiles_*.cu).
-template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool TEMP>
+// The launch of instance <KV_FORMAT, NKV, NQ, PAGED, OPTS> (used by tiles_*.cu).
+template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool OPTS>
 int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
                  cudaStream_t stream) {
-    const size_t smem = tck::Layout<NKV, NQ>::BYTES;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, TEMP>,
+    constexpr uint32_t S = KV_FORMAT == tck::kKvQk8 ? 16384u : 32768u;  // K and Q stage bytes
+    const size_t smem = tck::Layout<NKV, NQ, S, S>::BYTES;
+    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, OPTS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, TEMP>, dim3(grid),
+    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, OPTS>, dim3(grid),
                             dim3(tck::threads_for(PAGED)), smem, stream, mk, mv, mq, t));
     return MSA_OK;
 }

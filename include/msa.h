@@ -83,11 +83,17 @@ extern "C" {
  *   lse_temperature        [total_q][Hq] fp32 device output or NULL: the LSE of
  *                          the visible scores divided by T, log sum_t
  *                          exp(scale q.k_t / T) (-inf for a row with no key).
+ *   qk_fp8                 1: q is e4m3 bytes [total_q][Hq][D] and, with
+ *                          kv_format MSA_KV_FP8, S = Q K^T runs as an e4m3 MMA
+ *                          (fp32 accumulate) while V is staged to bf16 for the
+ *                          bf16 P V MMA (interface.py qk_dtype = fp8, pv_dtype =
+ *                          bf16); 0: q is bf16.
  */
 typedef struct msa_fwd_options {
     int partial_dtype;
     float lse_temperature_scale;
     float *lse_temperature;
+    int qk_fp8;
 } msa_fwd_options;
 
 /* Human-readable name of an MSA_* status code (static string). */

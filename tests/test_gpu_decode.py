@@ -96,3 +96,20 @@ def test_decode_repeat_calls_identical():
     b = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], d["q2k"])
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_decode_peaked_scores_rescale_accumulated_rows():
+    """With a softmax scale of 8 a row's later blocks often hold a max far
+    above the reference of its accumulated piece, so the decode rescales the
+    accumulated O row; the result still matches the oracle."""
+    import block_sparse_top_gb300 as msa
+    spec = synth.paged_decode_spec(8192)
+    d = synth.make_decode_inputs(spec, device=DEV)
+    o, lse = msa.sparse_attn_paged_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], d["q2k"],
+                                       softmax_scale=8.0)
+    torch.cuda.synchronize()
+    rows = synth.sample_query_rows(spec.B * spec.Sq, 48, must=[0, 7, 255])
+    o_ref, l_ref = oracle.sparse_attn_paged(d["q"].cpu(), d["k_pool"].cpu(), d["v_pool"].cpu(),
+                                            d["page_table"].cpu(), d["seqused"].cpu(), d["q2k"].cpu(), rows=rows,
+                                            scale=8.0)
+    assert_attn_close(o[rows], lse[rows], o_ref, l_ref, "decode peaked")

@@ -117,3 +117,25 @@ def test_dense_decode_matches_oracle(spec):
                                              seqused=d["seqused"].cpu(), rows=rows)
     og, lg = (o, lse) if rows is None else (o[rows], lse[rows])
     assert_attn_close(og, lg, o_ref, l_ref, spec.name)
+
+
+@pytest.mark.parametrize("qpk,topk", [(16, 16), (8, 8), (2, 16), (1, 4)])
+def test_fp8_qk_bf16_pv_matches_oracle(qpk, topk):
+    """e4m3 Q and K with S = Q K^T as an fp8 MMA, e4m3 V staged to bf16 for the
+    bf16 P V: the oracle runs on the decoded e4m3 values (exact in bf16)."""
+    import block_sparse_top_gb300 as msa
+    spec = synth.VarlenSpec(f"qk8_{qpk}", q_lens=(700, 129, 40), k_lens=(1024, 2048, 512), Hkv=2, qpk=qpk, topk=topk,
+                            causal=True, pattern="sink")
+    x = synth.make_varlen_inputs(spec, device=DEV)
+    q8, qd = to_fp8(x["q"])
+    k8, kd = to_fp8(x["k"])
+    v8, vd = to_fp8(x["v"])
+    csr = msa.build_k2q_csr_varlen(x["q2k"], x["cu_seqlens_q"], x["cu_seqlens_k"], 700, 2048, spec.qpk)
+    status = msa.new_status(DEV)
+    o, lse, lt = msa.sparse_attn_fwd_varlen(q8.to(DEV), k8, v8, csr, causal=True, kv_format="fp8",
+                                            lse_temperature_scale=0.75, status=status)
+    assert msa.read_status(status) & msa.MSA_STATUS_FATAL_MASK == 0
+    o_ref, l_ref, t_ref = oracle.sparse_attn_varlen(qd, kd, vd, x["q2k"].cpu(), x["cu_seqlens_q"].cpu(),
+                                                    x["cu_seqlens_k"].cpu(), causal=True, temperature=0.75)
+    assert_attn_close(o, lse, o_ref, l_ref, spec.name)
+    assert_attn_close(o, lt, o_ref, t_ref, spec.name + " temperature lse")

@@ -212,10 +212,10 @@ def test_partial_dtypes_match_oracle_and_fp32_is_at_least_as_close(qpk, topk):
     assert errs[msa.MSA_PARTIAL_FP32][1] <= errs[msa.MSA_PARTIAL_BF16][1]
 
 
-def test_large_scores_take_the_half_row_rescale_path():
-    """A softmax scale of 8 spreads the scores over hundreds of units, so the
-    second half-row's max often exceeds the first's by more than 2^64 in P:
-    the tile kernel rescales the stored first-half P; the result still matches."""
+def test_peaked_softmax_with_large_scores():
+    """A softmax scale of 8 spreads the scores over hundreds of units, so a
+    row's softmax is nearly one-hot; P of the row max is exactly 1 and the
+    output still matches the oracle."""
     import block_sparse_top_gb300 as msa
     spec = V("ragged_big_scores", (600, 300), (1024, 2048), qpk=8, topk=8)
     x = synth.make_varlen_inputs(spec, device=DEV)
