@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS_PER_CSR = 8
 KERNELS_PER_PARTIAL = 1  # attention tiles
 KERNELS_PER_COMBINE = 1  # LSE combine
-KERNELS_PER_PAGED = 5    # union, scan, plan write, attention tiles, LSE combine
+KERNELS_PER_PAGED = 2    # union plan, decode
 
 # DRAM traffic (read + write bytes per launch) of the attention-tile kernel on
 # the 32K causal sink workload from one single-pass ncu capture

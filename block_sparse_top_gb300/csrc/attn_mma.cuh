@@ -301,4 +301,38 @@ __device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 (&out)[2]) {
     out[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Stages 128 token rows of e4m3 values (128 bytes each, row t at src + t *
+// row_stride) as bf16 into a 128-byte-swizzled tile [2 column halves][128
+// rows][128 B] at shared address `tile` (halves 16384 bytes apart), exactly;
+// rows t >= nrows are zero.  One warp: lane l converts the 16-byte piece l % 8
+// (values 16 (l % 8) .. + 15: column half (l % 8) / 4) of rows l / 8 + 4 i,
+// with eight loads in flight before any is used.
+__device__ __forceinline__ void e4m3_rows_to_tile(uint32_t tile, const uint8_t *src, int64_t row_stride, int nrows,
+                                                  int lane) {
+    const int pc = lane & 7, r0 = lane >> 3;
+    const uint32_t half = tile + (uint32_t)(pc >> 2) * 16384u;
+#pragma unroll 1
+    for (int rb = r0; rb < 128; rb += 32) {
+        uint4 pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = rb + 4 * i;
+            pk[i] = r < nrows ? __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)r * row_stride) + pc)
+                              : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint4 o4[2];
+            e4m3x16_to_bf16(pk[i], o4);
+            const int r = rb + 4 * i;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int ch = (pc & 3) * 2 + c;  // 16-byte chunk of the 128-byte row
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(half + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4))),
+                             "r"(o4[c].x), "r"(o4[c].y), "r"(o4[c].z), "r"(o4[c].w));
+            }
+        }
+    }
+}
+
 }  // namespace msa

@@ -450,13 +450,9 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if constexpr (KV_FORMAT == MSA_KV_FP8 || QK8) {
-                // 128 tokens x 8 pieces of 16 e4m3 values (16 bytes), for K and
-                // then for V.  Lane l converts piece l % 8 of tokens l / 8 + 4 i:
-                // lanes 8i..8i+7 read one token's 128 bytes.  Eight 16-byte
-                // loads are in flight before any is used.  Paged: the unit's
-                // page of the pool (an invalid page gives zeros; its keys are
-                // masked), all 128 rows.
-                const int pc = lane & 7, r0 = lane >> 3;
+                // 128 tokens of e4m3 K (not QK8: that K is copied by TMA) and
+                // V.  Paged: the unit's page of the pool (an invalid page
+                // gives zeros; its keys are masked), all 128 rows.
                 int64_t k0row, klen;
                 if (p.unit_page) {
                     k0row = (int64_t)x.page * kBlk;
@@ -465,31 +461,11 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     k0row = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b) : (int64_t)x.b * p.Skv) + x.tok0;
                     klen = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - __ldg(p.cu_k + x.b) : (int64_t)p.Skv) - x.tok0;
                 }
-#pragma unroll 1
-                for (int k0 = QK8 ? 32 : 0; k0 < 64; k0 += 8) {
-                    const int isv = k0 >> 5, rb = r0 + 4 * (k0 & 31);
-                    const uint8_t *pbase = isv ? p.v_packed : p.k_packed;
-                    uint4 pk[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = rb + 4 * i;
-                        const bool in = r < klen && k0row + r < p.kv_rows;
-                        pk[i] = in ? __ldg(reinterpret_cast<const uint4 *>(pbase + ((k0row + r) * p.Hkv + x.h) * 128) + pc)
-                                   : make_uint4(0, 0, 0, 0);
-                    }
-                    // values 16 pc .. 16 pc + 15: column half pc / 4, chunks 2 (pc % 4), + 1
-                    const uint32_t tile = base + (isv ? L::V + kb * 32768 : L::K + kb * KS) + (pc >> 2) * 16384;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        uint4 o4[2];
-                        e4m3x16_to_bf16(pk[i], o4);
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
-                                             tile + tc::sw128_off(rb + 4 * i, (pc & 3) * 2 + c)),
-                                         "r"(o4[c].x), "r"(o4[c].y), "r"(o4[c].z), "r"(o4[c].w));
-                    }
-                }
+                const int nrows = (int)max((int64_t)0, min(min(klen, (int64_t)kBlk), p.kv_rows - k0row));
+                const int64_t first = nrows > 0 ? (k0row * p.Hkv + x.h) * 128 : 0;
+                if constexpr (!QK8)
+                    e4m3_rows_to_tile(base + L::K + kb * KS, p.k_packed + first, (int64_t)p.Hkv * 128, nrows, lane);
+                e4m3_rows_to_tile(base + L::V + kb * 32768, p.v_packed + first, (int64_t)p.Hkv * 128, nrows, lane);
                 } else {
                 // 128 tokens x 4 pieces of 32 values (16 packed bytes, two
                 // scales), for K and then for V.  Lane l converts piece l % 4

@@ -449,6 +449,24 @@ inline bool make_q8_map(CUtensorMap *map, const void *base, int64_t rows, int qp
     return r == CUDA_SUCCESS;
 }
 
+// 3D bf16 view of queries [tokens][Hq][128]: dims {128 elements, Hq heads,
+// tokens} with byte strides {256, Hq*256} and box {64, qpk, 128/qpk}: one copy
+// brings one column half of the qpk heads of a KV head for 128/qpk
+// consecutive tokens as 128 rows (row = token * qpk + head) of 128 bytes,
+// 128-byte swizzled (rows past the last token are zero).
+inline bool make_q_heads_map(CUtensorMap *map, const void *base, int64_t tokens, int Hq, int qpk) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)Hq, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {256, (cuuint64_t)Hq * 256};
+    cuuint32_t box[3] = {64, (cuuint32_t)qpk, (cuuint32_t)(128 / qpk)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2D bf16 map over the query rows [rows][128]: box {64, box_rows}; box_rows
 // = 1 is the gather4 form (four arbitrary rows per copy).
 inline bool make_q_map(CUtensorMap *map, const void *base, int64_t rows, int box_rows) {

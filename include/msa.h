@@ -275,18 +275,21 @@ int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int 
  *   q2k        [B][Hkv][Sq][topk] int32, device; ids >= ceil(seqused_k/page) are padding.
  *   o          [B*Sq][Hq][D] bf16; lse [B*Sq][Hq] fp32 or NULL.
  *   workspace  msa_sparse_attn_paged_fwd_workspace_size() bytes: per group
- *              its union of selected blocks and split table, the work plan
- *              (one unit per union block with its page and query table), and
- *              the split partials (topk per query head).
- * The work: per group (sequence b, KV head h, 128/(Hq/Hkv) consecutive
- * queries) the ascending union of the blocks its queries selected (ids at or
- * past ceil(seqused_k[b]/page) are padding; repeats set MSA_STATUS_DUPLICATE
- * and count once), each query's split ids and counts; then one attention tile
- * per union block holding all the group's queries (rows of queries that did
- * not select the block are masked; consecutive blocks of a group share the Q
- * tile) over the block's physical page (entries outside [0, num_pages) set
- * MSA_STATUS_PAGE_RANGE and the block is skipped); then the LSE combine.
- * Max max_pages: 8192.
+ *              its union of selected blocks with their pages and query
+ *              masks, and per SM two 128-row pieces (O and LSE) of the
+ *              groups the partition cuts.  The size depends on the current
+ *              device's SM count.
+ * The work, in two launches: per group (sequence b, KV head h, 128/(Hq/Hkv)
+ * consecutive queries) the ascending union of the blocks its queries
+ * selected (ids at or past ceil(seqused_k[b]/page) are padding and set
+ * MSA_STATUS_INDEX_RANGE; repeats of one query set MSA_STATUS_DUPLICATE and
+ * count once), each block's physical page (entries outside [0, num_pages)
+ * set MSA_STATUS_PAGE_RANGE and the block is skipped) and the queries that
+ * selected it; then one persistent kernel that streams each group's union
+ * blocks through tensor-core attention with one accumulator per group (rows
+ * of queries that did not select a block get no weight from it) and writes O
+ * and LSE; a group split between CTAs is merged by LSE by the CTA that
+ * finishes it last.  Max max_pages: 8192; at most 49152 groups.
  */
 size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
 int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
@@ -298,13 +301,12 @@ int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_p
 /*
  * General paged decode: as msa_sparse_attn_paged_fwd, plus
  *   kv_format  MSA_KV_BF16, or MSA_KV_FP8 (pools of e4m3 bytes, staged to bf16
- *              on load, exact; sparse mode only);
+ *              on load, exact);
  *   q2k        NULL selects the dense mode (interface.py sparse_decode_atten_func
  *              with q2k_indices = None): every block of each sequence, i.e.
  *              causal attention over all seqused_k[b] keys; topk is then ignored.
- * The dense mode runs the per-group union decode (an online softmax over each
- * group's blocks, partials only where a group is split between CTAs), with the
- * workspace msa_paged_attn_fwd_workspace_size(..., topk = 0, ...).
+ * The workspace is msa_paged_attn_fwd_workspace_size(..., topk, ...), with
+ * topk = 0 for the dense mode.
  */
 size_t msa_paged_attn_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
 int msa_paged_attn_fwd(const void *q, const void *k_pool, const void *v_pool, int kv_format, int num_pages,
