@@ -63,16 +63,12 @@ int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void 
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
         if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
-        // prefill: two K/V stages and three Q stages; paged decode (a unit is
-        // one chunk, its K/V block from HBM; a group's consecutive units share
-        // one Q tile): three K/V stages and one Q
-        if (t.unit_page) return launch_tiles_paged(mk, mv, mq, t, grid, stream);
+        // two K/V stages and three Q stages
         return opts ? launch_tiles_bf16_opts(mk, mv, mq, t, grid, stream)
                     : launch_tiles_bf16(mk, mv, mq, t, grid, stream);
     }
     // NVFP4 / FP8: the dequantising warp reads K and V itself (no K/V maps)
     if (kv_format == MSA_KV_FP8) {
-        if (t.unit_page) return launch_tiles_paged_fp8(mk, mv, mq, t, grid, stream);
         return opts ? launch_tiles_fp8_opts(mk, mv, mq, t, grid, stream) : launch_tiles_fp8(mk, mv, mq, t, grid, stream);
     }
     return opts ? launch_tiles_nvfp4_opts(mk, mv, mq, t, grid, stream)
@@ -322,15 +318,12 @@ TcParams prefill_params(const void *k, const void *v, const void *k_scales, cons
     t.stat_temp = reinterpret_cast<float2 *>(ws + w.stat_temp);
     t.part_dtype = MSA_PARTIAL_BF16;
     t.inv_temp = 1.f;
-    t.seqused = nullptr;
-    t.unit_page = nullptr;
     t.cu_q = t.cu_k = nullptr;
     t.status = status_dev;
     t.Hq = Hq; t.Hkv = Hkv; t.qpk = Hq / Hkv; t.topk = topk;
     t.causal = causal ? 1 : 0;
     t.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
     t.scale_log2 = t.scale * 1.4426950408889634f;
-    t.p_bound = 64.f;
     return t;
 }
 

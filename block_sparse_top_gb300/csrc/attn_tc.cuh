@@ -1,6 +1,6 @@
 // attn_tc.cuh -- the tcgen05 (5th-gen tensor core) block-sparse attention tile
-// kernel (prefill, and paged decode): persistent, one CTA per SM,
-// warp-specialised, 16 warps in prefill and 12 in paged decode.
+// kernel of the prefill forward: persistent, one CTA per SM,
+// warp-specialised, 16 warps.
 //
 //   warp 11     feed: walks the CTA's chunks in plan order and copies each
 //               chunk's plan unit, page and query ids into a 4-entry shared
@@ -27,10 +27,9 @@
 //               applies each split's weight and 1/l in one product.  Packed
 //               f32x2 FMA/add and three-input max halve the per-element
 //               instruction count of the row pass.
-//   warps 12-15 prefill epilogue: once PV has run, each chunk's O = P V (TMEM
-//               lanes of the warp) -> bf16 split partial, so the softmax warps
-//               never wait for PV.  In paged decode (12 warps, whole-row
-//               softmax) the softmax warps store O themselves.
+//   warps 12-15 epilogue: once PV has run, each chunk's O = P V (TMEM lanes
+//               of the warp) -> split partial, so the softmax warps never
+//               wait for PV.
 //
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 // Every wait is bounded; on a timeout the CTA raises MSA_STATUS_TIMEOUT,
@@ -54,10 +53,6 @@ struct TcParams {
     int part_dtype;                       // MSA_PARTIAL_*: storage of the split partials (OPTS instances)
     int temp_on;                          // 1: keep the temperature statistics (OPTS instances)
     float inv_temp;                       // 1 / lse_temperature_scale
-    // paged KV (decode): per-sequence used length and each unit's physical
-    // page (-1: invalid entry, the unit's keys are skipped); null otherwise
-    const int32_t *seqused;
-    const int32_t *unit_page;
     // ragged batches: cu_seqlens of the queries and keys [B+1]; null for a
     // uniform batch (sequence b holds queries b*Sq.. and keys b*Skv..)
     const int32_t *cu_q, *cu_k;
@@ -66,23 +61,17 @@ struct TcParams {
     int64_t cap;
     int64_t kv_rows;  // token rows of the K/V arrays (bound of the dequant loads)
     int64_t total_q;  // query rows of Q (all sequences)
-    // paged decode: largest log2 of a P value against a row's reference max
-    // before the row's accumulated O is rescaled to a new reference
-    float p_bound;
     float scale, scale_log2;
 };
 
 namespace tck {
 
-constexpr int kWarps = 12;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpLoad = 0, kWarpDequant = 1, kWarpMma = 2, kWarpSoftmax0 = 3, kWarpFeed = 11, kWarpEpi0 = 12;
-// Threads of an instance: prefill adds an epilogue warpgroup (warps 12-15)
-// that stores each chunk's O; in paged decode the softmax warps store it.
-constexpr int threads_for(bool paged) { return paged ? kThreads : kThreads + 128; }
 // Chunk ring between the feed warp and the loader: per chunk its plan unit
-// (16 B), the unit's page, its sequence's first key row (ragged batches), and
-// up to 128 query ids (qsplit entries).
+// (16 B), its sequence's first key row (ragged batches, at byte 20), and up
+// to 128 query ids (qsplit entries, from byte 32).
 constexpr int kRing = 4;
 constexpr uint32_t kRingEntry = 32 + 128 * 4;
 
@@ -122,7 +111,7 @@ constexpr int kKvQk8 = 3;
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, 0, 1);
 
 struct Unit {
-    int h, b, tok0, start, count, nch, page;
+    int h, b, tok0, start, count, nch;
 };
 
 __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
@@ -135,26 +124,20 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
     x.count = pu.count;
     int qc = 128 / p.qpk;
     x.nch = (pu.count + qc - 1) / qc;
-    x.page = p.unit_page ? p.unit_page[u] : 0;
     return x;
 }
 
 }  // namespace tck
 
-// NKV, NQ: K/V and Q stages (32 KB tiles; 2 and 3, or 3 and 1, fill the
-// shared memory).  PAGED (paged decode, the plan's units carry pages): each
-// CTA walks one contiguous run of units, consecutive units of a group share
-// one Q tile, and the softmax holds a whole S row in registers (one
-// tensor-memory load, 168 registers) instead of reading it in halves (133) --
-// the shorter chain suits decode, where one warp's rows gate each K/V stage.
-// OPTS (prefill): the instance that serves the forward's options at run
+// NKV, NQ: K/V and Q stages (32 KB tiles; 2 and 3 fill the shared memory).
+// OPTS: the instance that serves the forward's options at run
 // time -- the partials' storage type (bf16, fp16 or fp32) and, with temp_on,
 // the row sum of 2^(x / T), x = (S - m) scale_log2, with its statistics (m
 // scale / T, that sum) for the temperature LSE.  Without OPTS the epilogue
 // stores bf16 and nothing else: the run-time type switch alone cost the
 // 32K causal workload's tiles a tenth of their time.
-template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool OPTS>
-__global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
+template <int KV_FORMAT, int NKV, int NQ, bool OPTS>
+__global__ void __launch_bounds__(tck::kThreads, 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, TcParams p) {
     using namespace tck;
@@ -214,18 +197,14 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + L::TSLOT);
-    // the plan (and, in decode, the query tables) come from the previous kernel
+    // the plan comes from the previous kernel
     grid_dependency_wait();
     grid_dependents_launch();
     const int work = p.plan->work_count;
-    // The CTA's units: every gridDim.x-th of the plan (prefill: consecutive
-    // units read the same K/V head close together in time), or one
-    // contiguous run (paged decode: consecutive units of a group share the Q
-    // tile).  Every role walks the same sequence.
-    constexpr bool contiguous = PAGED;
-    const int u_begin = contiguous ? (int)((int64_t)work * blockIdx.x / gridDim.x) : (int)blockIdx.x;
-    const int u_end = contiguous ? (int)((int64_t)work * (blockIdx.x + 1) / gridDim.x) : work;
-    const int u_step = contiguous ? 1 : (int)gridDim.x;
+    // The CTA's units: every gridDim.x-th of the plan (consecutive units read
+    // the same K/V head close together in time).  Every role walks the same
+    // sequence.
+    const int u_begin = (int)blockIdx.x, u_end = work, u_step = (int)gridDim.x;
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loader
@@ -234,7 +213,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         // load sits on its issue path; issues the unit's K/V on its first
         // chunk and the chunk's Q rows.
         int ci = 0, ui = 0, c = 0;
-        int qn = 0, q_key = -1;  // Q tiles loaded; resident group (paged): first query * Hkv + head
+        int qn = 0;  // Q tiles loaded
         int kv_armed[NKV], q_armed[NQ];  // phase parity of each stage's last copy, -1: none
         for (int i = 0; i < NKV; ++i) kv_armed[i] = -1;
         for (int i = 0; i < NQ; ++i) q_armed[i] = -1;
@@ -253,7 +232,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             x.start = e[2];
             x.count = e[3];
             x.nch = (x.count + qc - 1) / qc;
-            x.page = e[4];
             const int seq_k0 = e[5];  // ragged: first key row of the sequence
             int ids[4];
 #pragma unroll
@@ -270,10 +248,8 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                                        MSA_STATUS_TIMEOUT);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                // token row: the unit's page of the pool, the sequence's keys of
-                // a ragged batch, or dense [B][Skv]
-                const int row = p.unit_page ? x.page * kBlk : (p.cu_k ? seq_k0 : x.b * p.Skv) + x.tok0;
-                const bool copy = !p.unit_page || x.page >= 0;
+                // token row: the sequence's keys of a ragged batch, or dense [B][Skv]
+                const int row = (p.cu_k ? seq_k0 : x.b * p.Skv) + x.tok0;
 #ifdef MSA_TEST_DROP_KV_ARRIVAL
                 // test build only: CTA 0 never signals its first unit's K/V, so
                 // the MMA warp's bounded wait runs out and the CTA aborts
@@ -282,42 +258,30 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 constexpr bool drop = false;
 #endif
                 if (lane == 0 && !drop) {
-                    if (copy)
-                        tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), QK8 ? 16384u : 65536u);
-                    else
-                        tc::mbar_arrive(bar(L::KV_FULL + kb));  // invalid page: no copy, keys masked
+                    tc::mbar_arrive_expect_tx(bar(L::KV_FULL + kb), QK8 ? 16384u : 65536u);
                     kv_armed[kb] = (ui / NKV) & 1;
                 }
                 __syncwarp();
                 if constexpr (QK8) {
                     // e4m3 K by TMA (V is staged to bf16 by the dequantising warp)
-                    if (copy && lane == 0 && !drop)
+                    if (lane == 0 && !drop)
                         tc::tma_load_3d(base + L::K + kb * KS, &tm_k, bar(L::KV_FULL + kb), 0, row, x.h);
                 } else {
                     // lane 0 copies K, lane 1 V, in one instruction
-                    if (copy && lane < 2 && !drop)
+                    if (lane < 2 && !drop)
                         tc::tma_load_4d(base + (lane ? L::V : L::K) + kb * 32768, lane ? &tm_v : &tm_k,
                                         bar(L::KV_FULL + kb), 0, row, 0, x.h);
                 }
             }
-            // Paged decode: a unit is one chunk holding all queries of its group
-            // (rows of queries that did not select the block are masked), so
-            // consecutive units of one group -- same first query, same KV head
-            // -- share the Q tile: it is loaded when the group changes.
             const int first = __shfl_sync(0xffffffffu, ids[0], 0);  // always valid (count > c*qc)
-            const int key = first * p.Hkv + x.h;
-            const bool load_q = !PAGED || key != q_key;
-            q_key = key;
             const int qs = qn % NQ;
-            if (load_q) {
-                if (lane == 0 && qn >= NQ)
-                    ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((qn / NQ) - 1) & 1, abort_flag, p.status,
-                                       MSA_STATUS_TIMEOUT);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                q_armed[qs] = (qn / NQ) & 1;
-                ++qn;
-            }
+            if (lane == 0 && qn >= NQ)
+                ok = tc::mbar_wait(bar(L::Q_EMPTY + qs), ((qn / NQ) - 1) & 1, abort_flag, p.status,
+                                   MSA_STATUS_TIMEOUT);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            q_armed[qs] = (qn / NQ) & 1;
+            ++qn;
             // The chunk's 128 Q rows (row R = query R / qpk of the chunk, head
             // R % qpk of the group), 128-byte swizzled K-major.  qpk >= 8: one
             // 5D box per query holds its whole group (row octets 2048 bytes
@@ -328,11 +292,10 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             // gather4 rows of padding repeat the chunk's first query.
             const uint32_t qt = base + L::Q + qs * QS;
             const int nq = min(qc, x.count - c * qc);
-            if (load_q && lane == 0)
+            if (lane == 0)
                 tc::mbar_arrive_expect_tx(bar(L::Q_FULL + qs),
                                           p.qpk >= 8 ? (uint32_t)(nq * p.qpk * (QK8 ? 128 : 256)) : QS);
-            if (!load_q) {
-            } else if (QK8) {
+            if (QK8) {
                 // e4m3 rows of 128 bytes: one 4D box per query (qpk >= 8: its
                 // row octets 1024 bytes apart), or four rows per gather4
                 if (p.qpk >= 8) {
@@ -406,7 +369,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
         bool ok = true;
         for (int u = u_begin + lane * u_step; u < u_end; u += 32 * u_step) {
             tc::prefetch_l2(p.units + u);
-            if (p.unit_page) tc::prefetch_l2(p.unit_page + u);
         }
         Unit xn{};
         if (u_begin < u_end) xn = load_unit(p, u_begin);
@@ -423,7 +385,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 const uint32_t e = base + L::RING + slot * kRingEntry;
                 if (lane == 0) {
                     cp_async16(e, p.units + u);
-                    if (p.unit_page) cp_async4(e + 16, p.unit_page + u);
                     if (p.cu_k) cp_async4(e + 20, p.cu_k + x.b);
                 }
 #pragma unroll
@@ -450,17 +411,10 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 if constexpr (KV_FORMAT == MSA_KV_FP8 || QK8) {
-                // 128 tokens of e4m3 K (not QK8: that K is copied by TMA) and
-                // V.  Paged: the unit's page of the pool (an invalid page
-                // gives zeros; its keys are masked), all 128 rows.
-                int64_t k0row, klen;
-                if (p.unit_page) {
-                    k0row = (int64_t)x.page * kBlk;
-                    klen = x.page >= 0 ? kBlk : 0;
-                } else {
-                    k0row = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b) : (int64_t)x.b * p.Skv) + x.tok0;
-                    klen = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - __ldg(p.cu_k + x.b) : (int64_t)p.Skv) - x.tok0;
-                }
+                // 128 tokens of e4m3 K (not QK8: that K is copied by TMA) and V
+                const int64_t k0row = (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b) : (int64_t)x.b * p.Skv) + x.tok0;
+                const int64_t klen =
+                    (p.cu_k ? (int64_t)__ldg(p.cu_k + x.b + 1) - __ldg(p.cu_k + x.b) : (int64_t)p.Skv) - x.tok0;
                 const int nrows = (int)max((int64_t)0, min(min(klen, (int64_t)kBlk), p.kv_rows - k0row));
                 const int64_t first = nrows > 0 ? (k0row * p.Hkv + x.h) * 128 : 0;
                 if constexpr (!QK8)
@@ -519,7 +473,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             int ci = 0, ui = 0;
             bool ok = true;
             int pv_ci = -1, pv_kb = 0, pv_last = 0;
-            bool pv_cont = false;  // paged: PV accumulates onto the warpgroup's O
             // Q tile geometry (see the loader): octet stride and half offset
             const uint32_t q_sbo = (p.qpk >= 8 && !QK8) ? 2048u : 1024u, q_half = p.qpk >= 8 ? 1024u : 16384u;
             auto pv_ready = [&](int cj) -> bool {
@@ -534,7 +487,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
-                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, (kk > 0 || pv_cont) ? 1u : 0u);
+                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, kk > 0 ? 1u : 0u);
                 tc::mma_commit(bar(L::O_FULL + b));
                 if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
@@ -591,49 +544,20 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 set_status(p.status, MSA_STATUS_TIMEOUT);
                 return false;
             };
-            // Q tiles as the loader issues them: one per chunk, or (paged
-            // decode) one per run of consecutive units of one group, told apart
-            // by first query * Hkv + head (read one unit ahead)
-            auto first_query = [&](const Unit &y) -> int64_t {
-                return PAGED ? (int64_t)(__ldg(p.qsplit + (int64_t)y.h * p.cap + y.start) & 0xFFFFFF) * p.Hkv + y.h : 0;
-            };
+            // Q tiles as the loader issues them: one per chunk
             int qn = -1;
-            int64_t q_first = -1, key_m1 = -1, key_m2 = -1;  // paged: group keys of units ci-1, ci-2
             Unit xnext{};
-            int64_t fnext = -1;
-            if (u_begin < u_end) {
-                xnext = load_unit(p, u_begin);
-                fnext = first_query(xnext);
-            }
+            if (u_begin < u_end) xnext = load_unit(p, u_begin);
             for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
                 const Unit x = xnext;
-                const int64_t fx = fnext;
-                const bool has_next = u + u_step < u_end;
-                if (has_next) {
-                    xnext = load_unit(p, u + u_step);
-                    fnext = first_query(xnext);
-                }
+                if (u + u_step < u_end) xnext = load_unit(p, u + u_step);
                 const int kb = ui % NKV;
                 for (int c = 0; c < x.nch && ok; ++c, ++ci) {
-                    bool release_q = true;
-                    if constexpr (!PAGED) {
-                        ++qn;
-                    } else {
-                        if (fx != q_first || c > 0) ++qn;  // (a paged unit is one chunk)
-                        q_first = fx;
-                        release_q = c < x.nch - 1 || !has_next || fnext != fx;
-                    }
-                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1, qn, release_q);
+                    ++qn;
+                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1, qn, true);
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
-                    if constexpr (PAGED) {
-                        // a warpgroup's consecutive units of one group (ci - 2,
-                        // ci) accumulate into its O buffer
-                        pv_cont = ci >= 2 && fx == key_m2;
-                        key_m2 = key_m1;
-                        key_m1 = fx;
-                    }
                 }
             }
             if (ok && pv_ci >= 0) drive(-1, 0, false, 0, 0, false);
@@ -643,8 +567,8 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             tc::mbar_wait(bar(L::DRAIN), 0, &dummy, p.status, MSA_STATUS_TIMEOUT);
         }
         __syncwarp();
-    } else if (!PAGED && warp >= kWarpEpi0) {
-        // ------------------------------------------------------------------ epilogue (prefill)
+    } else if (warp >= kWarpEpi0) {
+        // ------------------------------------------------------------------ epilogue
         // Chunk ci's O (TMEM lanes of this warp, buffer ci % 2) -> bf16 split
         // partial, once PV has run; frees the O buffer for the chunk two later.
         // The softmax warps store the statistics, so they never wait for PV.
@@ -727,25 +651,20 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             }
         }
     } else {
-        // ------------------------------------------------------------------ softmax (+ epilogue in decode)
+        // ------------------------------------------------------------------ softmax
         const int wg = (warp - kWarpSoftmax0) >> 2;  // 0: even chunks, 1: odd chunks
         const int R = 32 * (warp & 3) + lane;        // chunk row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t s_addr = tmem + lane_base + wg * 128;
-        const uint32_t o_addr = tmem + lane_base + 256 + wg * 128;
         const int j_of_row = R % p.qpk;  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
         // the unit and, loaded one unit ahead, its sequence's key count kv
-        // (paged: seqused[b]; ragged: from cu_seqlens_k) and cb = kv - (first
-        // query + query count) of the sequence: global query gq sees keys up to
-        // min(kv - 1, gq + cb) (bottom-right causal: local query s sees keys up
-        // to s + kv - Sq)
+        // (ragged: from cu_seqlens_k) and cb = kv - (first query + query
+        // count) of the sequence: global query gq sees keys up to min(kv - 1,
+        // gq + cb) (bottom-right causal: local query s sees keys up to s + kv
+        // - Sq)
         auto seq_of = [&](const Unit &y) -> int2 {
-            if (PAGED) {
-                const int kv = __ldg(p.seqused + y.b);
-                return make_int2(kv, kv - (y.b + 1) * p.Sq);
-            }
             if (p.cu_k) {
                 const int kv = __ldg(p.cu_k + y.b + 1) - __ldg(p.cu_k + y.b);
                 return make_int2(kv, kv - __ldg(p.cu_q + y.b + 1));
@@ -758,61 +677,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
             xnext = load_unit(p, u_begin);
             seqnext = seq_of(xnext);
         }
-        // paged decode: this warpgroup accumulates O over its consecutive units
-        // of one group (a piece); per row: the reference max, the sum of P, the
-        // row's piece (partial slot, -1 while it selected nothing) and its
-        // (query, KV head) group
-        float m_acc = -INFINITY, l_acc = 0.f, lr_acc = 0.f;  // reference, sum of P, sum of the rounded P
-        int piece_acc = -1, gq_acc = 0, h_acc = 0;
-        // group key of a unit: first query | (KV head mod 128) << 24 (query
-        // ids are below 2^24; the units compared, this warpgroup's consecutive
-        // ones, are at most two groups apart, so their heads differ mod 128)
-        int key_prev = -1;
-        int ci_prev = -1;  // this warpgroup's previous unit
-        // writes the rows' pieces and starts a new piece; the O buffer holds
-        // every PV of the piece (its last one has completed).  A piece is the
-        // fp32 partial U * (l / lr) with statistics (m scale, l): U sums the
-        // rounded P, so dividing by their sum lr makes each P's weight
-        // consistent, while l, the sum of the unrounded P, keeps the LSE exact
-        auto finalize = [&]() {
-            if constexpr (PAGED) {
-                if (__any_sync(0xffffffffu, piece_acc >= 0)) {
-                    const int64_t grp_acc = (int64_t)gq_acc * p.Hkv + h_acc;
-                    // piece of chunk c at float4 index 2 (index + c qpk) (32-byte pieces)
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part) +
-                                  2 * part_o_index(grp_acc, p.topk, p.qpk, piece_acc < 0 ? 0 : piece_acc, 0, j_of_row);
-                    const float fac = lr_acc > 0.f ? l_acc / lr_acc : 0.f;
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t po[64];
-                        tc::tmem_ld64(o_addr + 64 * hf, po);
-                        tc::tmem_ld_wait();
-                        if (piece_acc >= 0) {
-#pragma unroll
-                            for (int v4 = 0; v4 < 8; ++v4) {
-                                float4 *d = dst + (int64_t)2 * (8 * hf + v4) * p.qpk;
-                                __stcs(d, make_float4(__uint_as_float(po[8 * v4 + 0]) * fac,
-                                                      __uint_as_float(po[8 * v4 + 1]) * fac,
-                                                      __uint_as_float(po[8 * v4 + 2]) * fac,
-                                                      __uint_as_float(po[8 * v4 + 3]) * fac));
-                                __stcs(d + 1, make_float4(__uint_as_float(po[8 * v4 + 4]) * fac,
-                                                          __uint_as_float(po[8 * v4 + 5]) * fac,
-                                                          __uint_as_float(po[8 * v4 + 6]) * fac,
-                                                          __uint_as_float(po[8 * v4 + 7]) * fac));
-                            }
-                        }
-                    }
-                    if (piece_acc >= 0) {
-                        const float2 st = make_float2(l_acc > 0.f ? m_acc * p.scale : -INFINITY, l_acc);
-                        __stcs(p.stat_part + part_stat_index(grp_acc, p.topk, p.qpk, piece_acc, j_of_row), st);
-                    }
-                }
-                m_acc = -INFINITY;
-                l_acc = 0.f;
-                lr_acc = 0.f;
-                piece_acc = -1;
-            }
-        };
         for (int u = u_begin; u < u_end && ok; u += u_step) {
             const Unit x = xnext;
             const int kv_len = seqnext.x, seq_cb = seqnext.y;
@@ -826,131 +690,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                 const int qi = R / p.qpk, idx = c * qc + qi;
                 const bool in_chunk = idx < x.count;
                 const int packed = in_chunk ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
-                // split 255: a query of a paged unit's group that did not select the block
-                const bool valid = in_chunk && (!PAGED || ((uint32_t)packed >> 24) != 0xFFu);
-                if constexpr (PAGED) {
-                    // -------- paged decode: pieces accumulate in the O buffer
-                    const int key = (__ldg(p.qsplit + x.start) & 0xFFFFFF) | ((x.h & 127) << 24);
-                    ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    if (ci_prev >= 0) {
-                        // the PV of this warpgroup's previous unit has completed
-                        ok = tc::mbar_wait(bar(L::O_FULL + wg), (ci_prev >> 1) & 1, abort_flag, p.status,
-                                           MSA_STATUS_TIMEOUT);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        tc::fence_after_sync();
-                        if (key != key_prev) finalize();  // a new group: its PV overwrites O
-                    }
-                    // the S row (rows of queries that did not select the block
-                    // and padding rows: P = 0)
-                    const bool any_sel = __any_sync(0xffffffffu, valid);
-                    const int gq = packed & 0xFFFFFF;
-                    int nvis = 0;
-                    if (valid && x.page >= 0) {
-                        // keys of the block visible to query gq
-                        int limit = kv_len - 1;
-                        if (p.causal) limit = min(limit, gq + seq_cb);
-                        const int nv = limit - x.tok0 + 1;
-                        nvis = nv < 0 ? 0 : (nv > 128 ? 128 : nv);
-                    }
-                    uint32_t pr[128];
-                    float l = 0.f, lround = 0.f;
-                    if (any_sel) {
-#define MSA_LOAD_S_ROW()                                                 \
-    do {                                                                 \
-        tc::tmem_ld128(s_addr, pr);                                      \
-        tc::tmem_ld_wait();                                              \
-        if (nvis < 128) {                                                \
-            _Pragma("unroll") for (int j = 0; j < 128; ++j) if (j >= nvis) pr[j] = 0xff800000u; \
-        }                                                                \
-    } while (0)
-                        MSA_LOAD_S_ROW();
-                        float mm[4];
-#pragma unroll
-                        for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < 128; j += 8) {
-#pragma unroll
-                            for (int a = 0; a < 4; ++a)
-                                mm[a] = fmax3(mm[a], __uint_as_float(pr[j + 2 * a]), __uint_as_float(pr[j + 2 * a + 1]));
-                        }
-                        const float mh = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                        // a row whose max exceeds its reference by more than the
-                        // bound (rare): its O row and sum are rescaled to the new
-                        // max (O is stable: the previous PV has completed, the
-                        // next waits for O_EMPTY below)
-                        const bool grow = valid && m_acc != -INFINITY && (mh - m_acc) * p.scale_log2 > p.p_bound;
-                        if (__any_sync(0xffffffffu, grow)) {
-                            const float f = grow ? ex2_approx((m_acc - mh) * p.scale_log2) : 1.f;
-                            if (grow) {
-                                l_acc *= f;
-                                lr_acc *= f;
-                                m_acc = mh;
-                            }
-#pragma unroll 1
-                            for (int hf = 0; hf < 2; ++hf) {
-                                uint32_t po[64];
-                                tc::tmem_ld64(o_addr + 64 * hf, po);
-                                tc::tmem_ld_wait();
-#pragma unroll
-                                for (int j = 0; j < 64; ++j) po[j] = __float_as_uint(__uint_as_float(po[j]) * f);
-                                tc::tmem_st64h(o_addr + 64 * hf, po);
-                            }
-                            tc::tmem_st_wait();
-                            MSA_LOAD_S_ROW();
-                        }
-#undef MSA_LOAD_S_ROW
-                        if (valid && m_acc == -INFINITY) m_acc = mh;  // the piece's first visible keys of the row
-                        if (ci_prev >= 0) {
-                            tc::fence_before_sync();
-                            tc::mbar_arrive(bar(L::O_EMPTY + wg));  // O is read: this unit's PV may start
-                        }
-                        // P = exp2((S - m) scale_log2) packed to bf16 in place
-                        // (pr[j] <- keys 2j, 2j+1); the sums of P and of the
-                        // rounded P that PV uses (against a reference below the
-                        // row max the largest P is not 1)
-                        const float mc = (m_acc == -INFINITY) ? 0.f : m_acc * p.scale_log2;
-                        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-                        const float2 nm2 = make_float2(-mc, -mc);
-                        float2 ll = make_float2(0.f, 0.f), lr = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) {
-                            float2 e = __ffma2_rn(make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])),
-                                                  sc2, nm2);
-                            e.x = ex2_approx(e.x);
-                            e.y = ex2_approx(e.y);
-                            ll = __fadd2_rn(ll, e);
-                            pr[j] = pack_bf16x2(e.x, e.y);
-                            lr = __fadd2_rn(lr, make_float2(bf16_lo(pr[j]), bf16_hi(pr[j])));
-                        }
-                        l = ll.x + ll.y;
-                        lround = lr.x + lr.y;
-                    } else {
-                        if (ci_prev >= 0) {
-                            tc::fence_before_sync();
-                            tc::mbar_arrive(bar(L::O_EMPTY + wg));
-                        }
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) pr[j] = 0u;  // no row selects the block: P = 0
-                    }
-                    tc::tmem_st64(s_addr, pr);
-                    tc::tmem_st_wait();
-                    tc::fence_before_sync();
-                    tc::mbar_arrive(bar(L::P_FULL + wg));
-                    if (valid) {
-                        l_acc += l;
-                        lr_acc += lround;
-                        piece_acc = (packed >> 24) & 0xFF;
-                        gq_acc = gq;
-                        h_acc = x.h;
-                    }
-                    key_prev = key;
-                    ci_prev = ci;
-                    continue;
-                }
+                const bool valid = in_chunk;
                 ok = tc::mbar_wait(bar(L::S_FULL + wg), par, abort_flag, p.status, MSA_STATUS_TIMEOUT);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -973,7 +713,7 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                     const int gq = packed & 0xFFFFFF;
                     const int split = (packed >> 24) & 0xFF;
                     int nvis = 0;
-                    if (valid && (!p.unit_page || x.page >= 0)) {
+                    if (valid) {
                         // keys of the block visible to query gq
                         int limit = kv_len - 1;
                         if (p.causal) limit = min(limit, gq + seq_cb);
@@ -1051,17 +791,6 @@ __global__ void __launch_bounds__(tck::threads_for(PAGED), 1)
                             __stcs(p.stat_temp + si, make_float2(ltt > 0.f ? m * p.scale * p.inv_temp : -INFINITY, ltt));
                         }
                     }
-                }
-            }
-        }
-        if constexpr (PAGED) {
-            // the warpgroup's last piece, once its last PV has completed
-            if (ok && ci_prev >= 0) {
-                ok = tc::mbar_wait(bar(L::O_FULL + wg), (ci_prev >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
-                    tc::fence_after_sync();
-                    finalize();
                 }
             }
         }

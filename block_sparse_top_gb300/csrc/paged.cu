@@ -5,7 +5,7 @@
 #include <cstring>
 
 #include "paged_tc.cuh"
-#include "tiles.h"
+#include "tiles.h"  // num_sms
 
 namespace msa {
 

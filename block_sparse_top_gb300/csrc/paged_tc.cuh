@@ -710,36 +710,55 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 }
                 tc::named_bar_sync(1, 128);
                 if (*merge_flag) {
-                    // warp-cooperative: each warp merges 32 rows, lane l dims 4l .. 4l + 3
-                    const int ew = et >> 5;
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int r = ew * 32 + rr, rq = r / p.qpk;
-                        if (rq >= x.nq) continue;
-                        float mx = -INFINITY;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const int sl = (cc > c_first || (long long)off == total * cc / grid) ? 0 : 1;
-                            mx = fmaxf(mx, __ldcg(p.slot_lse + ((int64_t)cc * 2 + sl) * 128 + r));
+                    // Warp-cooperative: each warp merges its 32 rows, eight at a
+                    // time, lane l holding dims 4l .. 4l + 3; the pieces are
+                    // folded in one pass with a running max, two pieces' loads
+                    // in flight together.
+                    const int npc = c_last - c_first + 1;
+                    for (int r0 = (et >> 5) * 32; r0 < (et >> 5) * 32 + 32; r0 += 8) {
+                        float mr[8], den[8];
+                        float4 acc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            mr[i] = -INFINITY;
+                            den[i] = 0.f;
+                            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        float den = 0.f;
-                        if (mx != -INFINITY) {
-                            for (int cc = c_first; cc <= c_last; ++cc) {
-                                const int sl = (cc > c_first || (long long)off == total * cc / grid) ? 0 : 1;
-                                const int64_t rb = ((int64_t)cc * 2 + sl) * 128 + r;
-                                const float wgt = __expf(__ldcg(p.slot_lse + rb) - mx);
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.slot_o + rb * kD) + lane);
-                                acc.x += wgt * v.x;
-                                acc.y += wgt * v.y;
-                                acc.z += wgt * v.z;
-                                acc.w += wgt * v.w;
-                                den += wgt;
+#pragma unroll 2
+                        for (int k2 = 0; k2 < npc; ++k2) {
+                            const int cc = c_first + k2;
+                            const int sl = (cc > c_first || (long long)off == total * cc / grid) ? 0 : 1;
+                            const int64_t rb = ((int64_t)cc * 2 + sl) * 128 + r0;
+                            float lv[8];
+                            float4 ov[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                lv[i] = __ldcg(p.slot_lse + rb + i);
+                                ov[i] = __ldcg(reinterpret_cast<const float4 *>(p.slot_o + (rb + i) * kD) + lane);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float mn = fmaxf(mr[i], lv[i]);
+                                if (mn != -INFINITY) {  // the same for every lane (one row)
+                                    const float a = __expf(mr[i] - mn), bw = __expf(lv[i] - mn);
+                                    acc[i] = make_float4(acc[i].x * a + ov[i].x * bw, acc[i].y * a + ov[i].y * bw,
+                                                         acc[i].z * a + ov[i].z * bw, acc[i].w * a + ov[i].w * bw);
+                                    den[i] = den[i] * a + bw;
+                                    mr[i] = mn;
+                                }
                             }
                         }
-                        const float inv = den > 0.f ? 1.f / den : 0.f;
-                        const int64_t orr = ((int64_t)x.b * p.Sq + x.q0 + rq) * p.Hq + x.h * p.qpk + r % p.qpk;
-                        reinterpret_cast<uint2 *>(p.o + orr * kD)[lane] =
-                            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-                        if (p.lse && lane == 0) p.lse[orr] = den > 0.f ? mx + __logf(den) : -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int r = r0 + i, rq = r / p.qpk;
+                            if (rq >= x.nq) continue;
+                            const float inv = den[i] > 0.f ? 1.f / den[i] : 0.f;
+                            const int64_t orr = ((int64_t)x.b * p.Sq + x.q0 + rq) * p.Hq + x.h * p.qpk + r % p.qpk;
+                            reinterpret_cast<uint2 *>(p.o + orr * kD)[lane] =
+                                make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                                           pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+                            if (p.lse && lane == 0) p.lse[orr] = den[i] > 0.f ? mr[i] + __logf(den[i]) : -INFINITY;
+                        }
                     }
                 }
             }

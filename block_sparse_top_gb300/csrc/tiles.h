@@ -1,5 +1,5 @@
-// tiles.h -- host-side pieces of the attention tile pipeline shared by the
-// prefill (attn.cu) and the paged decode (paged.cu).
+// tiles.h -- host-side pieces of the prefill attention tile pipeline
+// (attn.cu, the tiles_*.cu instances).
 #pragma once
 #include "attn_tc.cuh"
 
@@ -43,19 +43,17 @@ MSA_TILE_INSTANCE(launch_tiles_fp8);
 MSA_TILE_INSTANCE(launch_tiles_fp8_opts);
 MSA_TILE_INSTANCE(launch_tiles_qk8);
 MSA_TILE_INSTANCE(launch_tiles_qk8_opts);
-MSA_TILE_INSTANCE(launch_tiles_paged);
-MSA_TILE_INSTANCE(launch_tiles_paged_fp8);
 
-// The launch of instance <KV_FORMAT, NKV, NQ, PAGED, OPTS> (used by tiles_*.cu).
-template <int KV_FORMAT, int NKV, int NQ, bool PAGED, bool OPTS>
+// The launch of instance <KV_FORMAT, NKV, NQ, OPTS> (used by tiles_*.cu).
+template <int KV_FORMAT, int NKV, int NQ, bool OPTS>
 int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
                  cudaStream_t stream) {
     constexpr uint32_t S = KV_FORMAT == tck::kKvQk8 ? 16384u : 32768u;  // K and Q stage bytes
     const size_t smem = tck::Layout<NKV, NQ, S, S>::BYTES;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, OPTS>,
+    MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, OPTS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, PAGED, OPTS>, dim3(grid),
-                            dim3(tck::threads_for(PAGED)), smem, stream, mk, mv, mq, t));
+    MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, OPTS>, dim3(grid),
+                            dim3(tck::kThreads), smem, stream, mk, mv, mq, t));
     return MSA_OK;
 }
 

@@ -2,5 +2,5 @@
 #include "tiles.h"
 
 namespace msa {
-MSA_TILE_INSTANCE(launch_tiles_qk8) { return launch_tiles<tck::kKvQk8, 3, 4, false, false>(mk, mv, mq, t, grid, stream); }
+MSA_TILE_INSTANCE(launch_tiles_qk8) { return launch_tiles<tck::kKvQk8, 3, 4, false>(mk, mv, mq, t, grid, stream); }
 }  // namespace msa
