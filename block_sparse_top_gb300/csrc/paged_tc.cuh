@@ -23,16 +23,17 @@
 //                   O += P V into the group's O buffer (two, alternating by
 //                   group), P read from tensor memory;
 //       warp 2      e4m3 pools only: stages K and V to bf16 in the ring;
-//       warps 4-7   softmax, one S row per thread: rows whose query did not
-//                   select the block get P = 0; each row keeps a reference
-//                   max for the whole group and rescales its O row only when
-//                   a block's max exceeds it by more than 2^p_bound;
-//       warps 8-11  epilogue: at the end of a group, O / (sum of P) and the
-//                   LSE; a group the CTA holds whole goes straight to the
-//                   output, a group cut by the partition leaves one piece per
-//                   CTA and the CTA that writes its last piece merges them by
-//                   LSE (an atomic count per group), so no further launch
-//                   and no per-block partials.
+//       warps 4-11  softmax, two warpgroups splitting each S row (keys 0-63
+//                   and 64-127 of the same TMEM lanes) and agreeing on one
+//                   reference max per row: rows whose query did not select
+//                   the block get P = 0, and a row's O is rescaled only when
+//                   a block's max exceeds the reference by more than
+//                   2^p_bound.  At the end of a group they write O / (sum of
+//                   P) and the LSE: a group the CTA holds whole goes straight
+//                   to the output; a group cut by the partition leaves one
+//                   piece per CTA, and the CTA that writes its last piece
+//                   merges them by LSE (an atomic count per group), so there
+//                   is no further launch and no per-block partial.
 //
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
 // Every wait is bounded; on a timeout the CTA raises MSA_STATUS_TIMEOUT,
@@ -98,13 +99,15 @@ __device__ __forceinline__ uint32_t ld_plan(const uint32_t *p) { return __ldcg(p
 namespace pdk {
 
 constexpr int kNKV = 3;  // K/V ring stages
+// 12 warps (three per SM sub-partition: 168 registers a thread); TMEM lane
+// quarter = warp % 4, so each warpgroup covers all 128 rows.
 constexpr int kWarps = 12, kThreads = kWarps * 32;
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpDequant = 2, kWarpSoftmax0 = 4, kWarpEpi0 = 8;
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpDequant = 2, kWarpSoftmax0 = 4;
 constexpr int kMaxGroups = 49152;  // the partition's prefix lives in the K/V ring before the pipeline starts
 constexpr int kMinShare = 8;       // fewest units of a CTA's share in the balanced partition
 
 // Shared memory: K [3] | V [3] | Q | mbarriers | TMEM slot | abort flag |
-// walk start | merge flag | row statistics [2][128] (float2).
+// walk start | merge flag.
 struct Layout {
     static constexpr uint32_t K = 0, V = kNKV * 32768u, Q = 2 * kNKV * 32768u, BAR = Q + 32768u;
     enum : int {
@@ -115,14 +118,12 @@ struct Layout {
         S_FULL,
         P_FULL = S_FULL + 2,
         O_FULL = P_FULL + 2,
-        O_EMPTY = O_FULL + 2,
-        ST_FULL = O_EMPTY + 2,
-        PV_DONE = ST_FULL + 2,
+        PV_DONE = O_FULL + 2,
         DRAIN,
         NBAR
     };
     static constexpr uint32_t TSLOT = BAR + 8 * NBAR, ABORT = TSLOT + 4, WALK = ABORT + 4, MERGE = WALK + 48,
-                              STAT = (MERGE + 4 + 15) & ~15u, BYTES = STAT + 2 * 128 * 8;
+                              BYTES = MERGE + 4;
     static_assert(BYTES <= 232448, "shared memory budget");
 };
 
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + L::ABORT);
     WalkStart *ws = reinterpret_cast<WalkStart *>(gbase + L::WALK);
     volatile int *merge_flag = reinterpret_cast<volatile int *>(gbase + L::MERGE);
-    float2 *stat = reinterpret_cast<float2 *>(gbase + L::STAT);
     auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -222,10 +222,8 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
         tc::mbar_init(bar(L::Q_EMPTY), 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar(L::S_FULL + i), 1);
-            tc::mbar_init(bar(L::P_FULL + i), 128);
+            tc::mbar_init(bar(L::P_FULL + i), 256);  // both softmax warpgroups
             tc::mbar_init(bar(L::O_FULL + i), 1);
-            tc::mbar_init(bar(L::O_EMPTY + i), 128);
-            tc::mbar_init(bar(L::ST_FULL + i), 128);
         }
         tc::mbar_init(bar(L::PV_DONE), 1);
         tc::mbar_init(bar(L::DRAIN), 1);
@@ -430,18 +428,17 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
             bool ok = true;
             int pv_k = -1, pv_s = 0, pv_pc = 0;
             bool pv_first = false, pv_last = false;
-            auto pv_ready = [&]() -> bool {
-                if (!tc::mbar_test(bar(L::P_FULL + (pv_k & 1)), (pv_k >> 1) & 1)) return false;
-                // a group's first PV overwrites the O buffer: the epilogue has read it (group pc - 2)
-                return !pv_first || pv_pc < 2 || tc::mbar_test(bar(L::O_EMPTY + (pv_pc & 1)), ((pv_pc >> 1) - 1) & 1);
-            };
+            // (a group's first PV overwrites the O buffer of group pc - 2, which
+            // the softmax warps have read before they wrote this P)
+            auto pv_ready = [&]() -> bool { return tc::mbar_test(bar(L::P_FULL + (pv_k & 1)), (pv_k >> 1) & 1); };
             auto issue_pv = [&]() {
                 tc::fence_after_sync();
                 const uint32_t vs = base + L::V + pv_s * 32768, ob = tmem + 256 + (pv_pc & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ts(ob, tmem + (pv_k & 1) * 128 + kk * 8, tc::sdesc_sw128(vs + kk * 2048, 16384, 1024),
-                               kIdescPV, (kk > 0 || !pv_first) ? 1u : 0u);
+                    // P of keys 16 kk .. 16 kk + 15: packed columns of key half kk / 4 (at 0 and 64)
+                    tc::mma_ts(ob, tmem + (pv_k & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, (kk > 0 || !pv_first) ? 1u : 0u);
                 tc::mma_commit(bar(L::KV_EMPTY + pv_s));
                 tc::mma_commit(bar(L::PV_DONE));
                 if (pv_last) tc::mma_commit(bar(L::O_FULL + (pv_pc & 1)));
@@ -505,10 +502,17 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
             tc::mbar_wait(bar(L::DRAIN), 0, &dummy, p.status, MSA_STATUS_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp >= kWarpSoftmax0 && warp < kWarpEpi0) {
+    } else if (warp >= kWarpSoftmax0) {
         // ------------------------------------------------------------------ softmax
-        const int R = 32 * (warp & 3) + lane;  // row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        // Two warpgroups split each S row: warps 4-7 keys 0-63, warps 8-11
+        // keys 64-127 of the same rows (TMEM lanes).  The two warps of a row
+        // quarter exchange their half maxima through the unit's K tile, which
+        // S has read and which is not reloaded before this unit's P is
+        // complete, and agree on one reference max per row.
+        const int hs = (warp - kWarpSoftmax0) >> 2;  // key half
+        const int q4 = warp & 3;
+        const int R = 32 * q4 + lane;  // row = TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const int qi = R / p.qpk;
         Walk w;
         bool more = walk_begin(w, wstart);
@@ -516,13 +520,16 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
         bool ok = true;
         DGroup x{};
         int kv = 0;
-        // per row, over the group: reference max (raw score), sum of P, sum of the rounded P
+        int pg = 0, pj0 = 0, pj1 = 0, pof = 0, pn = 0;  // the group: id, this CTA's units [pj0, pj1), first unit, units
+        // per row, over the group: reference max (raw score, the same in both
+        // halves), this half's sum of P and of the rounded P
         float m_ref = -INFINITY, l_acc = 0.f, lr_acc = 0.f;
         // the unit's block and its selecting queries, loaded one unit ahead
         int64_t ui = more ? (int64_t)w.g * p.maxu + w.j : 0;
         int blk_n = more ? ld_plan(p.ublk + ui) : 0, page_n = more ? ld_plan(p.upage + ui) : 0;
         uint32_t mw_n = more ? ld_plan(p.umask + ui * p.wq + (qi >> 5)) : 0u;
-        while (more && ok) {
+        // (the loop is left only at a barrier of all eight warps)
+        while (more) {
             const bool first = w.j == w.j0, last = w.j == w.jend - 1;
             if (first) {
                 ++pc;
@@ -530,6 +537,11 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 kv = __ldg(p.seqused + x.b);
                 m_ref = -INFINITY;
                 l_acc = lr_acc = 0.f;
+                pg = w.g;
+                pj0 = w.j0;
+                pj1 = w.jend;
+                pof = w.off;
+                pn = w.n;
             }
             const int blk = blk_n, page = page_n;
             const uint32_t mw = mw_n;
@@ -541,8 +553,10 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 mw_n = ld_plan(p.umask + ui * p.wq + (qi >> 5));
             }
             const int b = k & 1;
-            const uint32_t s_addr = tmem + lane_base + b * 128;
-            const uint32_t o_addr = tmem + lane_base + 256 + (pc & 1) * 128;
+            // this half's 64 S columns; its packed P goes to the first 32 of them
+            const uint32_t s_addr = tmem + lane_base + b * 128 + hs * 64;
+            const uint32_t o_addr = tmem + lane_base + 256 + (pc & 1) * 128 + hs * 64;
+            float *xch = reinterpret_cast<float *>(gbase + L::K + (k % kNKV) * 32768);
             // keys of the block visible to this row's query (0: not selected)
             int nvis = 0;
             if (qi < x.nq && ((mw >> (qi & 31)) & 1u) && page >= 0) {
@@ -550,71 +564,90 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 if (p.causal) limit = min(limit, kv - p.Sq + x.q0 + qi);  // bottom-right causal
                 nvis = min(max(limit - blk * kBlk + 1, 0), kBlk);
             }
-            ok = tc::mbar_wait(bar(L::S_FULL + b), (k >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+            const int nh = nvis - 64 * hs;  // visible keys of this half (may be <= 0 or > 64)
+            ok = ok && tc::mbar_wait(bar(L::S_FULL + b), (k >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
             tc::fence_after_sync();
-            uint32_t pr[128];
-            if (__any_sync(0xffffffffu, nvis > 0)) {
-#define MSA_LOAD_S_ROW()                                                                        \
-    do {                                                                                        \
-        tc::tmem_ld128(s_addr, pr);                                                             \
-        tc::tmem_ld_wait();                                                                     \
-        if (nvis < 128) {                                                                       \
-            _Pragma("unroll") for (int j = 0; j < 128; ++j) if (j >= nvis) pr[j] = 0xff800000u; \
-        }                                                                                       \
+            uint32_t pr[64];
+            // (the same in both warps of the pair: nvis depends on the row only)
+            const bool active = __any_sync(0xffffffffu, nvis > 0);
+            // Every named barrier is reached by all the warps it names or by
+            // none: the one per unit spans both warpgroups and carries their
+            // `ok`, so all eight leave together when one has given up; after
+            // it nothing leaves the loop before the next one.
+            float mhalf = -INFINITY;
+            if (active && ok) {
+#define MSA_LOAD_S_HALF()                                                                    \
+    do {                                                                                     \
+        tc::tmem_ld64(s_addr, pr);                                                           \
+        tc::tmem_ld_wait();                                                                  \
+        if (nh < 64) {                                                                       \
+            _Pragma("unroll") for (int j = 0; j < 64; ++j) if (j >= nh) pr[j] = 0xff800000u; \
+        }                                                                                    \
     } while (0)
-                MSA_LOAD_S_ROW();
+                MSA_LOAD_S_HALF();
                 float mm[4];
 #pragma unroll
                 for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 128; j += 8) {
+                for (int j = 0; j < 64; j += 8) {
 #pragma unroll
                     for (int a = 0; a < 4; ++a)
                         mm[a] = fmax3(mm[a], __uint_as_float(pr[j + 2 * a]), __uint_as_float(pr[j + 2 * a + 1]));
                 }
-                const float mh = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                mhalf = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                xch[hs * 128 + R] = mhalf;
+            }
+            ok = pdk::bar_and(1, 256, ok);
+            if (!ok) break;
+            if (active) {
+                const float mh = fmaxf(mhalf, xch[(1 - hs) * 128 + R]);
                 // a row whose block max exceeds its reference by more than the
                 // bound (rare): its O row and sums are rescaled to the new max
                 // once the group's previous PV has completed (the next PV waits
-                // for this unit's P)
+                // for this unit's P); both halves decide alike
                 const bool grow = nvis > 0 && m_ref != -INFINITY && (mh - m_ref) * p.scale_log2 > p.p_bound;
                 if (__any_sync(0xffffffffu, grow)) {
+                    bool okp = true;
                     if (!first) {
-                        ok = tc::mbar_wait(bar(L::PV_DONE), (k - 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
+                        // (both warps of the pair take this path alike: grow
+                        // follows from the shared maximum and reference)
+                        okp = tc::mbar_wait(bar(L::PV_DONE), (k - 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
+                        okp = pdk::bar_and(2 + q4, 64, __all_sync(0xffffffffu, okp));
+                        ok = okp;  // on an abort, the next unit's barrier ends the loop
+                    }
+                    if (!first && okp) {
                         tc::fence_after_sync();
                         const float f = grow ? ex2_approx((m_ref - mh) * p.scale_log2) : 1.f;
 #pragma unroll 1
                         for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t po[64];
-                            tc::tmem_ld64(o_addr + 64 * hf, po);
+                            uint32_t po[32];
+                            tc::tmem_ld32(o_addr + 32 * hf, po);
                             tc::tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 64; ++j) po[j] = __float_as_uint(__uint_as_float(po[j]) * f);
-                            tc::tmem_st64h(o_addr + 64 * hf, po);
+                            for (int j = 0; j < 32; ++j) po[j] = __float_as_uint(__uint_as_float(po[j]) * f);
+                            tc::tmem_st32(o_addr + 32 * hf, po);
                         }
                         tc::tmem_st_wait();
                         if (grow) {
                             l_acc *= f;
                             lr_acc *= f;
                         }
-                        MSA_LOAD_S_ROW();
+                        MSA_LOAD_S_HALF();
                     }
                     if (grow) m_ref = mh;
                 }
-#undef MSA_LOAD_S_ROW
+#undef MSA_LOAD_S_HALF
                 if (nvis > 0 && m_ref == -INFINITY) m_ref = mh;  // the group's first visible keys of the row
                 // P = exp2((S - m_ref) scale_log2) packed to bf16 in place (pr[j]
-                // <- keys 2j, 2j+1); sums of P and of the rounded P that PV uses
+                // <- keys 2j, 2j+1 of the half); sums of P and of the rounded P
+                // that PV uses
                 const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * p.scale_log2;
                 const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                 const float2 nm2 = make_float2(-mc, -mc);
                 float2 ll = make_float2(0.f, 0.f), lr = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     float2 e = __ffma2_rn(make_float2(__uint_as_float(pr[2 * j]), __uint_as_float(pr[2 * j + 1])),
                                           sc2, nm2);
                     e.x = ex2_approx(e.x);
@@ -627,117 +660,108 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 lr_acc += lr.x + lr.y;
             } else {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) pr[j] = 0u;  // no row of the warp selects the block: P = 0
+                for (int j = 0; j < 32; ++j) pr[j] = 0u;  // no row of the warp selects the block: P = 0
             }
-            tc::tmem_st64(s_addr, pr);
+            tc::tmem_st32(s_addr, pr);
             tc::tmem_st_wait();
+            float2 tot = make_float2(0.f, 0.f);
+            if (last) {
+                // the group's sums over both halves (through the K tile, before
+                // this unit's P lets the tile be reloaded)
+                float2 *x2 = reinterpret_cast<float2 *>(xch + 256);
+                x2[hs * 128 + R] = make_float2(l_acc, lr_acc);
+                tc::named_bar_sync(2 + q4, 64);
+                const float2 o2 = x2[(1 - hs) * 128 + R];
+                tot = make_float2(l_acc + o2.x, lr_acc + o2.y);
+            }
+            tc::fence_proxy_async();  // generic writes to the K tile before its next TMA load
             tc::fence_before_sync();
             tc::mbar_arrive(bar(L::P_FULL + b));
-            if (last) {
-                // the group's row statistics for the epilogue: LSE and 1 / (sum
-                // of the rounded P), once it has read those of group pc - 2
-                if (pc >= 2) {
-                    ok = tc::mbar_wait(bar(L::O_EMPTY + (pc & 1)), ((pc >> 1) - 1) & 1, abort_flag, p.status,
-                                       MSA_STATUS_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                }
-                stat[(pc & 1) * 128 + R] = make_float2(l_acc > 0.f ? m_ref * p.scale + __logf(l_acc) : -INFINITY,
-                                                       lr_acc > 0.f ? 1.f / lr_acc : 0.f);
-                tc::mbar_arrive(bar(L::ST_FULL + (pc & 1)));
-            }
             ++k;
-        }
-    } else if (warp >= kWarpEpi0) {
-        // ------------------------------------------------------------------ epilogue
-        const int R = 32 * (warp & 3) + lane;
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int qi = R / p.qpk, hj = R % p.qpk;
-        const int et = tid - kWarpEpi0 * 32;  // 0..127
-        Walk w;
-        bool more = walk_begin(w, wstart);
-        int pc = 0;
-        while (more) {
-            const int g = w.g, j0 = w.j, j1 = w.jend, off = w.off, n = w.n;
+            if (!last) continue;
+            // -------- the group's end: once its last PV has completed, this
+            // half's 64 columns of O / (sum of the rounded P) go to the output
+            // (a group the CTA holds whole) or to the piece's slot (a cut
+            // group).  The O buffer is read before any P of the group after
+            // next exists, so the MMA needs no other signal to reuse it.
             const int pp = pc & 1;
-            bool ok = tc::mbar_wait(bar(L::ST_FULL + pp), (pc >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
             ok = ok && tc::mbar_wait(bar(L::O_FULL + pp), (pc >> 1) & 1, abort_flag, p.status, MSA_STATUS_TIMEOUT);
-            // every epilogue thread leaves together on an abort (named barriers follow)
-            if (!pdk::bar_and(1, 128, ok)) break;
+            // both warpgroups leave together on an abort (named barriers follow)
+            ok = pdk::bar_and(1, 256, __all_sync(0xffffffffu, ok));
+            if (!ok) break;
             tc::fence_after_sync();
-            const float2 st = stat[pp * 128 + R];
-            uint32_t o[128];
-            tc::tmem_ld128(tmem + lane_base + 256 + pp * 128, o);
-            tc::tmem_ld_wait();
-            tc::fence_before_sync();
-            tc::mbar_arrive(bar(L::O_EMPTY + pp));  // O and the statistics are read
-            const DGroup x = dgroup(p, g);
-            const bool cut = !w.aligned && (j0 > 0 || j1 < n);
-            const bool rowv = qi < x.nq;
-            const int64_t orow = ((int64_t)x.b * p.Sq + x.q0 + qi) * p.Hq + x.h * p.qpk + hj;
-            if (!cut) {
-                if (rowv) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD);
+            const float lse_row = tot.x > 0.f ? m_ref * p.scale + __logf(tot.x) : -INFINITY;
+            const float inv = tot.y > 0.f ? 1.f / tot.y : 0.f;
+            const bool cut = !wstart.aligned && (pj0 > 0 || pj1 < pn);
+            const int64_t orow = ((int64_t)x.b * p.Sq + x.q0 + qi) * p.Hq + x.h * p.qpk + R % p.qpk;
+            const int slot = pc == 0 ? 0 : 1;  // a cut group's piece: the CTA's first in slot 0, its last in slot 1
+            const int64_t sb = ((int64_t)blockIdx.x * 2 + slot) * 128;
+            {
+                uint32_t o[64];
+                tc::tmem_ld64(tmem + lane_base + 256 + pp * 128 + 64 * hs, o);
+                tc::tmem_ld_wait();
+                if (!cut) {
+                    if (qi < x.nq) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD) + 8 * hs;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
+                                                pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
+                        if (hs == 0 && p.lse) p.lse[orow] = lse_row;
+                    }
+                } else {
+                    float4 *so = reinterpret_cast<float4 *>(p.slot_o + (sb + R) * kD) + 16 * hs;
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        dst[c] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * c + 0]) * st.y, __uint_as_float(o[8 * c + 1]) * st.y),
-                                            pack_bf16x2(__uint_as_float(o[8 * c + 2]) * st.y, __uint_as_float(o[8 * c + 3]) * st.y),
-                                            pack_bf16x2(__uint_as_float(o[8 * c + 4]) * st.y, __uint_as_float(o[8 * c + 5]) * st.y),
-                                            pack_bf16x2(__uint_as_float(o[8 * c + 6]) * st.y, __uint_as_float(o[8 * c + 7]) * st.y));
-                    if (p.lse) p.lse[orow] = st.x;
+                        __stcg(so + c, make_float4(__uint_as_float(o[4 * c + 0]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
+                                                   __uint_as_float(o[4 * c + 2]) * inv, __uint_as_float(o[4 * c + 3]) * inv));
+                    if (hs == 0) __stcg(p.slot_lse + sb + R, lse_row);
                 }
-            } else {
-                // this CTA's piece of a cut group: its first piece in slot 0, its last in slot 1
-                const int slot = pc == 0 ? 0 : 1;
-                const int64_t sb = ((int64_t)blockIdx.x * 2 + slot) * 128;
-                float4 *so = reinterpret_cast<float4 *>(p.slot_o + (sb + R) * kD);
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    __stcg(so + c, make_float4(__uint_as_float(o[4 * c + 0]) * st.y, __uint_as_float(o[4 * c + 1]) * st.y,
-                                               __uint_as_float(o[4 * c + 2]) * st.y, __uint_as_float(o[4 * c + 3]) * st.y));
-                __stcg(p.slot_lse + sb + R, st.x);
+            }
+            if (cut) {
                 // the CTA that writes the group's last piece merges all of them
                 const long long total = wstart.total;
                 const int grid = wstart.grid;
-                const int c_first = cta_of(off, total, grid), c_last = cta_of((long long)off + n - 1, total, grid);
-                __threadfence();  // this row's piece is visible before the count says so
-                tc::named_bar_sync(1, 128);
+                const int c_first = cta_of(pof, total, grid), c_last = cta_of((long long)pof + pn - 1, total, grid);
+                const int et = tid - kWarpSoftmax0 * 32;  // 0..255
+                __threadfence();  // this thread's part of the piece is visible before the count says so
+                tc::named_bar_sync(1, 256);
                 if (et == 0) {
                     __threadfence();
-                    const int prev = atomicAdd(p.merge_cnt + g, 1);
+                    const int prev = atomicAdd(p.merge_cnt + pg, 1);
                     __threadfence();
                     *merge_flag = prev == c_last - c_first;
                 }
-                tc::named_bar_sync(1, 128);
+                tc::named_bar_sync(1, 256);
                 if (*merge_flag) {
-                    // Warp-cooperative: each warp merges its 32 rows, eight at a
-                    // time, lane l holding dims 4l .. 4l + 3; the pieces are
-                    // folded in one pass with a running max, two pieces' loads
-                    // in flight together.
+                    // Warp-cooperative: each of the eight warps merges 16 rows,
+                    // eight at a time, lane l holding dims 4l .. 4l + 3; the
+                    // pieces are folded in one pass with a running max.
                     const int npc = c_last - c_first + 1;
-                    for (int r0 = (et >> 5) * 32; r0 < (et >> 5) * 32 + 32; r0 += 8) {
-                        float mr[8], den[8];
-                        float4 acc[8];
+                    for (int r0 = (et >> 5) * 16; r0 < (et >> 5) * 16 + 16; r0 += 4) {
+                        float mr[4], den[4];
+                        float4 acc[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 4; ++i) {
                             mr[i] = -INFINITY;
                             den[i] = 0.f;
                             acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-#pragma unroll 2
                         for (int k2 = 0; k2 < npc; ++k2) {
                             const int cc = c_first + k2;
-                            const int sl = (cc > c_first || (long long)off == total * cc / grid) ? 0 : 1;
+                            const int sl = (cc > c_first || (long long)pof == total * cc / grid) ? 0 : 1;
                             const int64_t rb = ((int64_t)cc * 2 + sl) * 128 + r0;
-                            float lv[8];
-                            float4 ov[8];
+                            float lv[4];
+                            float4 ov[4];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i = 0; i < 4; ++i) {
                                 lv[i] = __ldcg(p.slot_lse + rb + i);
                                 ov[i] = __ldcg(reinterpret_cast<const float4 *>(p.slot_o + (rb + i) * kD) + lane);
                             }
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i = 0; i < 4; ++i) {
                                 const float mn = fmaxf(mr[i], lv[i]);
                                 if (mn != -INFINITY) {  // the same for every lane (one row)
                                     const float a = __expf(mr[i] - mn), bw = __expf(lv[i] - mn);
@@ -749,23 +773,21 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                             }
                         }
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 4; ++i) {
                             const int r = r0 + i, rq = r / p.qpk;
                             if (rq >= x.nq) continue;
-                            const float inv = den[i] > 0.f ? 1.f / den[i] : 0.f;
+                            const float dinv = den[i] > 0.f ? 1.f / den[i] : 0.f;
                             const int64_t orr = ((int64_t)x.b * p.Sq + x.q0 + rq) * p.Hq + x.h * p.qpk + r % p.qpk;
                             reinterpret_cast<uint2 *>(p.o + orr * kD)[lane] =
-                                make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
-                                           pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+                                make_uint2(pack_bf16x2(acc[i].x * dinv, acc[i].y * dinv),
+                                           pack_bf16x2(acc[i].z * dinv, acc[i].w * dinv));
                             if (p.lse && lane == 0) p.lse[orr] = den[i] > 0.f ? mr[i] + __logf(den[i]) : -INFINITY;
                         }
                     }
                 }
+                // the merge flag is read by all before the next group's count
+                // may change it (at the next cut group's first barrier)
             }
-            ++pc;
-            // the next group of the run
-            w.j = w.jend - 1;
-            more = walk_next(w, p);
         }
     }
     tc::fence_before_sync();
