@@ -12,13 +12,15 @@ namespace msa {
 // ---------------------------------------------------------------------------
 // plan: one CTA (256 threads) per group
 // ---------------------------------------------------------------------------
-// Dynamic shared memory: bitmap [ceil(max_pages/32)] | slots [qc*topk] |
-// kept [qc*topk] | union [maxu] | masks [maxu][wq].
+// Dynamic shared memory: the sequence's page-table row [max_pages] | bitmap
+// [ceil(max_pages/32)] | slots [qc*topk] | kept [qc*topk] | union [maxu] |
+// masks [maxu][wq].
 __global__ void __launch_bounds__(256) paged_plan_kernel(DecodeParams p) {
     extern __shared__ uint32_t dsm[];
     const int nwords = (p.max_pages + 31) >> 5;
     const int nslot_max = p.q2k ? p.qc * p.topk : 0;
-    uint32_t *bitmap = dsm;
+    int32_t *ptab = reinterpret_cast<int32_t *>(dsm);
+    uint32_t *bitmap = dsm + p.max_pages;
     int32_t *sel = reinterpret_cast<int32_t *>(bitmap + nwords);
     int32_t *kept = sel + nslot_max;
     int32_t *ul = kept + nslot_max;
@@ -31,6 +33,8 @@ __global__ void __launch_bounds__(256) paged_plan_kernel(DecodeParams p) {
     const DGroup x = dgroup(p, g);
     const int kv = p.seqused[x.b];
     const int nvalid = kv <= 0 ? 0 : (int)min(ceil_div(kv, kBlk), (int64_t)p.max_pages);
+    // the sequence's pages, loaded with the selections rather than after the union
+    for (int i = tid; i < nvalid; i += blockDim.x) ptab[i] = p.page_table[(int64_t)x.b * p.max_pages + i];
     int nu;
     if (p.q2k) {
         const int nslots = x.nq * p.topk;
@@ -103,11 +107,12 @@ __global__ void __launch_bounds__(256) paged_plan_kernel(DecodeParams p) {
         __syncthreads();
     } else {
         nu = nvalid;  // dense: every block of the sequence, every query
+        __syncthreads();
     }
     const int64_t gbase = (int64_t)g * p.maxu;
     for (int e = tid; e < nu; e += blockDim.x) {
         const int j = p.q2k ? ul[e] : e;
-        int pg = p.page_table[(int64_t)x.b * p.max_pages + j];
+        int pg = ptab[j];
         if (pg < 0 || pg >= p.num_pages) {
             set_status(p.status, MSA_STATUS_PAGE_RANGE);
             pg = -1;  // the decode kernel skips the block
@@ -258,8 +263,8 @@ int paged_decode(const void *q, const void *k_pool, const void *v_pool, int kv_f
         mk = mv = mq;  // unused: the staging warp reads the e4m3 pools
     }
     const int nwords = (max_pages + 31) / 32;
-    const size_t psmem = q2k ? sizeof(uint32_t) * ((size_t)nwords + 2 * (size_t)d.qc * topk + (size_t)d.maxu * (1 + d.wq))
-                             : 0;
+    const size_t psmem =
+        sizeof(uint32_t) * ((size_t)max_pages + (q2k ? (size_t)nwords + 2 * (size_t)d.qc * topk + (size_t)d.maxu * (1 + d.wq) : 0));
     MSA_CUDA_TRY(cudaFuncSetAttribute(paged_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
     MSA_CUDA_TRY(launch_pdl(paged_plan_kernel, dim3(d.G), dim3(256), psmem, stream, p));
     return kv_format == MSA_KV_BF16 ? launch_paged_decode_bf16(mk, mv, mq, p, d.grid, stream)

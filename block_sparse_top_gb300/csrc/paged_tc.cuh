@@ -250,7 +250,12 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
 
     // ---------------------------------------------------------------- partition
     // Exclusive prefix of the union sizes in the K/V ring (free until the
-    // pipeline starts), then this CTA's run of units.
+    // pipeline starts), then this CTA's run of units.  The producer meanwhile
+    // loads the page of unit 0 of group blockIdx.x, where a whole-group run
+    // starts (used only if the run starts there).
+    int page_guess = -1;
+    if (KV_FORMAT == MSA_KV_BF16 && warp == kWarpLoad && lane == 0 && (int)blockIdx.x < p.G)
+        page_guess = ld_plan(p.upage + (int64_t)blockIdx.x * p.maxu);
     {
         int *scr = reinterpret_cast<int *>(gbase);  // [G + 1] prefix | [kWarps] warp sums | [kWarps] maxima
         int *wsum = scr + p.G + 1, *wmax = wsum + kWarps;
@@ -342,7 +347,10 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
             for (int i = 0; i < kNKV; ++i) kv_armed[i] = -1;
             bool ok = true;
             DGroup x{};
-            int page_next = more && KV_FORMAT == MSA_KV_BF16 ? ld_plan(p.upage + (int64_t)w.g * p.maxu + w.j) : 0;
+            int page_next = 0;
+            if (more && KV_FORMAT == MSA_KV_BF16)
+                page_next = (w.g == (int)blockIdx.x && w.j == 0) ? page_guess
+                                                                   : ld_plan(p.upage + (int64_t)w.g * p.maxu + w.j);
             while (more && ok) {
                 const bool first = w.j == w.j0;
                 if (first) {
