@@ -53,6 +53,7 @@ KERNELS_PER_PAGED = 2    # union plan, decode
 PROFILED_TRAFFIC: dict = {
     "b5ee4a9835e4ca32": 1.101e10,  # 2.47 GB read + 8.54 GB written
     "b02f23509976d36b": 1.087e10,  # 2.33 GB read + 8.54 GB written
+    "5b5733e4b8e18d14": 1.0749e10,  # 2.21 GB read + 8.54 GB written
 }
 
 

@@ -58,6 +58,13 @@ EDGE = [
     # three query groups per (sequence, KV head), the last one partial: consecutive
     # groups of one head share nothing, their Q tiles must not be reused
     D("qpk16_three_groups", qpk=16, Sq=20, topk=8, kv_len=4096, Hkv=3),
+    # one group only: its ~120 union blocks are shared out between CTAs (at
+    # least 8 units each), and the CTA finishing last merges ~14 pieces
+    D("one_group_many_pieces", B=1, Hkv=1, Sq=8, qpk=16, topk=16, kv_len=131072, trim=17),
+    # two groups of ~57 blocks and 152 SMs: cut groups whose pieces lie in
+    # different numbers of CTAs, some CTAs holding the end of one group and the
+    # start of the next
+    D("two_groups_cut", B=2, Hkv=1, Sq=8, qpk=16, topk=16, kv_len=8192, trim=17),
 ]
 
 

@@ -101,6 +101,9 @@ def D(name, **kw):
     D("dense_qpk1", qpk=1, Sq=8, kv_len=1024, trim=100),
     D("dense_short", qpk=16, Sq=8, kv_len=128, trim=123),   # seqused 5 < Sq: early queries see nothing
     D("dense_qpk2_many_groups", qpk=2, Sq=150, kv_len=2048, trim=300),
+    # one long sequence and one KV head: every CTA holds a piece of the one
+    # group (512 blocks, 64 pieces merged by the CTA finishing last)
+    D("dense_one_group_64k", B=1, Hkv=1, Sq=8, qpk=16, kv_len=65536, trim=17),
 ], ids=lambda s: s.name)
 def test_dense_decode_matches_oracle(spec):
     import block_sparse_top_gb300 as msa
