@@ -66,6 +66,22 @@ def test_size_queries(L):
     assert L.msa_sparse_attn_paged_fwd_workspace_size(32, 8, 64, 4, 128, 16, 1024) > 0
 
 
+def test_decode_size_queries(L):
+    # sparse and dense (topk 0) paged decode; the dense plan holds every block
+    sparse = L.msa_paged_attn_fwd_workspace_size(32, 8, 64, 4, 128, 16, 1024)
+    dense = L.msa_paged_attn_fwd_workspace_size(32, 8, 64, 4, 128, 0, 1024)
+    assert sparse == L.msa_sparse_attn_paged_fwd_workspace_size(32, 8, 64, 4, 128, 16, 1024)
+    assert dense > sparse > 0
+    # the sparse entry point has no dense mode; unsupported shapes give 0
+    assert L.msa_sparse_attn_paged_fwd_workspace_size(32, 8, 64, 4, 128, 0, 1024) == 0
+    assert L.msa_paged_attn_fwd_workspace_size(32, 8, 64, 4, 128, 5, 1024) == 0       # topk 5
+    assert L.msa_paged_attn_fwd_workspace_size(32, 8, 48, 4, 128, 16, 1024) == 0      # qhead_per_kv 12
+    assert L.msa_paged_attn_fwd_workspace_size(32, 8, 64, 4, 128, 16, 8193) == 0      # max_pages past 8192
+    # groups: B * Hkv * ceil(Sq / (128 / qpk)) at most 49152
+    assert L.msa_paged_attn_fwd_workspace_size(12288, 1, 64, 4, 128, 16, 8) > 0       # 49152 groups
+    assert L.msa_paged_attn_fwd_workspace_size(12289, 1, 64, 4, 128, 16, 8) == 0      # one more
+
+
 def test_bad_arguments_are_rejected_before_launch(L):
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
     null = None
@@ -86,6 +102,17 @@ def test_bad_arguments_are_rejected_before_launch(L):
     rc = L.msa_sparse_attn_paged_fwd(fake, fake, fake, 8, fake, 4, fake, fake, 2, 8, 64, 4, 128, 64, 16, 1, 0.0,
                                      fake, null, fake, 1 << 30, null, null)
     assert rc == -2   # page size 64
+    # general paged decode: kv_format must be bf16 or e4m3; a q2k with topk 0 is invalid
+    rc = L.msa_paged_attn_fwd(fake, fake, fake, 1, 8, fake, 4, fake, fake, 2, 8, 64, 4, 128, 128, 16, 1, 0.0,
+                              fake, null, fake, 1 << 30, null, null)
+    assert rc == -1   # MSA_KV_NVFP4 pools are not a decode format
+    rc = L.msa_paged_attn_fwd(fake, fake, fake, 0, 8, fake, 4, fake, fake, 2, 8, 64, 4, 128, 128, 0, 1, 0.0,
+                              fake, null, fake, 1 << 30, null, null)
+    assert rc == -1
+    # dense mode (q2k NULL), workspace too small
+    rc = L.msa_paged_attn_fwd(fake, fake, fake, 0, 8, fake, 4, fake, null, 2, 8, 64, 4, 128, 128, 0, 1, 0.0,
+                              fake, null, fake, 16, null, null)
+    assert rc == -3
     assert L.msa_nvfp4_quantize(fake, 4, 100, fake, fake, null) == -1   # D % 16 != 0
 
 
