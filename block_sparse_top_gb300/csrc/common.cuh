@@ -101,11 +101,15 @@ inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
 // time against unit length (a unit's K/V block is loaded once for up to 8
 // chunks).  W is sized by the split partials one (KV head, wave) pass writes
 // -- W * qhead_per_kv * topk rows of D bf16 plus two floats -- at about 512
-// MiB: on the 32K causal workload the tiles + combine took 4.86 ms at 32 MiB,
-// 4.63 at 128, 4.49 at 512, and 4.47 with one wave per head.
+// MiB for qhead_per_kv >= 8 (on the 32K causal workload the tiles took 2.263
+// ms at 256 MiB, 2.246 at 512, 2.255 at 1024, 2.277 at 2048) and 2048 MiB for
+// qhead_per_kv <= 4, whose chunks hold 32 or more queries and whose units are
+// short (the 384K qhead_per_kv 2 workload: 0.173 -> 0.181 of peak in bf16,
+// 0.117 -> 0.132 with NVFP4 K/V, against 512 MiB).
 inline int64_t wave_queries(int64_t total_q, int qpk, int topk) {
     const int64_t per_q = (int64_t)qpk * topk * (kD * 2 + 8);
-    int64_t w = ((((int64_t)512 << 20) / per_q) + 64) / 128 * 128;  // nearest multiple of 128
+    const int64_t budget = (int64_t)(qpk >= 8 ? 512 : 2048) << 20;
+    int64_t w = ((budget / per_q) + 64) / 128 * 128;  // nearest multiple of 128
     if (w < 128) w = 128;
     return w > total_q ? total_q : w;
 }
