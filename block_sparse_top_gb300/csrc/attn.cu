@@ -110,43 +110,51 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const void *__restrict_
 
 // The combine for qhead_per_kv 16 and 16-byte pieces (a group's pieces = 256
 // threads): one persistent CTA per SM walks groups blockIdx.x, + gridDim.x,
-// ...; thread 0 copies each group's split partials (n x 4 KB, contiguous) and
-// statistics (n x 128 B) into a ring of kRingBufs shared-memory buffers with
-// bulk copies, kRingBufs groups ahead, so that the bytes in flight do not live
-// in registers.  Each group is then merged in two phases:
-//   1. thread (head j, split s): its split's weight w = exp(a_s - A_j), with
-//      A_j the max over the group's splits of head j and den_j = sum w l_s
-//      (16-lane shuffles), into a shared weight table; lane s = 0 writes the
-//      LSE A_j + ln den_j;
-//   2. thread (8-dim chunk c, head j): O = sum_s w_s U_s / den_j over its
-//      pieces, in packed f32x2 FMAs,
-// so each weight is computed once, not once per piece.  The table is double
-// buffered, so one CTA barrier per group separates the phases.
+// ..., in three roles that meet only at mbarriers (no CTA barrier per group):
+//   warp 12 (copies): copies each group's split partials (n x 4 KB,
+//     contiguous) and statistics (n x 128 B) into a ring of kRingBufs
+//     shared-memory buffers with bulk copies, kRingBufs groups ahead;
+//   warps 8-11 (weights), once a group's copy has landed: lane (head j,
+//     split s), two passes of two heads per warp, the split's weight
+//     w = exp(a_s - A_j), with A_j the max over the group's splits of head j
+//     and den_j = sum w l_s (16-lane shuffles), into the buffer's weight
+//     table; lane s = 0 writes the LSE A_j + ln den_j; then the buffer is
+//     READY;
+//   warps 0-7 (merge, thread = (8-dim chunk c, head j)): once READY, fold
+//     O = sum_s w_s U_s / den_j over their pieces in packed f32x2 FMAs, store
+//     it, and release the buffer (one arrival per warp),
+// so each weight is computed once, not once per piece, and the merging warps
+// never wait for one another.
 constexpr int kRingBufs = 3;
+constexpr int kCombineThreads = 416;
 __host__ __device__ constexpr uint32_t ring_buf_bytes(int topk) { return (uint32_t)topk * (4096u + 128u); }
 template <int PD>
-__global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__restrict__ o_part,
-                                                              const float2 *__restrict__ stat_part,
-                                                              const float2 *__restrict__ stat_temp,
-                                                              const int32_t *__restrict__ split_counts,
-                                                              int64_t groups, int topk, uint4 *__restrict__ o,
-                                                              float *__restrict__ lse, float *__restrict__ lse_temp,
-                                                              uint32_t *status) {
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const uint4 *__restrict__ o_part,
+                                                                          const float2 *__restrict__ stat_part,
+                                                                          const float2 *__restrict__ stat_temp,
+                                                                          const int32_t *__restrict__ split_counts,
+                                                                          int64_t groups, int topk,
+                                                                          uint4 *__restrict__ o,
+                                                                          float *__restrict__ lse,
+                                                                          float *__restrict__ lse_temp,
+                                                                          uint32_t *status) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t base = smem_u32(smem), bb = ring_buf_bytes(topk);
-    const uint32_t bars = base + kRingBufs * bb;  // FULL[kRingBufs], EMPTY[kRingBufs]
+    const uint32_t bars = base + kRingBufs * bb;  // FULL[kRingBufs], EMPTY[kRingBufs], READY[kRingBufs]
     auto full = [&](int b) { return bars + 8u * b; };
     auto empty = [&](int b) { return bars + 8u * (kRingBufs + b); };
+    auto ready = [&](int b) { return bars + 8u * (2 * kRingBufs + b); };
     __shared__ int abort_flag_s;
-    __shared__ float wts[2][16][17];  // [parity][head][split] weights
-    __shared__ float inv_den[2][16];
+    __shared__ float wts[kRingBufs][16][17];  // [buffer][head][split] weights
+    __shared__ float inv_den[kRingBufs][16];
+    __shared__ int nsplit[kRingBufs];
     volatile int *abort_flag = &abort_flag_s;
-    const int t = threadIdx.x, c = t >> 4, j = t & 15, lane = t & 31;
-    const int jw = t >> 4, sw = t & 15;  // phase 1: head, split
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     if (t == 0) {
         for (int b = 0; b < kRingBufs; ++b) {
             tc::mbar_init(full(b), 1);
-            tc::mbar_init(empty(b), 8);  // one arrival per warp
+            tc::mbar_init(empty(b), 8);    // one arrival per merging warp
+            tc::mbar_init(ready(b), 128);  // every weights thread (each releases its own table writes)
         }
         *abort_flag = 0;
         tc::mbar_fence_init();
@@ -155,66 +163,88 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
     grid_dependents_launch();
     __syncthreads();
     const int64_t G = gridDim.x;
-    // thread 0: copy the k-th group of this CTA into buffer k % kRingBufs
-    auto issue = [&](int64_t k) -> bool {
-        const int64_t grp = blockIdx.x + k * G;
-        const int b = (int)(k % kRingBufs);
-        if (k >= kRingBufs &&
-            !tc::mbar_wait(empty(b), (uint32_t)(((k / kRingBufs) - 1) & 1), abort_flag, status, MSA_STATUS_TIMEOUT))
-            return false;
-        int n = split_counts[grp];
-        n = n < topk ? n : topk;
-        if (n > 0) {
-            tc::mbar_arrive_expect_tx(full(b), (uint32_t)n * (4096u + 128u));
-            tc::bulk_load(base + b * bb, o_part + grp * topk * 256, (uint32_t)n * 4096u, full(b));
-            tc::bulk_load(base + b * bb + topk * 4096u, stat_part + grp * topk * 16, (uint32_t)n * 128u, full(b));
-        } else {
-            tc::mbar_arrive(full(b));
-        }
-        return true;
-    };
-    bool ok = true;
-    int64_t issued = 0, k = 0;  // groups copied (thread 0), groups merged
-    if (t == 0)
-        for (; issued < kRingBufs && blockIdx.x + issued * G < groups && ok; ++issued) ok = issue(issued);
-    for (; blockIdx.x + k * G < groups; ++k) {
-        const int64_t grp = blockIdx.x + k * G;
-        const int b = (int)(k % kRingBufs), par = (int)(k & 1);
-        ok = tc::mbar_wait(full(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status, MSA_STATUS_TIMEOUT);
-        // the whole CTA leaves together (the phases below meet at a barrier):
-        // on a timed-out wait here or in thread 0's copy issue
-        if (!__syncthreads_and(ok && *abort_flag == 0)) break;
-        int n = split_counts[grp];
-        n = n < topk ? n : topk;
-        const uint4 *up = reinterpret_cast<const uint4 *>(smem + b * bb);
-        const float2 *stp = reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096);
-        // phase 1: weights of (head jw, split sw), max and sum over the 16 splits
-        {
-            const float2 st = sw < n ? stp[sw * 16 + jw] : make_float2(-INFINITY, 0.f);
-            const float a = isfinite(st.x) ? st.x : -INFINITY;
-            float A = a;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, o));
-            const float w = (a == -INFINITY) ? 0.f : __expf(a - A);
-            float den = w * st.y;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-            wts[par][jw][sw] = w;
-            if (sw == 0) {
-                inv_den[par][jw] = den > 0.f ? 1.f / den : 0.f;
-                const int64_t orow = grp * 16 + jw;
-                if (lse) lse[orow] = den > 0.f ? A + logf(den) : -INFINITY;
-                if (lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, jw);
+    if (warp == 12) {
+        // ------------------------------------------------------------ copies
+        if (lane != 0) return;
+        int64_t k = 0;
+        for (; blockIdx.x + k * G < groups; ++k) {
+            const int64_t grp = blockIdx.x + k * G;
+            const int b = (int)(k % kRingBufs);
+            if (k >= kRingBufs &&
+                !tc::mbar_wait(empty(b), (uint32_t)(((k / kRingBufs) - 1) & 1), abort_flag, status,
+                               MSA_STATUS_TIMEOUT))
+                break;
+            int n = split_counts[grp];
+            n = n < topk ? n : topk;
+            if (n > 0) {
+                tc::mbar_arrive_expect_tx(full(b), (uint32_t)n * (4096u + 128u));
+                tc::bulk_load(base + b * bb, o_part + grp * topk * 256, (uint32_t)n * 4096u, full(b));
+                tc::bulk_load(base + b * bb + topk * 4096u, stat_part + grp * topk * 16, (uint32_t)n * 128u,
+                              full(b));
+            } else {
+                tc::mbar_arrive(full(b));
             }
         }
-        __syncthreads();
-        // phase 2: the piece (chunk c, head j)
+        // the last kRingBufs copies land before the CTA can exit (after an
+        // abort nobody else waits for them)
+        volatile int dummy = 0;
+        for (int64_t kk = k > kRingBufs ? k - kRingBufs : 0; kk < k; ++kk)
+            tc::mbar_wait(full((int)(kk % kRingBufs)), (uint32_t)((kk / kRingBufs) & 1), &dummy, status, 0);
+        return;
+    }
+    if (warp >= 8) {
+        // ------------------------------------------------------------ weights
+        const int sw = lane & 15;
+        for (int64_t k = 0; blockIdx.x + k * G < groups; ++k) {
+            const int64_t grp = blockIdx.x + k * G;
+            const int b = (int)(k % kRingBufs);
+            const bool ok =
+                tc::mbar_wait(full(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status, MSA_STATUS_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            int n = split_counts[grp];
+            n = n < topk ? n : topk;
+            const float2 *stp = reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int jw = 4 * (warp - 8) + 2 * i + (lane >> 4);
+                const float2 st = sw < n ? stp[sw * 16 + jw] : make_float2(-INFINITY, 0.f);
+                const float a = isfinite(st.x) ? st.x : -INFINITY;
+                float A = a;
+#pragma unroll
+                for (int o2 = 8; o2 > 0; o2 >>= 1) A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, o2));
+                const float w = (a == -INFINITY) ? 0.f : __expf(a - A);
+                float den = w * st.y;
+#pragma unroll
+                for (int o2 = 8; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+                wts[b][jw][sw] = w;
+                if (sw == 0) {
+                    inv_den[b][jw] = den > 0.f ? 1.f / den : 0.f;
+                    const int64_t orow = grp * 16 + jw;
+                    if (lse) lse[orow] = den > 0.f ? A + logf(den) : -INFINITY;
+                    if (lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, jw);
+                }
+            }
+            if (warp == 8 && lane == 0) nsplit[b] = n;
+            tc::mbar_arrive(ready(b));
+        }
+        return;
+    }
+    // ---------------------------------------------------------------- mergers
+    const int c = t >> 4, j = t & 15;
+    for (int64_t k = 0; blockIdx.x + k * G < groups; ++k) {
+        const int64_t grp = blockIdx.x + k * G;
+        const int b = (int)(k % kRingBufs);
+        const bool ok = tc::mbar_wait(ready(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status,
+                                      MSA_STATUS_TIMEOUT);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int n = nsplit[b];
+        const uint4 *up = reinterpret_cast<const uint4 *>(smem + b * bb);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int sp = 0; sp < 16; ++sp) {
             if (sp >= n) break;
             const uint4 u = up[(sp * 16 + c) * 16 + j];
-            const float w = wts[par][j][sp];
+            const float w = wts[b][j][sp];
             const float2 w2 = make_float2(w, w);
             const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -228,25 +258,15 @@ __global__ void __launch_bounds__(256, 1) combine_ring_kernel(const uint4 *__res
                 acc[i] = __ffma2_rn(v, w2, acc[i]);
             }
         }
+        const float inv = inv_den[b][j];
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(empty(b));  // this warp is done with the buffer
-        const float inv = inv_den[par][j];
+        if (lane == 0) tc::mbar_arrive(empty(b));  // this warp is done with the buffer and its table
         uint4 out;
         out.x = pack_bf16x2(acc[0].x * inv, acc[0].y * inv);
         out.y = pack_bf16x2(acc[1].x * inv, acc[1].y * inv);
         out.z = pack_bf16x2(acc[2].x * inv, acc[2].y * inv);
         out.w = pack_bf16x2(acc[3].x * inv, acc[3].y * inv);
         o[(grp * 16 + j) * 16 + c] = out;
-        if (t == 0 && blockIdx.x + (k + kRingBufs) * G < groups && ok) {
-            ok = issue(k + kRingBufs);
-            if (ok) ++issued;
-        }
-    }
-    // after an abort, copies still in flight land before the CTA exits
-    if (t == 0) {
-        volatile int dummy = 0;
-        for (int64_t kk = k; kk < issued; ++kk)
-            tc::mbar_wait(full((int)(kk % kRingBufs)), (uint32_t)((kk / kRingBufs) & 1), &dummy, status, 0);
     }
 }
 
@@ -266,10 +286,10 @@ int combine_generic(const void *op, const float2 *sp, const float2 *tp, const in
 template <int PD>
 int combine_ring(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
                  int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
-    const size_t smem = kRingBufs * ring_buf_bytes(topk) + 16u * kRingBufs;
+    const size_t smem = kRingBufs * ring_buf_bytes(topk) + 24u * kRingBufs;
     MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel<PD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
-    MSA_CUDA_TRY(launch_pdl(combine_ring_kernel<PD>, dim3(grid), dim3(256), smem, stream,
+    MSA_CUDA_TRY(launch_pdl(combine_ring_kernel<PD>, dim3(grid), dim3(kCombineThreads), smem, stream,
                             static_cast<const uint4 *>(op), sp, tp, split_counts, groups, topk, ob, lse, lse_temp,
                             (uint32_t *)nullptr));
     return MSA_OK;
