@@ -55,6 +55,7 @@ PROFILED_TRAFFIC: dict = {
     "b02f23509976d36b": 1.087e10,  # 2.33 GB read + 8.54 GB written
     "5b5733e4b8e18d14": 1.0749e10,  # 2.21 GB read + 8.54 GB written
     "7cb41653a1839e32": 1.0781e10,  # 2.24 GB read + 8.54 GB written
+    "3b71fc819f216446": 1.0738e10,  # 2.20 GB read + 8.54 GB written
 }
 
 
