@@ -108,27 +108,30 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const void *__restrict_
     if (c == 0 && lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, qpk, j);
 }
 
-// The combine for qhead_per_kv 16 and 16-byte pieces (a group's pieces = 256
-// threads): one persistent CTA per SM walks groups blockIdx.x, + gridDim.x,
-// ..., in three roles that meet only at mbarriers (no CTA barrier per group):
-//   warp 12 (copies): copies each group's split partials (n x 4 KB,
-//     contiguous) and statistics (n x 128 B) into a ring of kRingBufs
-//     shared-memory buffers with bulk copies, kRingBufs groups ahead;
-//   warps 8-11 (weights), once a group's copy has landed: lane (head j,
-//     split s), two passes of two heads per warp, the split's weight
-//     w = exp(a_s - A_j), with A_j the max over the group's splits of head j
-//     and den_j = sum w l_s (16-lane shuffles), into the buffer's weight
-//     table; lane s = 0 writes the LSE A_j + ln den_j; then the buffer is
-//     READY;
-//   warps 0-7 (merge, thread = (8-dim chunk c, head j)): once READY, fold
-//     O = sum_s w_s U_s / den_j over their pieces in packed f32x2 FMAs, store
-//     it, and release the buffer (one arrival per warp),
+// The combine for 16-byte pieces (bf16 / fp16 partials) and topk <= 16: a
+// ring buffer holds a run of NG = 16 / qhead_per_kv consecutive groups (256
+// pieces: one per merging thread); one persistent CTA per SM walks the runs
+// blockIdx.x, + gridDim.x, ..., in three roles that meet only at mbarriers
+// (no CTA barrier per run):
+//   warp 12 (copies): copies each group's split partials (n x qpk x 256 B,
+//     contiguous) and the run's statistics into a ring of kRingBufs
+//     shared-memory buffers with bulk copies, kRingBufs runs ahead;
+//   warps 8-11 (weights), once a run's copy has landed: lane (row r = group
+//     r / qpk, head r % qpk; split s), two passes of two rows per warp, the
+//     split's weight w = exp(a_s - A_r), with A_r the max over the group's
+//     splits and den_r = sum w l_s (16-lane shuffles), into the buffer's
+//     weight table; lane s = 0 writes the LSE A_r + ln den_r; then the
+//     buffer is READY;
+//   warps 0-7 (merge, thread = (group, 8-dim chunk c, head j), head
+//     fastest): once READY, fold O = sum_s w_s U_s / den over their pieces
+//     in packed f32x2 FMAs, store it, and release the buffer (one arrival
+//     per warp),
 // so each weight is computed once, not once per piece, and the merging warps
 // never wait for one another.
 constexpr int kRingBufs = 3;
 constexpr int kCombineThreads = 416;
 __host__ __device__ constexpr uint32_t ring_buf_bytes(int topk) { return (uint32_t)topk * (4096u + 128u); }
-template <int PD>
+template <int PD, int QPK>
 __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const uint4 *__restrict__ o_part,
                                                                           const float2 *__restrict__ stat_part,
                                                                           const float2 *__restrict__ stat_temp,
@@ -145,11 +148,15 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const 
     auto empty = [&](int b) { return bars + 8u * (kRingBufs + b); };
     auto ready = [&](int b) { return bars + 8u * (2 * kRingBufs + b); };
     __shared__ int abort_flag_s;
-    __shared__ float wts[kRingBufs][16][17];  // [buffer][head][split] weights
+    __shared__ float wts[kRingBufs][16][17];  // [buffer][row = group * qpk + head][split] weights
     __shared__ float inv_den[kRingBufs][16];
-    __shared__ int nsplit[kRingBufs];
+    __shared__ int nsplit[kRingBufs][16];     // [buffer][group of the run]
     volatile int *abort_flag = &abort_flag_s;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    constexpr int qpk = QPK;
+    constexpr int ng = 16 / qpk;  // groups per run
+    const int64_t runs = (groups + ng - 1) / ng;
+    const uint32_t gbytes = (uint32_t)topk * (uint32_t)qpk * 256u;  // a group's partial slots
     if (t == 0) {
         for (int b = 0; b < kRingBufs; ++b) {
             tc::mbar_init(full(b), 1);
@@ -167,23 +174,31 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const 
         // ------------------------------------------------------------ copies
         if (lane != 0) return;
         int64_t k = 0;
-        for (; blockIdx.x + k * G < groups; ++k) {
-            const int64_t grp = blockIdx.x + k * G;
+        for (; blockIdx.x + k * G < runs; ++k) {
+            const int64_t run = blockIdx.x + k * G, grp0 = run * ng;
             const int b = (int)(k % kRingBufs);
             if (k >= kRingBufs &&
                 !tc::mbar_wait(empty(b), (uint32_t)(((k / kRingBufs) - 1) & 1), abort_flag, status,
                                MSA_STATUS_TIMEOUT))
                 break;
-            int n = split_counts[grp];
-            n = n < topk ? n : topk;
-            if (n > 0) {
-                tc::mbar_arrive_expect_tx(full(b), (uint32_t)n * (4096u + 128u));
-                tc::bulk_load(base + b * bb, o_part + grp * topk * 256, (uint32_t)n * 4096u, full(b));
-                tc::bulk_load(base + b * bb + topk * 4096u, stat_part + grp * topk * 16, (uint32_t)n * 128u,
-                              full(b));
-            } else {
-                tc::mbar_arrive(full(b));
+            const int nr = (int)min((int64_t)ng, groups - grp0);  // groups of this run
+            uint32_t bytes = 0;
+            for (int g = 0; g < nr; ++g) {
+                int n = split_counts[grp0 + g];
+                n = n < topk ? n : topk;
+                nsplit[b][g] = n;
+                bytes += (uint32_t)n * (uint32_t)qpk * 256u;
             }
+            for (int g = nr; g < ng; ++g) nsplit[b][g] = 0;
+            // the run's statistics, every split slot of its groups (topk qpk 8 B
+            // a group: a multiple of 16 bytes)
+            const uint32_t sbytes = (uint32_t)nr * (uint32_t)topk * (uint32_t)qpk * 8u;
+            tc::mbar_arrive_expect_tx(full(b), bytes + sbytes);
+            for (int g = 0; g < nr; ++g)
+                if (nsplit[b][g] > 0)
+                    tc::bulk_load(base + b * bb + g * gbytes, o_part + (grp0 + g) * topk * 16 * qpk,
+                                  (uint32_t)nsplit[b][g] * (uint32_t)qpk * 256u, full(b));
+            tc::bulk_load(base + b * bb + topk * 4096u, stat_part + grp0 * topk * qpk, sbytes, full(b));
         }
         // the last kRingBufs copies land before the CTA can exit (after an
         // abort nobody else waits for them)
@@ -195,19 +210,19 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const 
     if (warp >= 8) {
         // ------------------------------------------------------------ weights
         const int sw = lane & 15;
-        for (int64_t k = 0; blockIdx.x + k * G < groups; ++k) {
-            const int64_t grp = blockIdx.x + k * G;
+        for (int64_t k = 0; blockIdx.x + k * G < runs; ++k) {
+            const int64_t grp0 = (blockIdx.x + k * G) * ng;
             const int b = (int)(k % kRingBufs);
             const bool ok =
                 tc::mbar_wait(full(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status, MSA_STATUS_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) break;
-            int n = split_counts[grp];
-            n = n < topk ? n : topk;
             const float2 *stp = reinterpret_cast<const float2 *>(smem + b * bb + topk * 4096);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int jw = 4 * (warp - 8) + 2 * i + (lane >> 4);
-                const float2 st = sw < n ? stp[sw * 16 + jw] : make_float2(-INFINITY, 0.f);
+                const int r = 4 * (warp - 8) + 2 * i + (lane >> 4);  // row: group r / qpk, head r % qpk
+                const int g = ng == 1 ? 0 : r / qpk, j = r - g * qpk;
+                const int n = nsplit[b][g];
+                const float2 st = sw < n ? stp[(g * topk + sw) * qpk + j] : make_float2(-INFINITY, 0.f);
                 const float a = isfinite(st.x) ? st.x : -INFINITY;
                 float A = a;
 #pragma unroll
@@ -216,35 +231,37 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const 
                 float den = w * st.y;
 #pragma unroll
                 for (int o2 = 8; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
-                wts[b][jw][sw] = w;
+                wts[b][r][sw] = w;
                 if (sw == 0) {
-                    inv_den[b][jw] = den > 0.f ? 1.f / den : 0.f;
-                    const int64_t orow = grp * 16 + jw;
-                    if (lse) lse[orow] = den > 0.f ? A + logf(den) : -INFINITY;
-                    if (lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, 16, jw);
+                    inv_den[b][r] = den > 0.f ? 1.f / den : 0.f;
+                    const int64_t grp = grp0 + g;
+                    if (grp < groups) {
+                        const int64_t orow = grp * qpk + j;
+                        if (lse) lse[orow] = den > 0.f ? A + logf(den) : -INFINITY;
+                        if (lse_temp) lse_temp[orow] = combine_lse_temp(stat_temp, grp, n, topk, qpk, j);
+                    }
                 }
             }
-            if (warp == 8 && lane == 0) nsplit[b] = n;
             tc::mbar_arrive(ready(b));
         }
         return;
     }
     // ---------------------------------------------------------------- mergers
-    const int c = t >> 4, j = t & 15;
-    for (int64_t k = 0; blockIdx.x + k * G < groups; ++k) {
-        const int64_t grp = blockIdx.x + k * G;
+    const int j = t % qpk, c = (t / qpk) & 15, g = ng == 1 ? 0 : t / (16 * qpk), r = g * qpk + j;
+    for (int64_t k = 0; blockIdx.x + k * G < runs; ++k) {
+        const int64_t grp = (blockIdx.x + k * G) * ng + g;
         const int b = (int)(k % kRingBufs);
         const bool ok = tc::mbar_wait(ready(b), (uint32_t)((k / kRingBufs) & 1), abort_flag, status,
                                       MSA_STATUS_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const int n = nsplit[b];
-        const uint4 *up = reinterpret_cast<const uint4 *>(smem + b * bb);
+        const int n = nsplit[b][g];
+        const uint4 *up = reinterpret_cast<const uint4 *>(smem + b * bb + g * gbytes);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int sp = 0; sp < 16; ++sp) {
             if (sp >= n) break;
-            const uint4 u = up[(sp * 16 + c) * 16 + j];
-            const float w = wts[b][j][sp];
+            const uint4 u = up[(sp * 16 + c) * qpk + j];
+            const float w = wts[b][r][sp];
             const float2 w2 = make_float2(w, w);
             const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -258,15 +275,17 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_ring_kernel(const 
                 acc[i] = __ffma2_rn(v, w2, acc[i]);
             }
         }
-        const float inv = inv_den[b][j];
+        const float inv = inv_den[b][r];
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(empty(b));  // this warp is done with the buffer and its table
-        uint4 out;
-        out.x = pack_bf16x2(acc[0].x * inv, acc[0].y * inv);
-        out.y = pack_bf16x2(acc[1].x * inv, acc[1].y * inv);
-        out.z = pack_bf16x2(acc[2].x * inv, acc[2].y * inv);
-        out.w = pack_bf16x2(acc[3].x * inv, acc[3].y * inv);
-        o[(grp * 16 + j) * 16 + c] = out;
+        if (grp < groups) {
+            uint4 out;
+            out.x = pack_bf16x2(acc[0].x * inv, acc[0].y * inv);
+            out.y = pack_bf16x2(acc[1].x * inv, acc[1].y * inv);
+            out.z = pack_bf16x2(acc[2].x * inv, acc[2].y * inv);
+            out.w = pack_bf16x2(acc[3].x * inv, acc[3].y * inv);
+            o[(grp * qpk + j) * 16 + c] = out;
+        }
     }
 }
 
@@ -283,16 +302,30 @@ int combine_generic(const void *op, const float2 *sp, const float2 *tp, const in
     return MSA_OK;
 }
 
-template <int PD>
-int combine_ring(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
-                 int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
+template <int PD, int QPK>
+int combine_ring_q(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
+                   int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
     const size_t smem = kRingBufs * ring_buf_bytes(topk) + 24u * kRingBufs;
-    MSA_CUDA_TRY(cudaFuncSetAttribute(combine_ring_kernel<PD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    const int grid = (int)std::min<int64_t>(groups, (int64_t)num_sms());
-    MSA_CUDA_TRY(launch_pdl(combine_ring_kernel<PD>, dim3(grid), dim3(kCombineThreads), smem, stream,
+    MSA_CUDA_TRY(
+        cudaFuncSetAttribute(combine_ring_kernel<PD, QPK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const int64_t runs = (groups + 16 / QPK - 1) / (16 / QPK);
+    const int grid = (int)std::min<int64_t>(runs, (int64_t)num_sms());
+    MSA_CUDA_TRY(launch_pdl(combine_ring_kernel<PD, QPK>, dim3(grid), dim3(kCombineThreads), smem, stream,
                             static_cast<const uint4 *>(op), sp, tp, split_counts, groups, topk, ob, lse, lse_temp,
                             (uint32_t *)nullptr));
     return MSA_OK;
+}
+
+template <int PD>
+int combine_ring(const void *op, const float2 *sp, const float2 *tp, const int32_t *split_counts, int64_t groups,
+                 int qpk, int topk, uint4 *ob, float *lse, float *lse_temp, cudaStream_t stream) {
+    switch (qpk) {
+        case 1: return combine_ring_q<PD, 1>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+        case 2: return combine_ring_q<PD, 2>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+        case 4: return combine_ring_q<PD, 4>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+        case 8: return combine_ring_q<PD, 8>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+        default: return combine_ring_q<PD, 16>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+    }
 }
 
 }  // namespace
@@ -303,11 +336,11 @@ int combine_launch(const int32_t *split_counts, int64_t groups, int qpk, int top
     const float2 *sp = reinterpret_cast<const float2 *>(ws + w.stat_part);
     const float2 *tp = lse_temp ? reinterpret_cast<const float2 *>(ws + w.stat_temp) : nullptr;
     uint4 *ob = static_cast<uint4 *>(o);
-    // qhead_per_kv 16 with 16-byte pieces: staged through a shared-memory ring
-    if (qpk == 16 && topk <= 16 && part_dtype == MSA_PARTIAL_BF16)
-        return combine_ring<MSA_PARTIAL_BF16>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
-    if (qpk == 16 && topk <= 16 && part_dtype == MSA_PARTIAL_FP16)
-        return combine_ring<MSA_PARTIAL_FP16>(op, sp, tp, split_counts, groups, topk, ob, lse, lse_temp, stream);
+    // 16-byte pieces and topk <= 16: staged through a shared-memory ring
+    if (topk <= 16 && part_dtype == MSA_PARTIAL_BF16)
+        return combine_ring<MSA_PARTIAL_BF16>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp, stream);
+    if (topk <= 16 && part_dtype == MSA_PARTIAL_FP16)
+        return combine_ring<MSA_PARTIAL_FP16>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp, stream);
     if (part_dtype == MSA_PARTIAL_FP32)
         return combine_generic<MSA_PARTIAL_FP32>(op, sp, tp, split_counts, groups, qpk, topk, ob, lse, lse_temp,
                                                  stream);
