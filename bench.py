@@ -56,6 +56,7 @@ PROFILED_TRAFFIC: dict = {
     "5b5733e4b8e18d14": 1.0749e10,  # 2.21 GB read + 8.54 GB written
     "7cb41653a1839e32": 1.0781e10,  # 2.24 GB read + 8.54 GB written
     "3b71fc819f216446": 1.0738e10,  # 2.20 GB read + 8.54 GB written
+    "cc01a715c29fdf13": 1.0761e10,  # 2.22 GB read + 8.54 GB written
 }
 
 
