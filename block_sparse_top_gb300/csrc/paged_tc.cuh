@@ -708,7 +708,34 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
                 uint32_t o[64];
                 tc::tmem_ld64(tmem + lane_base + 256 + pp * 128 + 64 * hs, o);
                 tc::tmem_ld_wait();
-                if (!cut) {
+                if (!cut && !more) {
+                    // The CTA's last group: the K/V ring is idle (its last PV has
+                    // run and nothing more is loaded), so each warp stages its 32
+                    // rows' half (128 B a row, 16-byte chunks XOR-swizzled by
+                    // row) in K stage 0 and stores them back transposed, eight
+                    // lanes a row: whole 128-byte lines per store instruction.
+                    const uint32_t wrow = (uint32_t)(warp - kWarpSoftmax0) * 4096u;
+                    uint4 *stg = reinterpret_cast<uint4 *>(gbase + L::K + wrow);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        stg[lane * 8 + (c ^ (lane & 7))] =
+                            make_uint4(pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv),
+                                       pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv),
+                                       pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv),
+                                       pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv));
+                    __syncwarp();
+                    const int cc = lane & 7;
+#pragma unroll
+                    for (int k2 = 0; k2 < 8; ++k2) {
+                        const int rw = 4 * k2 + (lane >> 3);  // row of the warp this lane stores
+                        const int Rr = 32 * q4 + rw, qr = Rr / p.qpk;
+                        if (qr < x.nq) {
+                            const int64_t orr = ((int64_t)x.b * p.Sq + x.q0 + qr) * p.Hq + x.h * p.qpk + Rr % p.qpk;
+                            reinterpret_cast<uint4 *>(p.o + orr * kD)[8 * hs + cc] = stg[rw * 8 + (cc ^ (rw & 7))];
+                        }
+                    }
+                    if (hs == 0 && p.lse && qi < x.nq) p.lse[orow] = lse_row;
+                } else if (!cut) {
                     if (qi < x.nq) {
                         uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * kD) + 8 * hs;
 #pragma unroll
