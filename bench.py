@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS_PER_CSR = 8
 KERNELS_PER_PARTIAL = 1  # attention tiles
 KERNELS_PER_COMBINE = 1  # LSE combine
-KERNELS_PER_PAGED = 2    # union plan, decode
+KERNELS_PER_PAGED = 2    # union plan, decode (one kernel when each CTA plans its own group)
 
 # DRAM traffic (read + write bytes per launch) of the attention-tile kernel on
 # the 32K causal sink workload from one single-pass ncu capture
@@ -540,6 +540,17 @@ def measure_config(spec, dev, steps, warmup, peaks, peak_src):
     return res
 
 
+def decode_kernels_per_call(spec, num_sms: int) -> int:
+    """Kernels one paged-decode call launches: the decode kernel plans each
+    group itself (no plan kernel) when every group has a CTA of its own and no
+    union can exceed 10 blocks (the smallest balanced share, 8, plus a
+    quarter)."""
+    qc = 128 // spec.qpk
+    groups = spec.B * spec.Hkv * -(-spec.Sq // qc)
+    maxu = min(min(spec.Sq, qc) * spec.topk, spec.pages_per_seq)
+    return 1 if groups <= num_sms and maxu <= 10 else KERNELS_PER_PAGED
+
+
 def decode_sweep(args, dev, peaks, peak_src):
     """Paged decode GB/s per KV length.
 
@@ -591,12 +602,14 @@ def decode_sweep(args, dev, peaks, peak_src):
         us = a.elapsed_time(b) * 1e3 / (reps * n_calls)
         gbs = nbytes / (us * 1e-6) / 1e9
         out.append({"L": L, "us": round(us, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                    "bytes": nbytes, "gathered_kv_bytes_no_dedup": gathered, "input_sets": nsets})
+                    "bytes": nbytes, "gathered_kv_bytes_no_dedup": gathered, "input_sets": nsets,
+                    "kernels": decode_kernels_per_call(spec, torch.cuda.get_device_properties(dev).multi_processor_count)})
         del sets, outs, first, graph
         torch.cuda.empty_cache()
     return {"unit": "GB/s", "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
             "timing": "CUDA-graph replay of back-to-back calls cycling input sets (>= 600 MB per cycle)",
-            "kernels_per_call": KERNELS_PER_PAGED, "sweep": out}
+            "kernels_per_call": "per L in the sweep (1: each CTA plans its own group; 2: plan kernel + decode)",
+            "sweep": out}
 
 
 # ---------------------------------------------------------------------------

@@ -262,11 +262,22 @@ int paged_decode(const void *q, const void *k_pool, const void *v_pool, int kv_f
     } else {
         mk = mv = mq;  // unused: the staging warp reads the e4m3 pools
     }
-    const int nwords = (max_pages + 31) / 32;
-    const size_t psmem =
-        sizeof(uint32_t) * ((size_t)max_pages + (q2k ? (size_t)nwords + 2 * (size_t)d.qc * topk + (size_t)d.maxu * (1 + d.wq) : 0));
-    MSA_CUDA_TRY(cudaFuncSetAttribute(paged_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
-    MSA_CUDA_TRY(launch_pdl(paged_plan_kernel, dim3(d.G), dim3(256), psmem, stream, p));
+    // Local plan: when every group has a CTA of its own and no union can
+    // exceed a quarter over the smallest share (kMinShare units), the
+    // partition gives each group to one CTA whatever the data, so each CTA
+    // plans its own group and the plan kernel is not launched.
+    const bool local = d.G <= d.grid && d.maxu <= pdk::kMinShare + pdk::kMinShare / 4 &&
+                       pdk::plan_scratch_words(max_pages, q2k != nullptr, d.qc, topk, d.maxu, d.wq) * 4 <=
+                           pdk::Layout::Q;
+    p.local_plan = local ? 1 : 0;
+    if (!local) {
+        const int nwords = (max_pages + 31) / 32;
+        const size_t psmem = sizeof(uint32_t) *
+                             ((size_t)max_pages +
+                              (q2k ? (size_t)nwords + 2 * (size_t)d.qc * topk + (size_t)d.maxu * (1 + d.wq) : 0));
+        MSA_CUDA_TRY(cudaFuncSetAttribute(paged_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
+        MSA_CUDA_TRY(launch_pdl(paged_plan_kernel, dim3(d.G), dim3(256), psmem, stream, p));
+    }
     return kv_format == MSA_KV_BF16 ? launch_paged_decode_bf16(mk, mv, mq, p, d.grid, stream)
                                     : launch_paged_decode_fp8(mk, mv, mq, p, d.grid, stream);
 }

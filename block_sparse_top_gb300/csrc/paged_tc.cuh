@@ -1,5 +1,6 @@
 // paged_tc.cuh -- block-sparse paged decode in two launches: a union plan
-// kernel and a persistent tcgen05 decode kernel.
+// kernel and a persistent tcgen05 decode kernel (one launch when each decode
+// CTA can plan its own group, see local_plan).
 //
 // A group is (sequence b, KV head h, qc = 128/qhead_per_kv consecutive
 // queries): the 128 query-head rows (row R = query R / qpk of the group, head
@@ -73,6 +74,10 @@ struct DecodeParams {
     // a row's accumulated O is rescaled to a new reference max only when a
     // block's max exceeds the reference by more than this (log2 units)
     float p_bound;
+    // 1: no plan kernel ran; CTA c < G plans group c itself and holds it whole
+    // (the host sets this only when the partition is certain to give every
+    // group a CTA of its own: G <= grid and maxu <= kMinShare + kMinShare / 4)
+    int local_plan;
 };
 
 struct DGroup {
@@ -188,6 +193,151 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
     return r != 0;
 }
 
+// Plan of group g by all threads of the CTA, for the local-plan mode (every
+// thread calls it alike; it ends at a CTA barrier): the same plan the plan
+// kernel writes.  Every global load is issued up front (the
+// sequence length, its whole page-table row and the group's selections), so
+// the plan waits on one round trip.  Scratch (32-bit words, in the K/V ring):
+// page-table row [max_pages] | bitmap [nw] | per-word prefix [nw] | slots
+// [qc topk] | kept [qc topk] | union [maxu] | masks [maxu][wq] | warp sums
+// [kWarps] | sequence length | union size, nw = ceil(max_pages / 32).
+static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uint32_t *scr) {
+    const int nwords = (p.max_pages + 31) >> 5;
+    const int nslot_max = p.q2k ? p.qc * p.topk : 0;
+    int32_t *ptab = reinterpret_cast<int32_t *>(scr);
+    uint32_t *bitmap = scr + p.max_pages;
+    int32_t *wpre = reinterpret_cast<int32_t *>(bitmap + nwords);
+    int32_t *sel = wpre + nwords;
+    int32_t *kept = sel + nslot_max;
+    int32_t *ul = kept + nslot_max;
+    uint32_t *msk = reinterpret_cast<uint32_t *>(ul + p.maxu);
+    int32_t *warp_tot = reinterpret_cast<int32_t *>(msk + p.maxu * p.wq);
+    int32_t *s_kv = warp_tot + kWarps;
+    int32_t *s_nu = s_kv + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const DGroup x = dgroup(p, g);
+    const int nslots = p.q2k ? x.nq * p.topk : 0;
+    // ---- loads (one round trip) and zeroed tables
+    if (tid == 0) *s_kv = __ldg(p.seqused + x.b);
+    for (int i = tid; i < p.max_pages; i += kThreads) ptab[i] = __ldg(p.page_table + (int64_t)x.b * p.max_pages + i);
+    if (p.q2k) {
+        const int32_t *src = p.q2k + (((int64_t)x.b * p.Hkv + x.h) * p.Sq + x.q0) * p.topk;
+        for (int i = tid; i < nslots; i += kThreads) sel[i] = __ldg(src + i);
+        for (int i = tid; i < nwords; i += kThreads) bitmap[i] = 0u;
+        for (int i = tid; i < p.maxu * p.wq; i += kThreads) msk[i] = 0u;
+    }
+    __syncthreads();
+    const int kv = *s_kv;
+    const int nvalid = kv <= 0 ? 0 : (int)min(ceil_div(kv, kBlk), (int64_t)p.max_pages);
+    int nu;
+    if (p.q2k) {
+        // a slot is kept when its id is a valid block and no earlier slot of
+        // its query holds the same id
+        for (int i = tid; i < nslots; i += kThreads) {
+            const int t = i % p.topk;
+            const int j = sel[i];
+            int keep = -1;
+            if (j >= nvalid) {
+                set_status(p.status, MSA_STATUS_INDEX_RANGE);
+            } else if (j >= 0) {
+                bool dup = false;
+                for (int u = 1; u <= t; ++u) dup |= sel[i - u] == j;
+                if (dup) {
+                    set_status(p.status, MSA_STATUS_DUPLICATE);
+                } else {
+                    keep = j;
+                    atomicOr(&bitmap[j >> 5], 1u << (j & 31));
+                }
+            }
+            kept[i] = keep;
+        }
+        __syncthreads();
+        // the union in ascending block order: each word's exclusive prefix
+        // of set bits, and the union list
+        const int per = (nwords + kThreads - 1) / kThreads;
+        const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+        int cnt = 0;
+        for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+        int v = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane == 31) warp_tot[warp] = v;
+        __syncthreads();
+        int pos = v - cnt;
+        for (int w = 0; w < warp; ++w) pos += warp_tot[w];
+        for (int w = w0; w < w1; ++w) {
+            wpre[w] = pos;
+            uint32_t m = bitmap[w];
+            while (m) {
+                const int bit = __ffs(m) - 1;
+                m &= m - 1;
+                ul[pos++] = w * 32 + bit;
+            }
+        }
+        if (tid == kThreads - 1) *s_nu = pos;
+        __syncthreads();
+        nu = *s_nu;
+        // the queries of each union block: a kept id's union position is its
+        // word's prefix plus the set bits below it
+        for (int i = tid; i < nslots; i += kThreads) {
+            const int j = kept[i];
+            if (j < 0) continue;
+            const int qi = i / p.topk;
+            const int e = wpre[j >> 5] + __popc(bitmap[j >> 5] & ((1u << (j & 31)) - 1u));
+            atomicOr(&msk[e * p.wq + (qi >> 5)], 1u << (qi & 31));
+        }
+        __syncthreads();
+    } else {
+        nu = nvalid;  // dense: every block of the sequence, every query
+        if (tid == 0) *s_nu = nu;
+    }
+    const int64_t gbase = (int64_t)g * p.maxu;
+    for (int e = tid; e < nu; e += kThreads) {
+        const int j = p.q2k ? ul[e] : e;
+        int pg = ptab[j];
+        if (pg < 0 || pg >= p.num_pages) {
+            set_status(p.status, MSA_STATUS_PAGE_RANGE);
+            pg = -1;  // the decode skips the block
+        }
+        p.ublk[gbase + e] = j;
+        p.upage[gbase + e] = pg;
+        for (int w = 0; w < p.wq; ++w) {
+            uint32_t m;
+            if (p.q2k) {
+                m = msk[e * p.wq + w];
+            } else {
+                const int nb = min(32, x.nq - 32 * w);
+                m = nb <= 0 ? 0u : (nb == 32 ? 0xffffffffu : (1u << nb) - 1u);
+            }
+            p.umask[(gbase + e) * p.wq + w] = m;
+        }
+    }
+    if (tid == 0) {
+        p.nunits[g] = nu;
+        p.merge_cnt[g] = 0;
+    }
+    if (nu == 0) {
+        // no visible key for any row of the group: O = 0, LSE = -inf
+        const int rows = x.nq * p.qpk;
+        for (int i = tid; i < rows * 16; i += kThreads) {
+            const int r = i >> 4, c = i & 15;
+            const int64_t row = ((int64_t)x.b * p.Sq + x.q0 + r / p.qpk) * p.Hq + x.h * p.qpk + r % p.qpk;
+            reinterpret_cast<uint4 *>(p.o + row * kD)[c] = make_uint4(0, 0, 0, 0);
+            if (c == 0 && p.lse) p.lse[row] = -INFINITY;
+        }
+    }
+    __syncthreads();  // the scratch is reused by the next group
+}
+
+// Scratch words plan_group uses; its last word is the union size.
+__host__ __device__ inline size_t plan_scratch_words(int max_pages, bool sparse, int qc, int topk, int maxu, int wq) {
+    return (size_t)max_pages + 2 * (size_t)((max_pages + 31) / 32) + (sparse ? 2 * (size_t)qc * topk : 0) +
+           (size_t)maxu * (1 + wq) + kWarps + 2;
+}
+
 }  // namespace pdk
 
 // ---------------------------------------------------------------------------
@@ -245,9 +395,30 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(gbase + L::TSLOT);
-    grid_dependency_wait();  // the plan
+    grid_dependency_wait();  // the plan (local plan: the previous call, which may still read the workspace)
     grid_dependents_launch();
 
+    if (p.local_plan) {
+        // ------------------------------------------------------------ local plan
+        // This CTA's own group, planned into the workspace (the K/V ring is
+        // the scratch); the CTA holds it whole.
+        if ((int)blockIdx.x < p.G) plan_group(p, blockIdx.x, reinterpret_cast<uint32_t *>(gbase));
+        if (tid == 0) {
+            // the union size: the plan scratch's last word
+            const size_t last = plan_scratch_words(p.max_pages, p.q2k != nullptr, p.qc, p.topk, p.maxu, p.wq) - 1;
+            const int n = (int)blockIdx.x < p.G ? reinterpret_cast<const int32_t *>(gbase)[last] : 0;
+            WalkStart st{};
+            st.aligned = 1;
+            st.g0 = blockIdx.x;
+            st.n0 = n;
+            st.ue = n;
+            st.valid = n > 0;
+            st.grid = gridDim.x;
+            st.total = n;
+            *ws = st;
+        }
+        __syncthreads();
+    }
     // ---------------------------------------------------------------- partition
     // Exclusive prefix of the union sizes in the K/V ring (free until the
     // pipeline starts), then this CTA's run of units.  The producer meanwhile
@@ -256,7 +427,7 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
     int page_guess = -1;
     if (KV_FORMAT == MSA_KV_BF16 && warp == kWarpLoad && lane == 0 && (int)blockIdx.x < p.G)
         page_guess = ld_plan(p.upage + (int64_t)blockIdx.x * p.maxu);
-    {
+    if (!p.local_plan) {
         int *scr = reinterpret_cast<int *>(gbase);  // [G + 1] prefix | [kWarps] warp sums | [kWarps] maxima
         int *wsum = scr + p.G + 1, *wmax = wsum + kWarps;
         const int per = (p.G + kThreads - 1) / kThreads;

@@ -279,7 +279,9 @@ int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int 
  *              masks, and per SM two 128-row pieces (O and LSE) of the
  *              groups the partition cuts.  The size depends on the current
  *              device's SM count.
- * The work, in two launches: per group (sequence b, KV head h, 128/(Hq/Hkv)
+ * The work, in two launches (one when there are at most as many groups as
+ * SMs and no union can exceed 10 blocks: each CTA of the decode kernel then
+ * plans its own group): per group (sequence b, KV head h, 128/(Hq/Hkv)
  * consecutive queries) the ascending union of the blocks its queries
  * selected (ids at or past ceil(seqused_k[b]/page) are padding and set
  * MSA_STATUS_INDEX_RANGE; repeats of one query set MSA_STATUS_DUPLICATE and
