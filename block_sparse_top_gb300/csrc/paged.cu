@@ -10,143 +10,15 @@
 namespace msa {
 
 // ---------------------------------------------------------------------------
-// plan: one CTA (256 threads) per group
-// ---------------------------------------------------------------------------
-// Dynamic shared memory: the sequence's page-table row [max_pages] | bitmap
-// [ceil(max_pages/32)] | slots [qc*topk] | kept [qc*topk] | union [maxu] |
-// masks [maxu][wq].
+// plan: one CTA (256 threads) per group; the plan itself is plan_group
+// (paged_tc.cuh), which the decode kernel's local-plan mode runs too.
+// Dynamic shared memory: plan_scratch_words words.
 __global__ void __launch_bounds__(256) paged_plan_kernel(DecodeParams p) {
     extern __shared__ uint32_t dsm[];
-    const int nwords = (p.max_pages + 31) >> 5;
-    const int nslot_max = p.q2k ? p.qc * p.topk : 0;
-    int32_t *ptab = reinterpret_cast<int32_t *>(dsm);
-    uint32_t *bitmap = dsm + p.max_pages;
-    int32_t *sel = reinterpret_cast<int32_t *>(bitmap + nwords);
-    int32_t *kept = sel + nslot_max;
-    int32_t *ul = kept + nslot_max;
-    uint32_t *msk = reinterpret_cast<uint32_t *>(ul + p.maxu);
-    __shared__ int32_t warp_tot[8];
-    __shared__ int32_t s_nu;
-    const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dependency_wait();  // the previous call's decode kernel may still read this workspace
     grid_dependents_launch();
-    const DGroup x = dgroup(p, g);
-    const int kv = p.seqused[x.b];
-    const int nvalid = kv <= 0 ? 0 : (int)min(ceil_div(kv, kBlk), (int64_t)p.max_pages);
-    // the sequence's pages, loaded with the selections rather than after the union
-    for (int i = tid; i < nvalid; i += blockDim.x) ptab[i] = p.page_table[(int64_t)x.b * p.max_pages + i];
-    int nu;
-    if (p.q2k) {
-        const int nslots = x.nq * p.topk;
-        const int32_t *src = p.q2k + (((int64_t)x.b * p.Hkv + x.h) * p.Sq + x.q0) * p.topk;
-        for (int i = tid; i < nwords; i += blockDim.x) bitmap[i] = 0u;
-        for (int i = tid; i < nslots; i += blockDim.x) sel[i] = src[i];
-        __syncthreads();
-        // a slot is kept when its id is a valid block and no earlier slot of
-        // its query holds the same id
-        for (int i = tid; i < nslots; i += blockDim.x) {
-            const int t = i % p.topk;
-            const int j = sel[i];
-            int keep = -1;
-            if (j >= nvalid) {
-                set_status(p.status, MSA_STATUS_INDEX_RANGE);
-            } else if (j >= 0) {
-                bool dup = false;
-                for (int u = 1; u <= t; ++u) dup |= sel[i - u] == j;
-                if (dup) {
-                    set_status(p.status, MSA_STATUS_DUPLICATE);
-                } else {
-                    keep = j;
-                    atomicOr(&bitmap[j >> 5], 1u << (j & 31));
-                }
-            }
-            kept[i] = keep;
-        }
-        __syncthreads();
-        // compact the bitmap in ascending block order
-        const int per = (nwords + blockDim.x - 1) / blockDim.x;
-        const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
-        int cnt = 0;
-        for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
-        int v = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += y;
-        }
-        if (lane == 31) warp_tot[warp] = v;
-        __syncthreads();
-        int pos = v - cnt;
-        for (int w = 0; w < warp; ++w) pos += warp_tot[w];
-        for (int w = w0; w < w1; ++w) {
-            uint32_t m = bitmap[w];
-            while (m) {
-                const int bit = __ffs(m) - 1;
-                m &= m - 1;
-                ul[pos++] = w * 32 + bit;
-            }
-        }
-        if (tid == blockDim.x - 1) s_nu = pos;
-        __syncthreads();
-        nu = s_nu;
-        // the queries of each union block
-        for (int i = tid; i < nu * p.wq; i += blockDim.x) msk[i] = 0u;
-        __syncthreads();
-        for (int i = tid; i < nslots; i += blockDim.x) {
-            const int j = kept[i];
-            if (j < 0) continue;
-            const int qi = i / p.topk;
-            int lo = 0, hi = nu;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (ul[mid] < j) lo = mid + 1;
-                else hi = mid;
-            }
-            atomicOr(&msk[lo * p.wq + (qi >> 5)], 1u << (qi & 31));
-        }
-        __syncthreads();
-    } else {
-        nu = nvalid;  // dense: every block of the sequence, every query
-        __syncthreads();
-    }
-    const int64_t gbase = (int64_t)g * p.maxu;
-    for (int e = tid; e < nu; e += blockDim.x) {
-        const int j = p.q2k ? ul[e] : e;
-        int pg = ptab[j];
-        if (pg < 0 || pg >= p.num_pages) {
-            set_status(p.status, MSA_STATUS_PAGE_RANGE);
-            pg = -1;  // the decode kernel skips the block
-        }
-        p.ublk[gbase + e] = j;
-        p.upage[gbase + e] = pg;
-        for (int w = 0; w < p.wq; ++w) {
-            uint32_t m;
-            if (p.q2k) {
-                m = msk[e * p.wq + w];
-            } else {
-                const int nb = min(32, x.nq - 32 * w);
-                m = nb <= 0 ? 0u : (nb == 32 ? 0xffffffffu : (1u << nb) - 1u);
-            }
-            p.umask[(gbase + e) * p.wq + w] = m;
-        }
-    }
-    if (tid == 0) {
-        p.nunits[g] = nu;
-        p.merge_cnt[g] = 0;
-    }
-    if (nu == 0) {
-        // no visible key for any row of the group: O = 0, LSE = -inf
-        const int rows = x.nq * p.qpk;
-        for (int i = tid; i < rows * 16; i += blockDim.x) {
-            const int r = i >> 4, c = i & 15;
-            const int64_t row = ((int64_t)x.b * p.Sq + x.q0 + r / p.qpk) * p.Hq + x.h * p.qpk + r % p.qpk;
-            reinterpret_cast<uint4 *>(p.o + row * kD)[c] = make_uint4(0, 0, 0, 0);
-            if (c == 0 && p.lse) p.lse[row] = -INFINITY;
-        }
-    }
+    pdk::plan_group<256>(p, blockIdx.x, dsm);
 }
-
-
 
 namespace {
 
@@ -271,10 +143,8 @@ int paged_decode(const void *q, const void *k_pool, const void *v_pool, int kv_f
                            pdk::Layout::Q;
     p.local_plan = local ? 1 : 0;
     if (!local) {
-        const int nwords = (max_pages + 31) / 32;
-        const size_t psmem = sizeof(uint32_t) *
-                             ((size_t)max_pages +
-                              (q2k ? (size_t)nwords + 2 * (size_t)d.qc * topk + (size_t)d.maxu * (1 + d.wq) : 0));
+        const size_t psmem =
+            sizeof(uint32_t) * pdk::plan_scratch_words(max_pages, q2k != nullptr, d.qc, topk, d.maxu, d.wq);
         MSA_CUDA_TRY(cudaFuncSetAttribute(paged_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem));
         MSA_CUDA_TRY(launch_pdl(paged_plan_kernel, dim3(d.G), dim3(256), psmem, stream, p));
     }

@@ -193,15 +193,18 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
     return r != 0;
 }
 
-// Plan of group g by all threads of the CTA, for the local-plan mode (every
-// thread calls it alike; it ends at a CTA barrier): the same plan the plan
-// kernel writes.  Every global load is issued up front (the
+constexpr int kRowUpFront = 1024;  // page-table rows loaded whole by the plan
+
+// Plan of group g by all NT threads of the CTA (every thread calls it alike;
+// it ends at a CTA barrier), for the plan kernel (256 threads, one group per
+// CTA) and the decode kernel's local-plan mode (its 384 threads).  Every global load is issued up front (the
 // sequence length, its whole page-table row and the group's selections), so
 // the plan waits on one round trip.  Scratch (32-bit words, in the K/V ring):
 // page-table row [max_pages] | bitmap [nw] | per-word prefix [nw] | slots
 // [qc topk] | kept [qc topk] | union [maxu] | masks [maxu][wq] | warp sums
 // [kWarps] | sequence length | union size, nw = ceil(max_pages / 32).
-static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uint32_t *scr) {
+template <int NT>
+__device__ __noinline__ void plan_group(const DecodeParams &p, int g, uint32_t *scr) {
     const int nwords = (p.max_pages + 31) >> 5;
     const int nslot_max = p.q2k ? p.qc * p.topk : 0;
     int32_t *ptab = reinterpret_cast<int32_t *>(scr);
@@ -212,28 +215,34 @@ static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uin
     int32_t *ul = kept + nslot_max;
     uint32_t *msk = reinterpret_cast<uint32_t *>(ul + p.maxu);
     int32_t *warp_tot = reinterpret_cast<int32_t *>(msk + p.maxu * p.wq);
-    int32_t *s_kv = warp_tot + kWarps;
+    int32_t *s_kv = warp_tot + kWarps;  // (kWarps >= NW words reserved)
     int32_t *s_nu = s_kv + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const DGroup x = dgroup(p, g);
     const int nslots = p.q2k ? x.nq * p.topk : 0;
     // ---- loads (one round trip) and zeroed tables
     if (tid == 0) *s_kv = __ldg(p.seqused + x.b);
-    for (int i = tid; i < p.max_pages; i += kThreads) ptab[i] = __ldg(p.page_table + (int64_t)x.b * p.max_pages + i);
+    // a short page-table row is loaded whole, with the selections; a long one
+    // (many groups would each read it) only up to the sequence's length
+    const bool row_up_front = p.max_pages <= kRowUpFront;
+    if (row_up_front)
+        for (int i = tid; i < p.max_pages; i += NT) ptab[i] = __ldg(p.page_table + (int64_t)x.b * p.max_pages + i);
     if (p.q2k) {
         const int32_t *src = p.q2k + (((int64_t)x.b * p.Hkv + x.h) * p.Sq + x.q0) * p.topk;
-        for (int i = tid; i < nslots; i += kThreads) sel[i] = __ldg(src + i);
-        for (int i = tid; i < nwords; i += kThreads) bitmap[i] = 0u;
-        for (int i = tid; i < p.maxu * p.wq; i += kThreads) msk[i] = 0u;
+        for (int i = tid; i < nslots; i += NT) sel[i] = __ldg(src + i);
+        for (int i = tid; i < nwords; i += NT) bitmap[i] = 0u;
+        for (int i = tid; i < p.maxu * p.wq; i += NT) msk[i] = 0u;
     }
     __syncthreads();
     const int kv = *s_kv;
     const int nvalid = kv <= 0 ? 0 : (int)min(ceil_div(kv, kBlk), (int64_t)p.max_pages);
+    if (!row_up_front)  // (read after the barriers below)
+        for (int i = tid; i < nvalid; i += NT) ptab[i] = __ldg(p.page_table + (int64_t)x.b * p.max_pages + i);
     int nu;
     if (p.q2k) {
         // a slot is kept when its id is a valid block and no earlier slot of
         // its query holds the same id
-        for (int i = tid; i < nslots; i += kThreads) {
+        for (int i = tid; i < nslots; i += NT) {
             const int t = i % p.topk;
             const int j = sel[i];
             int keep = -1;
@@ -254,7 +263,7 @@ static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uin
         __syncthreads();
         // the union in ascending block order: each word's exclusive prefix
         // of set bits, and the union list
-        const int per = (nwords + kThreads - 1) / kThreads;
+        const int per = (nwords + NT - 1) / NT;
         const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
         int cnt = 0;
         for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
@@ -277,12 +286,12 @@ static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uin
                 ul[pos++] = w * 32 + bit;
             }
         }
-        if (tid == kThreads - 1) *s_nu = pos;
+        if (tid == NT - 1) *s_nu = pos;
         __syncthreads();
         nu = *s_nu;
         // the queries of each union block: a kept id's union position is its
         // word's prefix plus the set bits below it
-        for (int i = tid; i < nslots; i += kThreads) {
+        for (int i = tid; i < nslots; i += NT) {
             const int j = kept[i];
             if (j < 0) continue;
             const int qi = i / p.topk;
@@ -295,7 +304,7 @@ static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uin
         if (tid == 0) *s_nu = nu;
     }
     const int64_t gbase = (int64_t)g * p.maxu;
-    for (int e = tid; e < nu; e += kThreads) {
+    for (int e = tid; e < nu; e += NT) {
         const int j = p.q2k ? ul[e] : e;
         int pg = ptab[j];
         if (pg < 0 || pg >= p.num_pages) {
@@ -322,7 +331,7 @@ static __device__ __noinline__ void plan_group(const DecodeParams &p, int g, uin
     if (nu == 0) {
         // no visible key for any row of the group: O = 0, LSE = -inf
         const int rows = x.nq * p.qpk;
-        for (int i = tid; i < rows * 16; i += kThreads) {
+        for (int i = tid; i < rows * 16; i += NT) {
             const int r = i >> 4, c = i & 15;
             const int64_t row = ((int64_t)x.b * p.Sq + x.q0 + r / p.qpk) * p.Hq + x.h * p.qpk + r % p.qpk;
             reinterpret_cast<uint4 *>(p.o + row * kD)[c] = make_uint4(0, 0, 0, 0);
@@ -402,7 +411,7 @@ __global__ void __launch_bounds__(pdk::kThreads, 1)
         // ------------------------------------------------------------ local plan
         // This CTA's own group, planned into the workspace (the K/V ring is
         // the scratch); the CTA holds it whole.
-        if ((int)blockIdx.x < p.G) plan_group(p, blockIdx.x, reinterpret_cast<uint32_t *>(gbase));
+        if ((int)blockIdx.x < p.G) plan_group<kThreads>(p, blockIdx.x, reinterpret_cast<uint32_t *>(gbase));
         if (tid == 0) {
             // the union size: the plan scratch's last word
             const size_t last = plan_scratch_words(p.max_pages, p.q2k != nullptr, p.qc, p.topk, p.maxu, p.wq) - 1;
