@@ -49,30 +49,36 @@ int tiles_launch(const TcParams &t, int64_t capacity, const void *q, const void 
                  int kv_format, bool opts, cudaStream_t stream, bool qk_fp8) {
     int grid = (int)std::min<int64_t>(capacity, (int64_t)num_sms());
     if (grid < 1) grid = 1;
-    CUtensorMap mk, mv, mq;
+    CUtensorMap mk, mv, mq, mqh;
     memset(&mk, 0, sizeof mk);
     memset(&mv, 0, sizeof mv);
+    memset(&mqh, 0, sizeof mqh);
     if (qk_fp8) {
         // e4m3 Q and K by TMA, e4m3 V staged by the dequantising warp
         if (!make_q8_map(&mq, q, t.total_q * t.Hq, t.qpk) || !make_k8_map(&mk, k, t.Hkv, kv_tokens))
             return MSA_ERR_CUDA;
-        return opts ? launch_tiles_qk8_opts(mk, mv, mq, t, grid, stream) : launch_tiles_qk8(mk, mv, mq, t, grid, stream);
+        return opts ? launch_tiles_qk8_opts(mk, mv, mq, mqh, t, grid, stream)
+                    : launch_tiles_qk8(mk, mv, mq, mqh, t, grid, stream);
     }
+    // qpk < 8: rows gathered four at a time, or, for a chunk of consecutive
+    // query positions, one (positions x heads) box per column half
     const bool q_ok = t.qpk >= 8 ? make_q_group_map(&mq, q, t.total_q * t.Hkv, t.qpk)
-                                 : make_q_map(&mq, q, t.total_q * t.Hq, 1);
+                                 : make_q_map(&mq, q, t.total_q * t.Hq, 1) &&
+                                       make_q_heads_map(&mqh, q, t.total_q, t.Hq, t.qpk);
     if (!q_ok) return MSA_ERR_CUDA;
     if (kv_format == MSA_KV_BF16) {
         if (!make_kv_map(&mk, k, t.Hkv, kv_tokens) || !make_kv_map(&mv, v, t.Hkv, kv_tokens)) return MSA_ERR_CUDA;
         // two K/V stages and three Q stages
-        return opts ? launch_tiles_bf16_opts(mk, mv, mq, t, grid, stream)
-                    : launch_tiles_bf16(mk, mv, mq, t, grid, stream);
+        return opts ? launch_tiles_bf16_opts(mk, mv, mq, mqh, t, grid, stream)
+                    : launch_tiles_bf16(mk, mv, mq, mqh, t, grid, stream);
     }
     // NVFP4 / FP8: the dequantising warp reads K and V itself (no K/V maps)
     if (kv_format == MSA_KV_FP8) {
-        return opts ? launch_tiles_fp8_opts(mk, mv, mq, t, grid, stream) : launch_tiles_fp8(mk, mv, mq, t, grid, stream);
+        return opts ? launch_tiles_fp8_opts(mk, mv, mq, mqh, t, grid, stream)
+                    : launch_tiles_fp8(mk, mv, mq, mqh, t, grid, stream);
     }
-    return opts ? launch_tiles_nvfp4_opts(mk, mv, mq, t, grid, stream)
-                : launch_tiles_nvfp4(mk, mv, mq, t, grid, stream);
+    return opts ? launch_tiles_nvfp4_opts(mk, mv, mq, mqh, t, grid, stream)
+                : launch_tiles_nvfp4(mk, mv, mq, mqh, t, grid, stream);
 }
 
 namespace {

@@ -139,7 +139,8 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
 template <int KV_FORMAT, int NKV, int NQ, bool OPTS>
 __global__ void __launch_bounds__(tck::kThreads, 1)
     sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_q, TcParams p) {
+                         const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qh,
+                         TcParams p) {
     using namespace tck;
     constexpr bool QK8 = KV_FORMAT == kKvQk8;
     constexpr uint32_t KS = QK8 ? 16384u : 32768u, QS = QK8 ? 16384u : 32768u;  // K and Q stage bytes
@@ -323,6 +324,16 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 if (lane < nq)
                     tc::tma_load_5d(qt + (uint32_t)(lane * p.qpk * 256), &tm_q, bar(L::Q_FULL + qs), 0, 0, 0, 0,
                                     ids[0] * p.Hkv + x.h);
+            } else if (__all_sync(0xffffffffu, (lane >= nq || ids[0] == first + lane) &&
+                                                   (32 + lane >= nq || ids[1] == first + 32 + lane) &&
+                                                   (64 + lane >= nq || ids[2] == first + 64 + lane) &&
+                                                   (96 + lane >= nq || ids[3] == first + 96 + lane)) &&
+                       nq == qc) {
+                // consecutive query positions (a sink or diagonal block's
+                // queries): the chunk's rows are one box of (positions x heads
+                // x 64 columns) per column half, rows in the gather's order
+                if (lane < 2)
+                    tc::tma_load_3d(qt + lane * 16384u, &tm_qh, bar(L::Q_FULL + qs), lane * 64, x.h * p.qpk, first);
             } else {
                 // lane j issues the gather4 pair of rows 4j .. 4j+3
                 int r[4];

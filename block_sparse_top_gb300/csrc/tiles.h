@@ -32,9 +32,9 @@ int combine_launch(const int32_t *split_counts, int64_t groups, int qpk, int top
 // One launch function per tile-kernel instance, each compiled in a
 // translation unit of its own (tiles_*.cu) so that the build runs them in
 // parallel.
-#define MSA_TILE_INSTANCE(NAME)                                                                                   \
-    int NAME(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid, \
-             cudaStream_t stream)
+#define MSA_TILE_INSTANCE(NAME)                                                                             \
+    int NAME(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const CUtensorMap &mqh, \
+             const TcParams &t, int grid, cudaStream_t stream)
 MSA_TILE_INSTANCE(launch_tiles_bf16);
 MSA_TILE_INSTANCE(launch_tiles_bf16_opts);
 MSA_TILE_INSTANCE(launch_tiles_nvfp4);
@@ -46,14 +46,14 @@ MSA_TILE_INSTANCE(launch_tiles_qk8_opts);
 
 // The launch of instance <KV_FORMAT, NKV, NQ, OPTS> (used by tiles_*.cu).
 template <int KV_FORMAT, int NKV, int NQ, bool OPTS>
-int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const TcParams &t, int grid,
-                 cudaStream_t stream) {
+int launch_tiles(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mq, const CUtensorMap &mqh,
+                 const TcParams &t, int grid, cudaStream_t stream) {
     constexpr uint32_t S = KV_FORMAT == tck::kKvQk8 ? 16384u : 32768u;  // K and Q stage bytes
     const size_t smem = tck::Layout<NKV, NQ, S, S>::BYTES;
     MSA_CUDA_TRY(cudaFuncSetAttribute(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, OPTS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     MSA_CUDA_TRY(launch_pdl(sparse_fwd_tc_kernel<KV_FORMAT, NKV, NQ, OPTS>, dim3(grid),
-                            dim3(tck::kThreads), smem, stream, mk, mv, mq, t));
+                            dim3(tck::kThreads), smem, stream, mk, mv, mq, mqh, t));
     return MSA_OK;
 }
 

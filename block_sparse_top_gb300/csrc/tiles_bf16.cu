@@ -2,5 +2,7 @@
 #include "tiles.h"
 
 namespace msa {
-MSA_TILE_INSTANCE(launch_tiles_bf16) { return launch_tiles<MSA_KV_BF16, 2, 3, false>(mk, mv, mq, t, grid, stream); }
+MSA_TILE_INSTANCE(launch_tiles_bf16) {
+    return launch_tiles<MSA_KV_BF16, 2, 3, false>(mk, mv, mq, mqh, t, grid, stream);
+}
 }  // namespace msa

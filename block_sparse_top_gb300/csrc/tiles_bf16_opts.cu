@@ -2,5 +2,7 @@
 #include "tiles.h"
 
 namespace msa {
-MSA_TILE_INSTANCE(launch_tiles_bf16_opts) { return launch_tiles<MSA_KV_BF16, 2, 3, true>(mk, mv, mq, t, grid, stream); }
+MSA_TILE_INSTANCE(launch_tiles_bf16_opts) {
+    return launch_tiles<MSA_KV_BF16, 2, 3, true>(mk, mv, mq, mqh, t, grid, stream);
+}
 }  // namespace msa

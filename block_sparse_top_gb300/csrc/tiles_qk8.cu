@@ -2,5 +2,7 @@
 #include "tiles.h"
 
 namespace msa {
-MSA_TILE_INSTANCE(launch_tiles_qk8) { return launch_tiles<tck::kKvQk8, 3, 4, false>(mk, mv, mq, t, grid, stream); }
+MSA_TILE_INSTANCE(launch_tiles_qk8) {
+    return launch_tiles<tck::kKvQk8, 3, 4, false>(mk, mv, mq, mqh, t, grid, stream);
+}
 }  // namespace msa

@@ -4,6 +4,6 @@
 
 namespace msa {
 MSA_TILE_INSTANCE(launch_tiles_qk8_opts) {
-    return launch_tiles<tck::kKvQk8, 3, 4, true>(mk, mv, mq, t, grid, stream);
+    return launch_tiles<tck::kKvQk8, 3, 4, true>(mk, mv, mq, mqh, t, grid, stream);
 }
 }  // namespace msa
