@@ -57,6 +57,7 @@ PROFILED_TRAFFIC: dict = {
     "7cb41653a1839e32": 1.0781e10,  # 2.24 GB read + 8.54 GB written
     "3b71fc819f216446": 1.0738e10,  # 2.20 GB read + 8.54 GB written
     "cc01a715c29fdf13": 1.0761e10,  # 2.22 GB read + 8.54 GB written
+    "6f386edfcd051062": 1.0790e10,  # 2.25 GB read + 8.54 GB written
 }
 
 
