@@ -93,12 +93,16 @@ static_assert(sizeof(PlanUnit) == 16, "plan unit is 16 bytes");
 constexpr int kMaxHkv = 32767;  // KV heads a plan unit can name
 
 inline int q_per_chunk(int qpk) { return 128 / qpk; }
-// Queries per unit: 8 chunks (K/V block loaded once per unit).
-inline int q_per_unit(int qpk) { return 8 * q_per_chunk(qpk); }
+// Queries per unit (its K/V block is loaded once for all its chunks): 8
+// chunks for qhead_per_kv >= 8, 16 below, where a chunk holds 32 or more
+// queries, units are few per block and a dequantised (NVFP4, e4m3) block is
+// converted once per unit.  Tile times against 8 chunks: 32K qpk 16 +1 %,
+// 48K qpk 16 +3 % at 16 chunks; 384K qpk 2 bf16 -3.4 %, NVFP4 -20 %.
+inline int q_per_unit(int qpk) { return (qpk >= 8 ? 8 : 16) * q_per_chunk(qpk); }
 
 // Queries per wave.  Units run head-major, then wave by wave, and a unit never
 // crosses a wave, so W trades the reach of the queries the CTAs read at one
-// time against unit length (a unit's K/V block is loaded once for up to 8
+// time against unit length (a unit's K/V block is loaded once for all its
 // chunks).  W is sized by the split partials one (KV head, wave) pass writes
 // -- W * qhead_per_kv * topk rows of D bf16 plus two floats -- at about 512
 // MiB for qhead_per_kv >= 8 (on the 32K causal workload the tiles took 2.263
