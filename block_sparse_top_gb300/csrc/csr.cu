@@ -74,22 +74,6 @@ __device__ __forceinline__ const int32_t *sel_of(const int32_t *q2k, const CsrSh
                   : q2k + (((int64_t)b * s.Hkv + h) * s.Sq + sl) * s.topk;
 }
 
-// Validity of one slot: 0 <= j < nvalid and not named by an earlier slot.
-__device__ __forceinline__ bool slot_valid(const int32_t *sel, int t, int nvalid, uint32_t *status) {
-    int j = sel[t];
-    if (j < 0) return false;
-    if (j >= nvalid) {
-        set_status(status, MSA_STATUS_INDEX_RANGE);
-        return false;
-    }
-    for (int u = 0; u < t; ++u)
-        if (sel[u] == j) {
-            set_status(status, MSA_STATUS_DUPLICATE);
-            return false;
-        }
-    return true;
-}
-
 // Blocks of sequence b a query may name: those below the used KV length.
 __device__ __forceinline__ int seq_nvalid(const int32_t *seqused, int b, const Seq &x) {
     int64_t kv = seqused ? (int64_t)seqused[b] : (int64_t)x.kv;
@@ -97,6 +81,56 @@ __device__ __forceinline__ int seq_nvalid(const int32_t *seqused, int b, const S
     if (n > x.nblk) n = x.nblk;
     if (n < 0) n = 0;
     return (int)n;
+}
+
+// One query's top-k list in registers (ids[0 .. topk), topk <= 32; read as
+// 16-byte vectors when the list is 16-byte aligned -- topk is a multiple of 4,
+// so it is whenever q2k is) and the mask of its valid slots: bit t set when
+// slot t names a block 0 <= j < nvalid that no earlier slot named.  With a
+// status word, an id at or past nvalid raises MSA_STATUS_INDEX_RANGE and a
+// repeated id MSA_STATUS_DUPLICATE.
+__device__ __forceinline__ uint32_t load_slots(const int32_t *sel, int topk, int nvalid, uint32_t *status,
+                                               int (&ids)[32]) {
+    const bool vec = (reinterpret_cast<uintptr_t>(sel) & 15u) == 0;
+#pragma unroll
+    for (int t4 = 0; t4 < 8; ++t4) {
+        int4 v = make_int4(-1, -1, -1, -1);
+        if (4 * t4 < topk) {
+            if (vec) {
+                v = __ldg(reinterpret_cast<const int4 *>(sel) + t4);
+            } else {
+                v = make_int4(__ldg(sel + 4 * t4), __ldg(sel + 4 * t4 + 1), __ldg(sel + 4 * t4 + 2),
+                              __ldg(sel + 4 * t4 + 3));
+            }
+        }
+        ids[4 * t4 + 0] = v.x;
+        ids[4 * t4 + 1] = v.y;
+        ids[4 * t4 + 2] = v.z;
+        ids[4 * t4 + 3] = v.w;
+    }
+    uint32_t valid = 0u;
+    bool range = false, dup = false;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        if (t >= topk) break;
+        const int j = ids[t];
+        if (j < 0) continue;
+        if (j >= nvalid) {
+            range = true;
+            continue;
+        }
+        bool seen = false;
+#pragma unroll
+        for (int u = 0; u < t; ++u) seen |= ids[u] == j;
+        if (seen) {
+            dup = true;
+            continue;
+        }
+        valid |= 1u << t;
+    }
+    if (status && range) set_status(status, MSA_STATUS_INDEX_RANGE);
+    if (status && dup) set_status(status, MSA_STATUS_DUPLICATE);
+    return valid;
 }
 
 // Ragged batches: the per-sequence table and row offsets row_off [B+1] from
@@ -176,15 +210,12 @@ __device__ void build_masks(uint32_t *masks, const int32_t *q2k, const int32_t *
     int i = threadIdx.x;
     int sq = tile * kTileQ + i;
     if (sq < x.sq) {
-        int nvalid = seq_nvalid(seqused, b, x);
-        const int32_t *sel = sel_of(q2k, s, x, b, h, sq);
-        int cnt = 0;
-        for (int t = 0; t < s.topk; ++t) {
-            if (!slot_valid(sel, t, nvalid, status)) continue;
-            atomicOr(&masks[sel[t] * 4 + (i >> 5)], 1u << (i & 31));
-            ++cnt;
-        }
-        if (split_counts) split_counts[(x.q0 + sq) * s.Hkv + h] = cnt;
+        int ids[32];
+        const uint32_t valid = load_slots(sel_of(q2k, s, x, b, h, sq), s.topk, seq_nvalid(seqused, b, x), status, ids);
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+            if ((valid >> t) & 1u) atomicOr(&masks[ids[t] * 4 + (i >> 5)], 1u << (i & 31));
+        if (split_counts) split_counts[(x.q0 + sq) * s.Hkv + h] = __popc(valid);
     }
     __syncthreads();
 }
@@ -325,8 +356,8 @@ __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_
     int i = threadIdx.x;
     int sq = tile * kTileQ + i;
     if (sq >= x.sq) return;
-    int nvalid = seq_nvalid(seqused, b, x);
-    const int32_t *sel = sel_of(q2k, s, x, b, h, sq);
+    int ids[32];
+    const uint32_t valid = load_slots(sel_of(q2k, s, x, b, h, sq), s.topk, seq_nvalid(seqused, b, x), nullptr, ids);
     const int32_t *off = tile_off + (((int64_t)h * s.B + b) * s.ntiles + tile) * s.nblk;
     const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1) + x.row0;
     int32_t *qi = q_indices + (int64_t)h * s.cap;
@@ -334,14 +365,18 @@ __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_
     int32_t gq = (int32_t)(x.q0 + sq);
     int w = i >> 5;
     uint32_t below = (1u << (i & 31)) - 1u;
+    // every slot's row start and tile offset are loaded before any is used
+    int base[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) base[t] = ((valid >> t) & 1u) ? rp[ids[t]] + off[ids[t]] : 0;
     int rank = 0;
-    for (int t = 0; t < s.topk; ++t) {
-        if (!slot_valid(sel, t, nvalid, nullptr)) continue;
-        int j = sel[t];
-        const uint32_t *m = masks + j * 4;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+        if (!((valid >> t) & 1u)) continue;
+        const uint32_t *m = masks + ids[t] * 4;
         int r = __popc(m[w] & below);
         for (int y = 0; y < w; ++y) r += __popc(m[y]);
-        int64_t pos = (int64_t)rp[j] + off[j] + r;
+        const int64_t pos = (int64_t)base[t] + r;
         qi[pos] = gq;
         qs[pos] = gq | (rank << 24);
         ++rank;
