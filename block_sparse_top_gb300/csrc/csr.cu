@@ -412,6 +412,10 @@ struct PlanShape {
     int64_t W, nwaves;
     int qpu;
     const int32_t *row_off;  // ragged: first row of each sequence [B+1]; uniform: null
+    // uniform batch with Sq a multiple of 128: every wave boundary is a tile
+    // boundary, so a row's position of query b Sq + 128 t is row_ptr plus the
+    // column scan's offset of tile t (tile_off), with no search; else null
+    const int32_t *tile_off;
 };
 
 // Sequence and block of global row r.
@@ -440,8 +444,21 @@ __device__ __forceinline__ void segment_range(const int32_t *row_ptr, const int3
     const int64_t w = rem / s.rows;
     r = rem % s.rows;
     const int32_t *rp = row_ptr + (int64_t)h * (s.rows + 1);
-    const int32_t *qi = q_indices + (int64_t)h * s.cap;
     const int32_t b0 = rp[r], b1 = rp[r + 1];
+    if (ps.tile_off) {
+        const int b = (int)(r / s.nblk), j = (int)(r % s.nblk);
+        const int32_t *off = ps.tile_off + (int64_t)h * s.B * s.ntiles * s.nblk + (int64_t)b * s.ntiles * s.nblk + j;
+        auto pos = [&](int64_t q) -> int32_t {  // first position of the row holding a query >= q
+            const int64_t sl = q - (int64_t)b * s.Sq;
+            if (sl <= 0) return b0;
+            if (sl >= s.Sq) return b1;
+            return b0 + off[(sl / kTileQ) * s.nblk];
+        };
+        lo = pos(w * ps.W);
+        hi = pos((w + 1) * ps.W);
+        return;
+    }
+    const int32_t *qi = q_indices + (int64_t)h * s.cap;
     lo = lower_bound(qi, b0, b1, (int32_t)(w * ps.W));
     hi = lower_bound(qi, lo, b1, (int32_t)((w + 1) * ps.W));
 }
@@ -529,6 +546,7 @@ PlanShape make_plan_shape(const CsrShape &s, int qpk) {
     ps.nwaves = num_waves(s.total_q, qpk, s.topk);
     ps.qpu = q_per_unit(qpk);
     ps.row_off = nullptr;
+    ps.tile_off = nullptr;
     return ps;
 }
 
@@ -605,6 +623,7 @@ int csr_launch(const CsrShape &s, const int32_t *q2k, int qhead_per_kv, const in
     if (plan) {
         PlanShape ps = make_plan_shape(s, qhead_per_kv);
         ps.row_off = row_off;
+        if (!s.seqs && s.Sq % kTileQ == 0 && ps.W % kTileQ == 0) ps.tile_off = tile_counts;
         int32_t *ups = reinterpret_cast<int32_t *>(ws + w.units_per_row);
         int32_t *total = reinterpret_cast<int32_t *>(ws + w.total);
         int64_t n = ps.nwaves * s.Hkv * s.rows;
