@@ -222,9 +222,13 @@ __device__ void build_masks(uint32_t *masks, const int32_t *q2k, const int32_t *
 
 __global__ void csr_hist_kernel(const int32_t *__restrict__ q2k, const int32_t *__restrict__ seqused, CsrShape s,
                                 int32_t *__restrict__ tile_counts, int32_t *__restrict__ split_counts,
-                                uint32_t *status) {
+                                int32_t *__restrict__ row_ptr, uint32_t *status) {
     extern __shared__ uint32_t masks[];
     int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
+    grid_dependency_wait();  // the previous kernel on the stream may still read split_counts
+    grid_dependents_launch();
+    // uniform batch: row_ptr[h][0] = 0 (the column scan writes every other entry)
+    if (!s.seqs && tile == 0 && b == 0 && threadIdx.x == 0) row_ptr[(int64_t)h * (s.rows + 1)] = 0;
     const Seq x = seq_info(s, b);
     if (tile * kTileQ >= x.sq) return;  // past this sequence's queries (whole CTA)
     build_masks(masks, q2k, seqused, s, x, tile, b, h, status, split_counts);
@@ -241,6 +245,8 @@ __global__ void csr_hist_kernel(const int32_t *__restrict__ q2k, const int32_t *
 // blockDim = (32 block columns, ty tile slices): slice y sums its run of
 // tiles, thread y = 0 scans the ty slice sums, each slice rewrites its run.
 __global__ void csr_colscan_kernel(int32_t *__restrict__ tile_counts, int32_t *__restrict__ row_ptr, CsrShape s) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     __shared__ int32_t part[32][33];
     const int ty = blockDim.y;
     int j = blockIdx.x * 32 + threadIdx.x;
@@ -287,6 +293,8 @@ constexpr int kScanItems = 8;
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(int32_t *data, int64_t n, int64_t stride,
                                                                     int exclusive, int32_t *totals) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     __shared__ int32_t tile[kScanItems * kScanThreads + kScanItems * kScanThreads / 32];  // padded rows
     __shared__ int32_t warp_sums[32];
     int32_t *d = data + blockIdx.x * stride;
@@ -348,6 +356,8 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(int32_t *dat
 __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_t *__restrict__ seqused, CsrShape s,
                                    const int32_t *__restrict__ tile_off, const int32_t *__restrict__ row_ptr,
                                    int32_t *__restrict__ q_indices, int32_t *__restrict__ qsplit) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     extern __shared__ uint32_t masks[];
     int tile = blockIdx.x, b = blockIdx.y, h = blockIdx.z;
     const Seq x = seq_info(s, b);
@@ -385,6 +395,8 @@ __global__ void csr_scatter_kernel(const int32_t *__restrict__ q2k, const int32_
 
 __global__ void csr_tail_kernel(const int32_t *__restrict__ row_ptr, CsrShape s, int32_t *__restrict__ q_indices,
                                 int32_t *__restrict__ qsplit) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     int h = blockIdx.y;
     int64_t nnz = row_ptr[(int64_t)h * (s.rows + 1) + s.rows];
     for (int64_t i = nnz + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < s.cap;
@@ -466,6 +478,8 @@ __device__ __forceinline__ void segment_range(const int32_t *row_ptr, const int3
 // Units per segment: ceil(count / q_per_unit).
 __global__ void plan_count_kernel(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ q_indices,
                                   CsrShape s, PlanShape ps, int32_t *__restrict__ units_per_seg) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= ps.nwaves * s.Hkv * s.rows) return;
     int h;
@@ -479,6 +493,8 @@ __global__ void plan_write_kernel(const int32_t *__restrict__ row_ptr, const int
                                   CsrShape s, PlanShape ps, const int32_t *__restrict__ unit_off,
                                   const int32_t *__restrict__ total, PlanHeader *plan, PlanUnit *units, int capacity,
                                   int qpk, uint32_t *status) {
+    grid_dependency_wait();  // the previous CSR step
+    grid_dependents_launch();
     int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx == 0) {
         int32_t tot = *total;
@@ -598,27 +614,26 @@ int csr_launch(const CsrShape &s, const int32_t *q2k, int qhead_per_kv, const in
         smem_set = true;
     }
     dim3 tgrid(s.ntiles, s.B, s.Hkv);
-    csr_hist_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, split_counts, status_dev);
-    MSA_LAUNCH_CHECK();
+    // The CSR kernels are chained with programmatic dependent launch: each
+    // waits for the one before it (grid_dependency_wait) at its start.
+    MSA_CUDA_TRY(launch_pdl(csr_hist_kernel, tgrid, dim3(kTileQ), mask_smem, stream, q2k, seqused, s, tile_counts,
+                            split_counts, row_ptr, status_dev));
     if (s.seqs) {
-        // rows past the sequences' blocks (capacity above need) count 0
+        // rows past the sequences' blocks (capacity above need) count 0 (a
+        // uniform batch's row_ptr[h][0] is written by the histogram kernel)
         MSA_CUDA_TRY(cudaMemsetAsync(row_ptr, 0, sizeof(int32_t) * (size_t)(s.rows + 1) * s.Hkv, stream));
-    } else {
-        // row_ptr[h][0] = 0; the column scan writes every other entry
-        MSA_CUDA_TRY(cudaMemset2DAsync(row_ptr, sizeof(int32_t) * (s.rows + 1), 0, sizeof(int32_t), s.Hkv, stream));
     }
     dim3 cgrid((unsigned)ceil_div(s.nblk, 32), s.B, s.Hkv);
-    csr_colscan_kernel<<<cgrid, dim3(32, (unsigned)std::min(32, s.ntiles)), 0, stream>>>(tile_counts, row_ptr, s);
-    MSA_LAUNCH_CHECK();
+    MSA_CUDA_TRY(launch_pdl(csr_colscan_kernel, cgrid, dim3(32, (unsigned)std::min(32, s.ntiles)), 0, stream,
+                            tile_counts, row_ptr, s));
     // inclusive scan of the row totals in [1, rows]
-    segment_scan_kernel<<<s.Hkv, 1024, 0, stream>>>(row_ptr + 1, s.rows, s.rows + 1, 0, nullptr);
-    MSA_LAUNCH_CHECK();
-    csr_scatter_kernel<<<tgrid, kTileQ, mask_smem, stream>>>(q2k, seqused, s, tile_counts, row_ptr, q_indices,
-                                                             qsplit);
-    MSA_LAUNCH_CHECK();
+    MSA_CUDA_TRY(launch_pdl(segment_scan_kernel, dim3(s.Hkv), dim3(kScanThreads), 0, stream, row_ptr + 1, s.rows,
+                            s.rows + 1, 0, (int32_t *)nullptr));
+    MSA_CUDA_TRY(launch_pdl(csr_scatter_kernel, tgrid, dim3(kTileQ), mask_smem, stream, q2k, seqused, s,
+                            (const int32_t *)tile_counts, (const int32_t *)row_ptr, q_indices, qsplit));
     int tail_blocks = (int)std::min<int64_t>(ceil_div(s.cap, 256), 1024);
-    csr_tail_kernel<<<dim3(tail_blocks, s.Hkv), 256, 0, stream>>>(row_ptr, s, q_indices, qsplit);
-    MSA_LAUNCH_CHECK();
+    MSA_CUDA_TRY(launch_pdl(csr_tail_kernel, dim3(tail_blocks, s.Hkv), dim3(256), 0, stream, (const int32_t *)row_ptr,
+                            s, q_indices, qsplit));
 
     if (plan) {
         PlanShape ps = make_plan_shape(s, qhead_per_kv);
@@ -628,16 +643,16 @@ int csr_launch(const CsrShape &s, const int32_t *q2k, int qhead_per_kv, const in
         int32_t *total = reinterpret_cast<int32_t *>(ws + w.total);
         int64_t n = ps.nwaves * s.Hkv * s.rows;
         int blocks = (int)ceil_div(n, 256);
-        plan_count_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups);
-        MSA_LAUNCH_CHECK();
-        segment_scan_kernel<<<1, 1024, 0, stream>>>(ups, n, 0, 1, total);
-        MSA_LAUNCH_CHECK();
+        MSA_CUDA_TRY(launch_pdl(plan_count_kernel, dim3(blocks), dim3(256), 0, stream, (const int32_t *)row_ptr,
+                                (const int32_t *)q_indices, s, ps, ups));
+        MSA_CUDA_TRY(launch_pdl(segment_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, ups, n, (int64_t)0, 1,
+                                total));
         PlanHeader *ph = static_cast<PlanHeader *>(plan);
         PlanUnit *units = reinterpret_cast<PlanUnit *>(ph + 1);
         int capacity = (int)plan_capacity(s.rows, s.total_q, s.Hkv, s.topk, qhead_per_kv);
-        plan_write_kernel<<<blocks, 256, 0, stream>>>(row_ptr, q_indices, s, ps, ups, total, ph, units, capacity,
-                                                      qhead_per_kv, status_dev);
-        MSA_LAUNCH_CHECK();
+        MSA_CUDA_TRY(launch_pdl(plan_write_kernel, dim3(blocks), dim3(256), 0, stream, (const int32_t *)row_ptr,
+                                (const int32_t *)q_indices, s, ps, (const int32_t *)ups, (const int32_t *)total, ph,
+                                units, capacity, qhead_per_kv, status_dev));
     }
     return MSA_OK;
 }
