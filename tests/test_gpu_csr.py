@@ -136,3 +136,19 @@ def test_csr_deterministic_across_runs():
         b, _ = _gpu_csr(q2k, spec.Skv, spec.qpk)
         for x, y in zip(a, (b.row_ptr, b.q_indices, b.qsplit, b.split_counts)):
             assert torch.equal(x, y)
+
+
+def test_csr_q2k_view_not_16_byte_aligned():
+    """A q2k view starting 4 bytes past a 16-byte boundary takes the builder's
+    scalar loads and gives the same CSR as the oracle."""
+    spec = synth.PrefillSpec("a", B=1, Sq=1000, Skv=2048, Hkv=2, qpk=4, topk=8, causal=True, pattern="sink")
+    q2k = synth.make_prefill_q2k(spec)
+    flat = torch.empty(q2k.numel() + 1, dtype=torch.int32, device=DEV)
+    view = flat[1:].view(q2k.shape)
+    view.copy_(q2k.to(DEV))
+    assert view.data_ptr() % 16 == 4
+    ref = oracle.build_k2q_csr(q2k, spec.Skv)
+    csr, st = _gpu_csr(view, spec.Skv, spec.qpk)
+    _check_equal(csr, ref)
+    _check_plan(csr)
+    assert st == 0
