@@ -545,12 +545,11 @@ def measure_config(spec, dev, steps, warmup, peaks, peak_src):
 def decode_kernels_per_call(spec, num_sms: int) -> int:
     """Kernels one paged-decode call launches: the decode kernel plans each
     group itself (no plan kernel) when every group has a CTA of its own and no
-    union can exceed 10 blocks (the smallest balanced share, 8, plus a
-    quarter)."""
+    union can exceed 16 blocks (twice the smallest balanced share, 8)."""
     qc = 128 // spec.qpk
     groups = spec.B * spec.Hkv * -(-spec.Sq // qc)
     maxu = min(min(spec.Sq, qc) * spec.topk, spec.pages_per_seq)
-    return 1 if groups <= num_sms and maxu <= 10 else KERNELS_PER_PAGED
+    return 1 if groups <= num_sms and maxu <= 16 else KERNELS_PER_PAGED
 
 
 def decode_sweep(args, dev, peaks, peak_src):

@@ -135,10 +135,14 @@ int paged_decode(const void *q, const void *k_pool, const void *v_pool, int kv_f
         mk = mv = mq;  // unused: the staging warp reads the e4m3 pools
     }
     // Local plan: when every group has a CTA of its own and no union can
-    // exceed a quarter over the smallest share (kMinShare units), the
-    // partition gives each group to one CTA whatever the data, so each CTA
-    // plans its own group and the plan kernel is not launched.
-    const bool local = d.G <= d.grid && d.maxu <= pdk::kMinShare + pdk::kMinShare / 4 &&
+    // exceed twice the smallest share (kMinShare units), each CTA plans its
+    // own group and holds it whole, and the plan kernel is not launched.  Up
+    // to a quarter over the smallest share the partition would give each
+    // group to one CTA whatever the data; beyond that, on very uneven unions,
+    // a CTA may hold up to twice an equal share, which still costs less than
+    // cutting groups this short (the merge of a cut group's pieces and the
+    // plan launch).
+    const bool local = d.G <= d.grid && d.maxu <= 2 * pdk::kMinShare &&
                        pdk::plan_scratch_words(max_pages, q2k != nullptr, d.qc, topk, d.maxu, d.wq) * 4 <=
                            pdk::Layout::Q;
     p.local_plan = local ? 1 : 0;

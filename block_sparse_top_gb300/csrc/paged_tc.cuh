@@ -75,8 +75,8 @@ struct DecodeParams {
     // block's max exceeds the reference by more than this (log2 units)
     float p_bound;
     // 1: no plan kernel ran; CTA c < G plans group c itself and holds it whole
-    // (the host sets this only when the partition is certain to give every
-    // group a CTA of its own: G <= grid and maxu <= kMinShare + kMinShare / 4)
+    // (the host sets this only when every group can have a CTA of its own and
+    // no union is long: G <= grid and maxu <= 2 * kMinShare)
     int local_plan;
 };
 

@@ -280,7 +280,7 @@ int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int 
  *              groups the partition cuts.  The size depends on the current
  *              device's SM count.
  * The work, in two launches (one when there are at most as many groups as
- * SMs and no union can exceed 10 blocks: each CTA of the decode kernel then
+ * SMs and no union can exceed 16 blocks: each CTA of the decode kernel then
  * plans its own group): per group (sequence b, KV head h, 128/(Hq/Hkv)
  * consecutive queries) the ascending union of the blocks its queries
  * selected (ids at or past ceil(seqused_k[b]/page) are padding and set
