@@ -120,3 +120,21 @@ def test_decode_peaked_scores_rescale_accumulated_rows():
                                             d["page_table"].cpu(), d["seqused"].cpu(), d["q2k"].cpu(), rows=rows,
                                             scale=8.0)
     assert_attn_close(o[rows], lse[rows], o_ref, l_ref, "decode peaked")
+
+
+def test_decode_uneven_unions_one_launch():
+    """Unions of at most 16 blocks run as one launch, each CTA planning and
+    holding its own group whatever the union sizes: here one group keeps all
+    16 blocks, one keeps 4 and the rest only their last visible block."""
+    spec = D("uneven_unions", B=4, Sq=8, Hkv=2, qpk=16, topk=16, kv_len=2048, trim=17)
+
+    def mutate(d):
+        q2k = d["q2k"]                     # [B, Hkv, Sq, topk], slot 0 = last visible block
+        keep = torch.ones_like(q2k, dtype=torch.bool)
+        keep[:, :, :, 1:] = False
+        keep[0, 0] = True                  # the long group: every slot
+        keep[1, 1, :, :4] = True           # a short one: four slots per query
+        d["q2k"] = torch.where(keep, q2k, torch.full_like(q2k, -1))
+
+    st, _, _ = run_case(spec, mutate=mutate)
+    assert st == 0
