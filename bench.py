@@ -44,7 +44,6 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS_PER_CSR = 8
 KERNELS_PER_PARTIAL = 1  # attention tiles
 KERNELS_PER_COMBINE = 1  # LSE combine
-KERNELS_PER_PAGED = 2    # union plan, decode (one kernel when each CTA plans its own group)
 
 # DRAM traffic (read + write bytes per launch) of the attention-tile kernel on
 # the 32K causal sink workload from one single-pass ncu capture
@@ -542,14 +541,12 @@ def measure_config(spec, dev, steps, warmup, peaks, peak_src):
     return res
 
 
-def decode_kernels_per_call(spec, num_sms: int) -> int:
-    """Kernels one paged-decode call launches: the decode kernel plans each
-    group itself (no plan kernel) when every group has a CTA of its own and no
-    union can exceed 16 blocks (twice the smallest balanced share, 8)."""
-    qc = 128 // spec.qpk
-    groups = spec.B * spec.Hkv * -(-spec.Sq // qc)
-    maxu = min(min(spec.Sq, qc) * spec.topk, spec.pages_per_seq)
-    return 1 if groups <= num_sms and maxu <= 16 else KERNELS_PER_PAGED
+def decode_kernels_per_call(spec) -> int:
+    """Kernels one paged-decode call launches, as the library reports it for
+    this shape on the current device (1: the decode kernel plans each group
+    itself; 2: plan kernel + decode)."""
+    import block_sparse_top_gb300 as msa
+    return msa.paged_fwd_launches(spec.B, spec.Sq, spec.Hq, spec.Hkv, spec.topk, spec.pages_per_seq)
 
 
 def decode_sweep(args, dev, peaks, peak_src):
@@ -604,7 +601,7 @@ def decode_sweep(args, dev, peaks, peak_src):
         gbs = nbytes / (us * 1e-6) / 1e9
         out.append({"L": L, "us": round(us, 2), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
                     "bytes": nbytes, "gathered_kv_bytes_no_dedup": gathered, "input_sets": nsets,
-                    "kernels": decode_kernels_per_call(spec, torch.cuda.get_device_properties(dev).multi_processor_count)})
+                    "kernels": decode_kernels_per_call(spec)})
         del sets, outs, first, graph
         torch.cuda.empty_cache()
     return {"unit": "GB/s", "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,

@@ -291,6 +291,15 @@ def paged_workspace(B: int, Sq: int, Hq: int, Hkv: int, topk: int, max_pages: in
     return _ws(n, device)
 
 
+def paged_fwd_launches(B: int, Sq: int, Hq: int, Hkv: int, topk: int, max_pages: int) -> int:
+    """msa_sparse_attn_paged_fwd_launches: kernels one decode call of this shape
+    launches on the current device (1 or 2; topk = 0 for the dense mode)."""
+    n = lib().msa_sparse_attn_paged_fwd_launches(B, Sq, Hq, Hkv, 128, topk, max_pages)
+    if n < 0:
+        raise MsaError(n, "msa_sparse_attn_paged_fwd_launches")
+    return n
+
+
 def sparse_attn_paged_fwd(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor,
                           seqused: torch.Tensor, q2k: torch.Tensor, *, causal: bool = True,
                           softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,

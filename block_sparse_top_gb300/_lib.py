@@ -99,6 +99,8 @@ def load(path: str):
     L.msa_sparse_attn_combine.restype = I
     L.msa_sparse_attn_paged_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
     L.msa_sparse_attn_paged_fwd_workspace_size.restype = SZ
+    L.msa_sparse_attn_paged_fwd_launches.argtypes = [I, I, I, I, I, I, I]
+    L.msa_sparse_attn_paged_fwd_launches.restype = I
     L.msa_sparse_attn_paged_fwd.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, P, SZ, P, P]
     L.msa_sparse_attn_paged_fwd.restype = I
     L.msa_k2q_csr_varlen_workspace_size.argtypes = [I, I, I, I, I, I, I, I]

@@ -75,6 +75,18 @@ int check_decode_shape(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_
     return MSA_OK;
 }
 
+// Local plan: when every group has a CTA of its own and no union can exceed
+// twice the smallest share (kMinShare units), each CTA plans its own group
+// and holds it whole, and the plan kernel is not launched.  Up to a quarter
+// over the smallest share the partition would give each group to one CTA
+// whatever the data; beyond that, on very uneven unions, a CTA may hold up to
+// twice an equal share, which still costs less than cutting groups this
+// short (the merge of a cut group's pieces and the plan launch).
+bool decode_local_plan(const DecodeShape &d, int max_pages, int topk) {
+    return d.G <= d.grid && d.maxu <= 2 * pdk::kMinShare &&
+           pdk::plan_scratch_words(max_pages, topk > 0, d.qc, topk, d.maxu, d.wq) * 4 <= pdk::Layout::Q;
+}
+
 size_t decode_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages) {
     if (check_decode_shape(B, Sq, Hq, Hkv, D, topk, max_pages) != MSA_OK) return 0;
     return decode_workspace_layout(decode_shape(B, Sq, Hq, Hkv, topk, max_pages)).bytes;
@@ -134,17 +146,7 @@ int paged_decode(const void *q, const void *k_pool, const void *v_pool, int kv_f
     } else {
         mk = mv = mq;  // unused: the staging warp reads the e4m3 pools
     }
-    // Local plan: when every group has a CTA of its own and no union can
-    // exceed twice the smallest share (kMinShare units), each CTA plans its
-    // own group and holds it whole, and the plan kernel is not launched.  Up
-    // to a quarter over the smallest share the partition would give each
-    // group to one CTA whatever the data; beyond that, on very uneven unions,
-    // a CTA may hold up to twice an equal share, which still costs less than
-    // cutting groups this short (the merge of a cut group's pieces and the
-    // plan launch).
-    const bool local = d.G <= d.grid && d.maxu <= 2 * pdk::kMinShare &&
-                       pdk::plan_scratch_words(max_pages, q2k != nullptr, d.qc, topk, d.maxu, d.wq) * 4 <=
-                           pdk::Layout::Q;
+    const bool local = decode_local_plan(d, max_pages, topk);
     p.local_plan = local ? 1 : 0;
     if (!local) {
         const size_t psmem =
@@ -165,6 +167,13 @@ extern "C" size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq
                                                            int max_pages) {
     if (topk <= 0) return 0;
     return decode_workspace_size(B, Sq, Hq, Hkv, D, topk, max_pages);
+}
+
+extern "C" int msa_sparse_attn_paged_fwd_launches(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages) {
+    if (topk < 0) return MSA_ERR_INVALID_ARG;
+    const int rc = check_decode_shape(B, Sq, Hq, Hkv, D, topk, max_pages);
+    if (rc != MSA_OK) return rc;
+    return decode_local_plan(decode_shape(B, Sq, Hq, Hkv, topk, max_pages), max_pages, topk) ? 1 : 2;
 }
 
 extern "C" int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,

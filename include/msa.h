@@ -294,6 +294,15 @@ int msa_sparse_attn_fwd_varlen(const void *q, const void *k, const void *v, int 
  * finishes it last.  Max max_pages: 8192; at most 49152 groups.
  */
 size_t msa_sparse_attn_paged_fwd_workspace_size(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
+/*
+ * Kernel launches one msa_sparse_attn_paged_fwd (topk > 0) or
+ * msa_paged_attn_fwd (topk = 0: the dense mode) call of this shape makes on
+ * the current device: 1 (the decode kernel plans each group itself) or 2
+ * (the plan kernel, then the decode kernel).  Depends only on the shape and
+ * the device's SM count, never on the data.  Returns MSA_ERR_INVALID_ARG or
+ * MSA_ERR_UNSUPPORTED for a shape the calls reject.  Launches nothing.
+ */
+int msa_sparse_attn_paged_fwd_launches(int B, int Sq, int Hq, int Hkv, int D, int topk, int max_pages);
 int msa_sparse_attn_paged_fwd(const void *q, const void *k_pool, const void *v_pool, int num_pages,
                               const int32_t *page_table, int max_pages, const int32_t *seqused_k,
                               const int32_t *q2k, int B, int Sq, int Hq, int Hkv, int D, int page_size,

@@ -82,6 +82,20 @@ def test_decode_size_queries(L):
     assert L.msa_paged_attn_fwd_workspace_size(12289, 1, 64, 4, 128, 16, 8) == 0      # one more
 
 
+def test_decode_launch_count_query(L):
+    # 1K keys (8 pages, unions of at most 8 blocks) and 128 groups: one launch
+    # on any device with at least 128 SMs; 4K keys (unions up to 32): two
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, 16, 8) == 1
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, 16, 16) == 1     # 2K: unions of <= 16
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, 16, 32) == 2
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, 0, 8) == 1       # dense mode, 8 pages
+    assert L.msa_sparse_attn_paged_fwd_launches(4096, 8, 64, 4, 128, 16, 8) == 2    # more groups than SMs
+    # shapes the decode calls reject give their error codes
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, 5, 8) == -2      # topk 5: unsupported
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 63, 4, 128, 16, 8) == -1     # Hq % Hkv
+    assert L.msa_sparse_attn_paged_fwd_launches(32, 8, 64, 4, 128, -1, 8) == -1
+
+
 def test_bad_arguments_are_rejected_before_launch(L):
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
     null = None
