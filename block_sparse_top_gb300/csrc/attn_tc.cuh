@@ -20,7 +20,7 @@
 //   warp 2      MMA issuer (one lane): S_i = Q_i K^T into tensor memory, then
 //               O_{i-1} = P_{i-1} V with P read from tensor memory.
 //   warps 3-6,  softmax for even / odd chunks: each thread owns one S row
-//   warps 7-10  (TMEM lane), reads it in two halves of 64 columns, applies the
+//   warps 7-10  (TMEM lane), reads it in quarters of 32 columns, applies the
 //               bottom-right causal limit, writes P = exp(S - m) as bf16 over
 //               S and stores the split's statistics (m * scale, l = sum P);
 //               the split partial is kept unnormalised so that the combine
@@ -617,12 +617,12 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 const int pb = part_piece_bytes(p.part_dtype);
                 char *dst = static_cast<char *>(p.o_part) + part_o_index(grp, p.topk, p.qpk, split, 0, j_of_row) * pb;
                 const int64_t cstride = (int64_t)p.qpk * pb;
-                uint32_t r[64];
+                uint32_t r[32];
 #pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    tc::tmem_ld64(o_addr + 64 * hf, r);
+                for (int qq = 0; qq < 4; ++qq) {  // quarters of 32 columns: 4 pieces each
+                    tc::tmem_ld32(o_addr + 32 * qq, r);
                     tc::tmem_ld_wait();
-                    if (hf == 1) {
+                    if (qq == 3) {
                         tc::fence_before_sync();
                         tc::mbar_arrive(bar(L::O_EMPTY + b));  // O is read: the next PV may start
                     }
@@ -630,8 +630,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     // streaming stores: evict first from L2
                     if (OPTS && p.part_dtype == MSA_PARTIAL_FP32) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
-                            float4 *d = reinterpret_cast<float4 *>(dst + (8 * hf + v4) * cstride);
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            float4 *d = reinterpret_cast<float4 *>(dst + (4 * qq + v4) * cstride);
                             __stcs(d, make_float4(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]),
                                                   __uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])));
                             __stcs(d + 1, make_float4(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]),
@@ -639,23 +639,23 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         }
                     } else if (OPTS && p.part_dtype == MSA_PARTIAL_FP16) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
+                        for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 o4;
                             o4.x = pack_f16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
                             o4.y = pack_f16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
                             o4.z = pack_f16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
                             o4.w = pack_f16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                            __stcs(reinterpret_cast<uint4 *>(dst + (8 * hf + v4) * cstride), o4);
+                            __stcs(reinterpret_cast<uint4 *>(dst + (4 * qq + v4) * cstride), o4);
                         }
                     } else {
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
+                        for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 o4;
                             o4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]), __uint_as_float(r[8 * v4 + 1]));
                             o4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3]));
                             o4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5]));
                             o4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7]));
-                            __stcs(reinterpret_cast<uint4 *>(dst + (8 * hf + v4) * cstride), o4);
+                            __stcs(reinterpret_cast<uint4 *>(dst + (4 * qq + v4) * cstride), o4);
                         }
                     }
                 }
@@ -716,10 +716,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 }
                 {
                     tc::fence_after_sync();
-                    // The S row is read 64 keys at a time: one pass for the max, one
-                    // for P (a whole row in registers leaves the compiler no room).
-                    uint32_t r[64];
-                    tc::tmem_ld64(s_addr, r);
+                    // The S row is read 32 keys at a time in rolled loops: one pass
+                    // for the max, one for P.
+                    uint32_t r[32];
+                    tc::tmem_ld32(s_addr, r);
                     // row info while the load is in flight
                     const int gq = packed & 0xFFFFFF;
                     const int split = (packed >> 24) & 0xFF;
@@ -732,11 +732,11 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         nvis = nv < 0 ? 0 : (nv > 128 ? 128 : nv);
                     }
                     // keys past the causal limit (diagonal block rows) become -inf
-                    auto mask_half = [&](int hf) {
-                        const int lim = nvis - 64 * hf;
-                        if (lim < 64) {
+                    auto mask_q = [&](int qq) {
+                        const int lim = nvis - 32 * qq;
+                        if (lim < 32) {
 #pragma unroll
-                            for (int j = 0; j < 64; ++j)
+                            for (int j = 0; j < 32; ++j)
                                 if (j >= lim) r[j] = 0xff800000u;
                         }
                     };
@@ -744,35 +744,36 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     float mm[4];
 #pragma unroll
                     for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (hf == 1) tc::tmem_ld64(s_addr + 64, r);
+#pragma unroll 1
+                    for (int qq = 0; qq < 4; ++qq) {
+                        if (qq > 0) tc::tmem_ld32(s_addr + 32 * qq, r);
                         tc::tmem_ld_wait();
-                        mask_half(hf);
+                        mask_q(qq);
 #pragma unroll
-                        for (int j = 0; j < 64; j += 8) {
+                        for (int j = 0; j < 32; j += 8) {
 #pragma unroll
                             for (int a = 0; a < 4; ++a)
                                 mm[a] = fmax3(mm[a], __uint_as_float(r[j + 2 * a]), __uint_as_float(r[j + 2 * a + 1]));
                         }
                     }
                     const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
-                    // P = exp2(S * scale_log2 - m * scale_log2): each half is read
-                    // again, packed to bf16 pairs in place (r[j] <- keys 2j, 2j+1 of
-                    // the half) and stored over columns the half has already read;
-                    // row sum in packed f32x2 adds (TEMP: also of 2^(x / T))
+                    // P = exp2(S * scale_log2 - m * scale_log2): each quarter is
+                    // read again, packed to bf16 pairs in place (r[j] <- keys 2j,
+                    // 2j+1 of the quarter) and stored over columns already read;
+                    // row sum in packed f32x2 adds (TEMP: also of 2^(x / T)), in the
+                    // same order as over whole halves
                     const float mc = (m == -INFINITY) ? 0.f : m * p.scale_log2;
                     const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
                     const float2 nm2 = make_float2(-mc, -mc);
                     float2 ll[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     float2 lt = make_float2(0.f, 0.f);
 #pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tc::tmem_ld64(s_addr + 64 * hf, r);
+                    for (int qq = 0; qq < 4; ++qq) {
+                        tc::tmem_ld32(s_addr + 32 * qq, r);
                         tc::tmem_ld_wait();
-                        mask_half(hf);
+                        mask_q(qq);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < 16; ++j) {
                             float2 e =
                                 __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2, nm2);
                             if (OPTS && p.temp_on) {
@@ -784,7 +785,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                             ll[j & 1] = __fadd2_rn(ll[j & 1], e);
                             r[j] = pack_bf16x2(e.x, e.y);
                         }
-                        tc::tmem_st32(s_addr + 32 * hf, r);
+                        tc::tmem_st16(s_addr + 16 * qq, r);
                     }
                     const float l = (ll[0].x + ll[0].y) + (ll[1].x + ll[1].y);
                     tc::tmem_st_wait();

@@ -354,6 +354,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 #undef MSA_W8
 }
+// Stores r[0..15] into 16 consecutive columns (from a 32-register array).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[32]) {
+#define MSA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                  "r"(r[i + 6]), "r"(r[i + 7])
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16};\n" ::"r"(taddr),
+                 MSA_W8(0), MSA_W8(8)
+                 : "memory");
+#undef MSA_W8
+}
 // Stores r[0..63] into 64 consecutive columns (from a 64-register array).
 __device__ __forceinline__ void tmem_st64h(uint32_t taddr, const uint32_t (&r)[64]) {
 #define MSA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
