@@ -58,6 +58,7 @@ PROFILED_TRAFFIC: dict = {
     "cc01a715c29fdf13": 1.0761e10,  # 2.22 GB read + 8.54 GB written
     "6f386edfcd051062": 1.0790e10,  # 2.25 GB read + 8.54 GB written
     "a80da73977f45668": 1.0778e10,  # 2.24 GB read + 8.54 GB written
+    "362d894189bb3b67": 1.0715e10,  # 2.18 GB read + 8.54 GB written
 }
 
 
