@@ -744,11 +744,19 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     float mm[4];
 #pragma unroll
                     for (int a = 0; a < 4; ++a) mm[a] = -INFINITY;
+                    bool masked = false;
 #pragma unroll 1
                     for (int qq = 0; qq < 4; ++qq) {
                         if (qq > 0) tc::tmem_ld32(s_addr + 32 * qq, r);
                         tc::tmem_ld_wait();
-                        mask_q(qq);
+                        // keys past the causal limit: -inf here and, stored back,
+                        // for the P pass (the store is warp-wide: every lane
+                        // writes its quarter, masked or not)
+                        if (__any_sync(0xffffffffu, nvis - 32 * qq < 32)) {
+                            mask_q(qq);
+                            tc::tmem_st32(s_addr + 32 * qq, r);
+                            masked = true;
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
 #pragma unroll
@@ -757,6 +765,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         }
                     }
                     const float m = fmax3(fmax3(mm[0], mm[1], mm[2]), mm[3], -INFINITY);
+                    if (masked) tc::tmem_st_wait();  // the masked keys are in tensor memory
                     // P = exp2(S * scale_log2 - m * scale_log2): each quarter is
                     // read again, packed to bf16 pairs in place (r[j] <- keys 2j,
                     // 2j+1 of the quarter) and stored over columns already read;
@@ -771,7 +780,6 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     for (int qq = 0; qq < 4; ++qq) {
                         tc::tmem_ld32(s_addr + 32 * qq, r);
                         tc::tmem_ld_wait();
-                        mask_q(qq);
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             float2 e =
