@@ -122,8 +122,8 @@ __device__ __forceinline__ Unit load_unit(const TcParams &p, int u) {
     x.tok0 = pu.blk * kBlk;
     x.start = pu.start;
     x.count = pu.count;
-    int qc = 128 / p.qpk;
-    x.nch = (pu.count + qc - 1) / qc;
+    const int qc_sh = 7 - (31 - __clz(p.qpk));  // log2(128 / qhead_per_kv): qhead_per_kv is a power of two
+    x.nch = (pu.count + (1 << qc_sh) - 1) >> qc_sh;
     return x;
 }
 
@@ -155,7 +155,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + L::ABORT);
     auto bar = [&](int i) -> uint32_t { return base + L::BAR + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qc = 128 / p.qpk;
+    // qhead_per_kv is a power of two: row R of a chunk is query R >> qpk_sh,
+    // head R & (qhead_per_kv - 1)
+    const int qpk_sh = 31 - __clz(p.qpk), qc_sh = 7 - qpk_sh;
+    const int qc = 128 >> qpk_sh;
 
     if (tid == 0) {
         for (int i = 0; i < NKV; ++i) {
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             x.b = e[1];
             x.start = e[2];
             x.count = e[3];
-            x.nch = (x.count + qc - 1) / qc;
+            x.nch = (x.count + qc - 1) >> qc_sh;
             const int seq_k0 = e[5];  // ragged: first key row of the sequence
             int ids[4];
 #pragma unroll
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     int r[4];
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int R = 4 * lane + t, qi = R / p.qpk;
+                        const int R = 4 * lane + t, qi = R >> qpk_sh;
                         const int g0 = __shfl_sync(0xffffffffu, ids[0], qi & 31);
                         const int g1 = __shfl_sync(0xffffffffu, ids[1], qi & 31);
                         const int g2 = __shfl_sync(0xffffffffu, ids[2], qi & 31);
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         const int sl = qi >> 5;
                         int gq = sl == 0 ? g0 : sl == 1 ? g1 : sl == 2 ? g2 : g3;
                         if (gq < 0) gq = first;
-                        r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
+                        r[t] = gq * p.Hq + x.h * p.qpk + (R & (p.qpk - 1));
                     }
                     tc::tma_gather4_hint(qt + lane * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
                 }
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 int r[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const int R = 4 * lane + t, qi = R / p.qpk;
+                    const int R = 4 * lane + t, qi = R >> qpk_sh;
                     const int g0 = __shfl_sync(0xffffffffu, ids[0], qi & 31);
                     const int g1 = __shfl_sync(0xffffffffu, ids[1], qi & 31);
                     const int g2 = __shfl_sync(0xffffffffu, ids[2], qi & 31);
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     const int sl = qi >> 5;
                     int gq = sl == 0 ? g0 : sl == 1 ? g1 : sl == 2 ? g2 : g3;
                     if (gq < 0) gq = first;
-                    r[t] = gq * p.Hq + x.h * p.qpk + (R % p.qpk);
+                    r[t] = gq * p.Hq + x.h * p.qpk + (R & (p.qpk - 1));
                 }
                 tc::tma_gather4_hint(qt + lane * 512, &tm_q, bar(L::Q_FULL + qs), 0, r[0], r[1], r[2], r[3], keep);
                 tc::tma_gather4_hint(qt + 16384 + lane * 512, &tm_q, bar(L::Q_FULL + qs), 64, r[0], r[1], r[2], r[3],
@@ -585,7 +588,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         // The softmax warps store the statistics, so they never wait for PV.
         const int R = 32 * (warp & 3) + lane;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int j_of_row = R % p.qpk, qi = R / p.qpk;
+        const int j_of_row = R & (p.qpk - 1), qi = R >> qpk_sh;
         int ci = 0;
         bool ok = true;
         Unit xnext{};
@@ -667,7 +670,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
         const int R = 32 * (warp & 3) + lane;        // chunk row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t s_addr = tmem + lane_base + wg * 128;
-        const int j_of_row = R % p.qpk;  // query head of the group this row holds
+        const int j_of_row = R & (p.qpk - 1);  // query head of the group this row holds
         int ci = 0;
         bool ok = true;
         // the unit and, loaded one unit ahead, its sequence's key count kv
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             for (int c = 0; c < x.nch && ok; ++c, ++ci) {
                 if ((ci & 1) != wg) continue;
                 const uint32_t par = (ci >> 1) & 1;
-                const int qi = R / p.qpk, idx = c * qc + qi;
+                const int qi = R >> qpk_sh, idx = c * qc + qi;
                 const bool in_chunk = idx < x.count;
                 const int packed = in_chunk ? p.qsplit[(int64_t)x.h * p.cap + x.start + idx] : 0;
                 const bool valid = in_chunk;
