@@ -497,11 +497,17 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
             auto issue_pv = [&](int cj, int kbj, int last) {
                 const int b = cj & 1;
                 tc::fence_after_sync();
-                const uint32_t vs = base + L::V + kbj * 32768;
+                // step kk: P columns 8 kk.., V rows 16 kk.. (2048 bytes, 128
+                // descriptor units, further on)
+                const uint64_t vd = tc::sdesc_sw128(base + L::V + kbj * 32768, 16384, 1024);
+                uint32_t pa[8];
+                uint64_t vb[8];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ts(tmem + 256 + b * 128, tmem + b * 128 + kk * 8,
-                               tc::sdesc_sw128(vs + kk * 2048, 16384, 1024), kIdescPV, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                    pa[kk] = tmem + b * 128 + kk * 8;
+                    vb[kk] = vd + (uint64_t)(kk * 128);
+                }
+                tc::mma_ts8(tmem + 256 + b * 128, pa, vb, kIdescPV);
                 tc::mma_commit(bar(L::O_FULL + b));
                 if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
@@ -518,13 +524,19 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                         tc::mma_ss_f8(tmem + b * 128, tc::sdesc_sw128(qt + kk * 32, 16, 1024),
                                       tc::sdesc_sw128(ks + kk * 32, 16, 1024), kIdescS8, kk > 0);
                 } else {
+                    // step kk: 32 bytes (2 descriptor units) into the row, the
+                    // second 64-column half from kk = 4 (the stage bases are
+                    // 1024-byte aligned, so base + offset never carries out of
+                    // the address field)
+                    const uint64_t qd = tc::sdesc_sw128(qt, 16, q_sbo), kd = tc::sdesc_sw128(ks, 16, 1024);
+                    const uint64_t qd_h = qd + (q_half >> 4), kd_h = kd + (16384u >> 4);
+                    uint64_t qa[8], kb8[8];
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t qoff = (kk >> 2) * q_half + (kk & 3) * 32;
-                        tc::mma_ss(tmem + b * 128, tc::sdesc_sw128(qt + qoff, 16, q_sbo),
-                                   tc::sdesc_sw128(ks + koff, 16, 1024), kIdescS, kk > 0);
+                        qa[kk] = (kk < 4 ? qd : qd_h) + (uint64_t)((kk & 3) * 2);
+                        kb8[kk] = (kk < 4 ? kd : kd_h) + (uint64_t)((kk & 3) * 2);
                     }
+                    tc::mma_ss8(tmem + b * 128, qa, kb8, kIdescS);
                 }
                 tc::mma_commit(bar(L::S_FULL + b));
                 if (release_q) tc::mma_commit(bar(L::Q_EMPTY + qs));

@@ -255,6 +255,42 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 // D[tmem] (+)= A[tmem] * B[smem desc]
+// Eight kind::f16 MMAs (K = 16 each) into d_tmem from one asm block: the
+// first overwrites D, the other seven accumulate; A and B from shared memory
+// (descriptors a[i], b[i]).
+__device__ __forceinline__ void mma_ss8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                        uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %1, %1;\n setp.eq.b32 p1, %1, %1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %1, p0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, p1;\n}\n" ::"r"(d_tmem),
+        "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+        : "memory");
+}
+// The same with A in tensor memory (columns a[i]) and B from shared memory.
+__device__ __forceinline__ void mma_ts8(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                        uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p0, p1;\n setp.ne.b32 p0, %1, %1;\n setp.eq.b32 p1, %1, %1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %1, p0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %1, p1;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %17, %1, p1;\n}\n" ::"r"(d_tmem),
+        "r"(idesc), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+        : "memory");
+}
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
     asm volatile(
