@@ -59,6 +59,7 @@ PROFILED_TRAFFIC: dict = {
     "6f386edfcd051062": 1.0790e10,  # 2.25 GB read + 8.54 GB written
     "a80da73977f45668": 1.0778e10,  # 2.24 GB read + 8.54 GB written
     "362d894189bb3b67": 1.0715e10,  # 2.18 GB read + 8.54 GB written
+    "c932c9210ba72cff": 1.0688e10,  # 2.15 GB read + 8.54 GB written
 }
 
 
