@@ -511,10 +511,10 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 tc::mma_commit(bar(L::O_FULL + b));
                 if (last) tc::mma_commit(bar(L::KV_EMPTY + kbj));
             };
-            // S_cj reads Q tile qn (its stage qn % NQ) and frees the stage when
+            // S_cj reads the Q tile in stage qs and frees the stage when
             // release_q (the tile's last chunk)
-            auto issue_s = [&](int cj, int kbj, int qn, bool release_q) {
-                const int b = cj & 1, qs = qn % NQ;
+            auto issue_s = [&](int cj, int kbj, int qs, bool release_q) {
+                const int b = cj & 1;
                 tc::fence_after_sync();
                 const uint32_t qt = base + L::Q + qs * QS, ks = base + L::K + kbj * KS;
                 if constexpr (QK8) {
@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 if (release_q) tc::mma_commit(bar(L::Q_EMPTY + qs));
             };
             // polls until S_ci (if s_cj >= 0) and the pending PV are both issued
-            auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par, int qn, bool release_q) -> bool {
+            auto drive = [&](int s_cj, int kbj, bool need_kv, int kv_par, int qs, uint32_t q_par, bool release_q) -> bool {
                 bool s_done = s_cj < 0, pv_done = pv_ci < 0, kv_ok = !need_kv;
                 const uint64_t t0 = tc::global_ns();
                 for (uint32_t i = 0;; ++i) {
@@ -551,8 +551,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                     if (i > 0) __nanosleep(32);
                     if (!s_done) {
                         if (!kv_ok) kv_ok = tc::mbar_test(bar(L::KV_FULL + kbj), (uint32_t)kv_par);
-                        if (kv_ok && tc::mbar_test(bar(L::Q_FULL + qn % NQ), (qn / NQ) & 1)) {
-                            issue_s(s_cj, kbj, qn, release_q);
+                        if (kv_ok && tc::mbar_test(bar(L::Q_FULL + qs), q_par)) {
+                            issue_s(s_cj, kbj, qs, release_q);
                             s_done = true;
                         }
                     }
@@ -571,7 +571,8 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 return false;
             };
             // Q tiles as the loader issues them: one per chunk
-            int qn = -1;
+            int q_stage = 0;  // stage and phase parity of the next Q tile
+            uint32_t q_par = 0;
             Unit xnext{};
             if (u_begin < u_end) xnext = load_unit(p, u_begin);
             for (int u = u_begin; u < u_end && ok; u += u_step, ++ui) {
@@ -579,14 +580,17 @@ __global__ void __launch_bounds__(tck::kThreads, 1)
                 if (u + u_step < u_end) xnext = load_unit(p, u + u_step);
                 const int kb = ui % NKV;
                 for (int c = 0; c < x.nch && ok; ++c, ++ci) {
-                    ++qn;
-                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1, qn, true);
+                    ok = drive(ci, kb, c == 0, (ui / NKV) & 1, q_stage, q_par, true);
+                    if (++q_stage == NQ) {
+                        q_stage = 0;
+                        q_par ^= 1u;
+                    }
                     pv_ci = ci;
                     pv_kb = kb;
                     pv_last = (c == x.nch - 1);
                 }
             }
-            if (ok && pv_ci >= 0) drive(-1, 0, false, 0, 0, false);
+            if (ok && pv_ci >= 0) drive(-1, 0, false, 0, 0, 0u, false);
             // all issued MMAs complete before tensor memory is released
             tc::mma_commit(bar(L::DRAIN));
             volatile int dummy = 0;
