@@ -60,6 +60,7 @@ PROFILED_TRAFFIC: dict = {
     "a80da73977f45668": 1.0778e10,  # 2.24 GB read + 8.54 GB written
     "362d894189bb3b67": 1.0715e10,  # 2.18 GB read + 8.54 GB written
     "c932c9210ba72cff": 1.0688e10,  # 2.15 GB read + 8.54 GB written
+    "d7e317ae04c8bfe8": 1.0686e10,  # 2.15 GB read + 8.54 GB written
 }
 
 
