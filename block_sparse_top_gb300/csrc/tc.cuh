@@ -67,9 +67,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait: gives up after kWaitLimitNs, raises the CTA abort flag and
 // the device status bit so every role can drain and exit; returns false at
 // once when another role has raised the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort_flag, uint32_t *status,
-                                          uint32_t status_bit) {
-    if (mbar_try_wait(addr, parity)) return true;
+// The polling loop of mbar_wait, out of line: a wait that does not complete at
+// its first try costs far more than the call, and every call site stays small.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, volatile int *abort_flag,
+                                                   uint32_t *status, uint32_t status_bit) {
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(addr, parity)) return true;
@@ -81,6 +82,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volati
     *abort_flag = 1;
     set_status(status, status_bit);
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, volatile int *abort_flag, uint32_t *status,
+                                          uint32_t status_bit) {
+    if (mbar_try_wait(addr, parity)) return true;
+    return mbar_wait_slow(addr, parity, abort_flag, status, status_bit);
 }
 
 // cp.async completion tracked by an mbarrier (no-increment arrive).
