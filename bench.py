@@ -61,6 +61,7 @@ PROFILED_TRAFFIC: dict = {
     "362d894189bb3b67": 1.0715e10,  # 2.18 GB read + 8.54 GB written
     "c932c9210ba72cff": 1.0688e10,  # 2.15 GB read + 8.54 GB written
     "d7e317ae04c8bfe8": 1.0686e10,  # 2.15 GB read + 8.54 GB written
+    "c328ed59c4f503f0": 1.0655e10,  # 2.12 GB read + 8.54 GB written
 }
 
 
