@@ -471,6 +471,8 @@ def run_ours(args, world, rank):
                              for c in OTHER_CONFIGS}
     if not args.no_decode:
         result["decode"] = decode_sweep(args, dev, peaks, peak_src)
+    if not args.no_variants:
+        result["variants"] = measure_variants(dev, args.config_steps, args.warmup, peaks, peak_src)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = oracle_rate(spec, x_cpu, args.cpu_budget)
     return result
@@ -541,6 +543,111 @@ def measure_config(spec, dev, steps, warmup, peaks, peak_src):
                         "peak_source": f"{peak_src} bf16 burst"},
            "step_frac_of_peak": round(flops / (step_ms * 1e-3) / 1e12 / peak, 4)}
     del x, k, v, csr, csr_ws, fwd_ws, out, lse, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+RAGGED_32K = synth.VarlenSpec("ragged_sink_32k", q_lens=(16384, 8192, 4096, 4096), k_lens=(16384, 8192, 4096, 4096),
+                              Hkv=4, qpk=16, topk=16, causal=True, pattern="sink")
+
+
+def measure_variants(dev, steps, warmup, peaks, peak_src):
+    """The other forward paths on the 32K causal sink workload (the same
+    inputs, so the same effective FLOP): ragged-batch entry point, e4m3 K/V,
+    e4m3 Q and K, fp16 / fp32 partials, temperature LSE; plus a ragged batch of
+    four sequences and the dense paged decode.  Each step is the CSR build and
+    one forward call, timed with CUDA events over `steps` back-to-back steps
+    (outputs of the ragged entry point come from PyTorch's caching allocator
+    inside the timed region)."""
+    import block_sparse_top_gb300 as msa
+    spec = synth.CAUSAL_SINK_32K
+    x = synth.make_prefill_inputs(spec, device=dev)
+    flops = prefill_flops(spec, x["q2k"])
+    peak = peaks["bf16_tflops"]
+    B, Sq, Hq, D = x["q"].shape
+    Skv, Hkv, qpk = spec.Skv, spec.Hkv, spec.qpk
+    q_v, k_v, v_v = x["q"].view(B * Sq, Hq, D), x["k"].view(B * Skv, Hkv, D), x["v"].view(B * Skv, Hkv, D)
+    q2k_v = x["q2k"][0].contiguous()  # [Hkv, Sq, topk]: one sequence
+    cu_q = torch.tensor([0, Sq], dtype=torch.int32, device=dev)
+    cu_k = torch.tensor([0, Skv], dtype=torch.int32, device=dev)
+    k8 = k_v.float().to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    v8 = v_v.float().to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    q8 = q_v.float().to(torch.float8_e4m3fn).contiguous()
+    csr, csr_ws = msa.csr_buffers(B, Hkv, Sq, Skv, spec.topk, qpk, dev)
+    fwd_ws = msa.fwd_workspace(B, Sq, Hq, spec.topk, dev)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((B, Sq, Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def time_steps(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def varlen(q, k, v, **kw):
+        c = msa.build_k2q_csr_varlen(q2k_v, cu_q, cu_k, Sq, Skv, qpk)
+        msa.sparse_attn_fwd_varlen(q, k, v, c, causal=True, **kw)
+
+    def uniform_fp8():
+        msa.build_k2q_csr(x["q2k"], Skv, qpk, out=csr, workspace=csr_ws)
+        msa.sparse_attn_fwd(x["q"], k8.view(B, Skv, Hkv, D), v8.view(B, Skv, Hkv, D), csr, causal=True,
+                            kv_format="fp8", workspace=fwd_ws, out=out, lse=lse)
+
+    res = {"workload": "causal_sink_32k (C2) unless named otherwise", "steps": steps, "warmup": warmup,
+           "peak": peak, "peak_source": f"{peak_src} bf16 burst"}
+
+    def rec(name, ms, fl=flops, note=None):
+        tf = fl / (ms * 1e-3) / 1e12
+        res[name] = {"ms_per_step": round(ms, 4), "TFLOP/s": round(tf, 3), "step_frac_of_peak": round(tf / peak, 4)}
+        if note:
+            res[name]["path"] = note
+
+    rec("varlen_entry_bf16", time_steps(lambda: varlen(q_v, k_v, v_v)), note="msa_build_k2q_csr_varlen + msa_sparse_attn_fwd_varlen, one sequence")
+    rec("e4m3_kv", time_steps(uniform_fp8), note="K/V as e4m3 bytes, staged to bf16 in the tile kernel")
+    rec("e4m3_qk", time_steps(lambda: varlen(q8, k8, v8, kv_format="fp8")), note="S = Q K^T as an e4m3 MMA, PV in bf16")
+    rec("partials_fp16", time_steps(lambda: varlen(q_v, k_v, v_v, partial_dtype=msa.MSA_PARTIAL_FP16)))
+    rec("partials_fp32", time_steps(lambda: varlen(q_v, k_v, v_v, partial_dtype=msa.MSA_PARTIAL_FP32)))
+    rec("temperature_lse", time_steps(lambda: varlen(q_v, k_v, v_v, lse_temperature_scale=2.0)), note="lse_temperature_scale 2")
+    del x, q_v, k_v, v_v, k8, v8, q8, csr, csr_ws, fwd_ws, out, lse
+    torch.cuda.empty_cache()
+    # a ragged batch: four causal sink sequences, 32K queries in all
+    r = RAGGED_32K
+    xr = synth.make_varlen_inputs(r, device=dev)
+    fl_r, q0 = 0.0, 0
+    for n_q, n_k in zip(r.q_lens, r.k_lens):
+        q2k_s = xr["q2k"][:, q0:q0 + n_q].unsqueeze(0)
+        vis = visible_keys(q2k_s, n_q, torch.tensor([n_k], device=dev), r.causal)
+        fl_r += 4.0 * r.D * r.qpk * float(vis.sum())
+        q0 += n_q
+
+    def ragged():
+        c = msa.build_k2q_csr_varlen(xr["q2k"], xr["cu_seqlens_q"], xr["cu_seqlens_k"], max(r.q_lens), max(r.k_lens),
+                                     r.qpk)
+        msa.sparse_attn_fwd_varlen(xr["q"], xr["k"], xr["v"], c, causal=True)
+
+    rec("ragged_sink_32k", time_steps(ragged), fl=fl_r,
+        note=f"{r.B} sequences of {'/'.join(str(n) for n in r.q_lens)} queries and keys, Hkv {r.Hkv}, qhead_per_kv {r.qpk}, topk {r.topk}")
+    del xr
+    torch.cuda.empty_cache()
+    # the dense paged decode (no selection: every block of each sequence)
+    ds = synth.paged_decode_spec(32768)
+    d = synth.make_decode_inputs(ds, device=dev)
+    su = d["seqused"].to(torch.int64).cpu()
+    kv_bytes = sum(int(su[b]) * ds.Hkv * ds.D * 2 * 2 for b in range(ds.B))
+    dbytes = float(kv_bytes + 2 * ds.B * ds.Sq * ds.Hq * ds.D * 2 + ds.B * ds.Sq * ds.Hq * 4)
+    ms_d = time_steps(lambda: msa.paged_attn_fwd(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seqused"], None))
+    gbs = dbytes / (ms_d * 1e-3) / 1e9
+    res["dense_decode_32k"] = {"us_per_call": round(ms_d * 1e3, 2), "GB/s": round(gbs, 1),
+                               "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": dbytes,
+                               "path": "msa_paged_attn_fwd with q2k NULL: B 32, Sq 8, Hkv 4, qhead_per_kv 16, 32K keys"}
+    del d
     torch.cuda.empty_cache()
     return res
 
@@ -654,6 +761,8 @@ def main():
     ap.add_argument("--decode-L", type=int, nargs="*", default=list(synth.DECODE_SWEEP_L))
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other prefill workloads")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the other forward paths (ragged batches, e4m3, partial types, temperature LSE, dense decode)")
     ap.add_argument("--decode-only", action="store_true",
                     help="run only the paged-decode sweep (for profiling its kernels); prints its JSON")
     ap.add_argument("--config-steps", type=int, default=10)
