@@ -558,7 +558,8 @@ def measure_variants(dev, steps, warmup, peaks, peak_src):
     four sequences and the dense paged decode.  Each step is the CSR build and
     one forward call, timed with CUDA events over `steps` back-to-back steps
     (outputs of the ragged entry point come from PyTorch's caching allocator
-    inside the timed region)."""
+    inside the timed region; the CSR row count is passed in, as a caller that
+    knows its batch would, so no call reads cu_seqlens back)."""
     import block_sparse_top_gb300 as msa
     spec = synth.CAUSAL_SINK_32K
     x = synth.make_prefill_inputs(spec, device=dev)
@@ -591,8 +592,10 @@ def measure_variants(dev, steps, warmup, peaks, peak_src):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / steps
 
+    rows_1 = (Skv + 127) // 128  # the row count, known on the host (no read-back of cu_seqlens per call)
+
     def varlen(q, k, v, **kw):
-        c = msa.build_k2q_csr_varlen(q2k_v, cu_q, cu_k, Sq, Skv, qpk)
+        c = msa.build_k2q_csr_varlen(q2k_v, cu_q, cu_k, Sq, Skv, qpk, total_rows=rows_1)
         msa.sparse_attn_fwd_varlen(q, k, v, c, causal=True, **kw)
 
     def uniform_fp8():
@@ -627,9 +630,11 @@ def measure_variants(dev, steps, warmup, peaks, peak_src):
         fl_r += 4.0 * r.D * r.qpk * float(vis.sum())
         q0 += n_q
 
+    rows_r = sum((n + 127) // 128 for n in r.k_lens)
+
     def ragged():
         c = msa.build_k2q_csr_varlen(xr["q2k"], xr["cu_seqlens_q"], xr["cu_seqlens_k"], max(r.q_lens), max(r.k_lens),
-                                     r.qpk)
+                                     r.qpk, total_rows=rows_r)
         msa.sparse_attn_fwd_varlen(xr["q"], xr["k"], xr["v"], c, causal=True)
 
     rec("ragged_sink_32k", time_steps(ragged), fl=fl_r,
